@@ -1,0 +1,269 @@
+"""Thin Python binding of libpw.so, the fused mixed-precision APL MoE layer
+for GB300 (sm_103a).
+
+The functions keep the C ABI's names (pw_pack, pw_set_commit, pw_reload_async,
+pw_moe_forward, ...) and only marshal arguments: torch tensors become raw
+pointers, the current torch stream becomes the CUDA stream.  Every step of the
+layer runs in the library's own kernels; there is no fallback path, and every
+entry point raises if the library has not been built.
+
+PyTorch supplies device memory (plane pages, tables, descriptors, workspace)
+and streams; the library allocates none of its own.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpw.so")
+
+PW_OK = 0
+PW_EINVAL = -1
+PW_ECUDA = -2
+PW_ENOTRESIDENT = -3
+PW_ERELOAD = -4
+PW_ETIMEOUT = -5
+PW_ENOMEM = -6
+PW_EDEVICE = -7
+PW_STATUS_NAN_LOGIT = 1
+PW_STATUS_TIMEOUT = 2
+PW_STATUS_BAD_DESC = 4
+KIND_GATE_UP = 0
+KIND_DOWN = 1
+MAX_BITS = 8
+
+_lib = None
+
+_sz = ctypes.c_size_t
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_pi = ctypes.POINTER(ctypes.c_int)
+
+_SIGS = {
+    "pw_last_error": (ctypes.c_char_p, []),
+    "pw_plane_bytes": (_sz, [_i, _i]),
+    "pw_lut_bytes": (_sz, [_i, _i, _i]),
+    "pw_lut_offset": (_sz, [_i, _i, _i]),
+    "pw_pack": (_i, [_vp, _i, _i, _i, _vp, _i, _vp, _vp]),
+    "pw_desc_bytes": (_sz, [_i, _i]),
+    "pw_table_create": (_i, [ctypes.POINTER(_vp), _i, _i, _i, _i, _vp, _sz, _vp]),
+    "pw_block_register": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, ctypes.POINTER(_vp), _vp, _i, _vp]),
+    "pw_set_commit": (_i, [_vp, _i, _i, _i, _i, _vp]),
+    "pw_reload_async": (_i, [_vp, _i, _i, _i, _i, _vp]),
+    "pw_reload_query": (_i, [_vp, _i, _i, _i]),
+    "pw_block_state": (_i, [_vp, _i, _i, _i, _pi, _pi, _pi]),
+    "pw_table_destroy": (_i, [_vp]),
+    "pw_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "pw_moe_forward": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "pw_moe_forward_host": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
+    "pw_workspace_status": (_i, [_vp, _vp, _pi]),
+}
+
+
+class PWError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{msg} (status {code})")
+        self.code = code
+
+
+def lib():
+    """Loads libpw.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+                               "(python -m any_precision_weight_gb300.build)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def exported_symbols():
+    return sorted(_SIGS)
+
+
+def _check(rc: int, what: str) -> int:
+    if rc < 0:
+        raise PWError(rc, f"{what}: {lib().pw_last_error().decode()}")
+    return rc
+
+
+def _ptr(t):
+    """Address of a torch tensor or numpy array (None stays NULL)."""
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+# ----------------------------------------------------------------------------- format
+
+def pw_plane_bytes(R: int, K: int) -> int:
+    return lib().pw_plane_bytes(R, K)
+
+
+def pw_lut_bytes(R: int, b_min: int, n_bits: int) -> int:
+    return lib().pw_lut_bytes(R, b_min, n_bits)
+
+
+def pw_lut_offset(R: int, b_min: int, b: int) -> int:
+    return lib().pw_lut_offset(R, b_min, b)
+
+
+def pw_pack(idx: np.ndarray, parent_lut: np.ndarray, n_bits: int = 8, b_min: int = 3,
+            planes_out=None, luts_out=None):
+    """Packs uint8 parent indices [R][K] and the fp16 parent table [R][2^n].
+
+    Returns (planes uint32 [n][R][K/32], luts uint16 flat) as numpy arrays, or
+    fills the given host buffers (numpy arrays over any host memory).
+    """
+    idx = np.ascontiguousarray(idx, dtype=np.uint8)
+    par = np.ascontiguousarray(parent_lut, dtype=np.float16).view(np.uint16)
+    R, K = idx.shape
+    if planes_out is None:
+        planes_out = np.empty((n_bits, R, K // 32), dtype=np.uint32)
+    if luts_out is None:
+        luts_out = np.empty(pw_lut_bytes(R, b_min, n_bits) // 2, dtype=np.uint16)
+    _check(lib().pw_pack(_ptr(idx), R, K, n_bits, _ptr(par), b_min, _ptr(planes_out),
+                         _ptr(luts_out)), "pw_pack")
+    return planes_out, luts_out
+
+
+# ----------------------------------------------------------------------------- page table
+
+class PagedMoE:
+    """Owns the device memory of one model's MoE blocks and the C page table.
+
+    Plane pages, tables and descriptors are torch CUDA tensors; host backing
+    copies are pinned torch CPU tensors.  Only the pages a block may use
+    (``alloc_planes``) are allocated on the device.
+    """
+
+    def __init__(self, n_layers: int, n_experts: int, H: int, I: int, device="cuda", stream=None):
+        import torch
+        self.L, self.E, self.H, self.I = n_layers, n_experts, H, I
+        self.device = torch.device(device)
+        nb = lib().pw_desc_bytes(n_layers, n_experts)
+        self._desc = torch.zeros(nb + 128, dtype=torch.uint8, device=self.device)
+        base = self._desc.data_ptr()
+        self._desc_ptr = base + ((-base) % 128)
+        h = _vp()
+        _check(lib().pw_table_create(ctypes.byref(h), n_layers, n_experts, H, I, self._desc_ptr, nb,
+                                     _stream(stream)), "pw_table_create")
+        self._t = h
+        self._keep = {}
+
+    def rows_cols(self, kind: int):
+        return (2 * self.I, self.H) if kind == KIND_GATE_UP else (self.H, self.I)
+
+    def register(self, layer: int, expert: int, kind: int, planes_host, luts_host, q_init: int,
+                 n_bits: int = 8, b_min: int = 3, alloc_planes: int | None = None, stream=None):
+        """planes_host / luts_host: pinned torch CPU tensors (or numpy arrays) in
+        pw_pack layout; kept alive by this object."""
+        import torch
+        R, K = self.rows_cols(kind)
+        pb = pw_plane_bytes(R, K)
+        na = n_bits if alloc_planes is None else max(q_init, min(alloc_planes, n_bits))
+        pages = torch.empty(na * pb, dtype=torch.uint8, device=self.device)
+        luts = torch.empty(pw_lut_bytes(R, b_min, n_bits), dtype=torch.uint8, device=self.device)
+        ptrs = (_vp * n_bits)(*[pages.data_ptr() + p * pb if p < na else None for p in range(n_bits)])
+        _check(lib().pw_block_register(self._t, layer, expert, kind, n_bits, b_min, _ptr(planes_host),
+                                       _ptr(luts_host), ptrs, luts.data_ptr(), q_init, _stream(stream)),
+               "pw_block_register")
+        self._keep[(layer, expert, kind)] = (pages, luts, planes_host, luts_host)
+
+    def pages(self, layer, expert, kind):
+        """(device plane pages tensor, device table tensor) of one block."""
+        return self._keep[(layer, expert, kind)][:2]
+
+    def device_bytes(self) -> int:
+        return sum(v[0].numel() + v[1].numel() for v in self._keep.values())
+
+    def pw_set_commit(self, layer, expert, kind, q, stream=None):
+        return _check(lib().pw_set_commit(self._t, layer, expert, kind, q, _stream(stream)),
+                      "pw_set_commit")
+
+    def pw_reload_async(self, layer, expert, kind, q_target, stream=None):
+        return _check(lib().pw_reload_async(self._t, layer, expert, kind, q_target, _stream(stream)),
+                      "pw_reload_async")
+
+    def pw_reload_query(self, layer, expert, kind) -> int:
+        return _check(lib().pw_reload_query(self._t, layer, expert, kind), "pw_reload_query")
+
+    def pw_block_state(self, layer, expert, kind):
+        q, res, tgt = _i(), _i(), _i()
+        _check(lib().pw_block_state(self._t, layer, expert, kind, ctypes.byref(q), ctypes.byref(res),
+                                    ctypes.byref(tgt)), "pw_block_state")
+        return q.value, res.value, tgt.value
+
+    def workspace(self, T: int, top_k: int):
+        import torch
+        nb = lib().pw_workspace_bytes(T, self.E, top_k, self.H, self.I)
+        return torch.empty(max(nb, 256), dtype=torch.uint8, device=self.device)
+
+    def pw_moe_forward(self, layer, x, logits, top_k, renorm, residual=None, out=None, ws=None,
+                       routing=False, stream=None):
+        """x [T][H] fp16 and logits [T][E] fp32 CUDA tensors.  Returns out, or
+        (out, topk_idx, topk_w, offsets, perm) with routing=True."""
+        import torch
+        T = x.shape[0]
+        assert x.dtype == torch.float16 and logits.dtype == torch.float32
+        assert x.is_contiguous() and logits.is_contiguous()
+        if out is None:
+            out = torch.empty_like(x)
+        if ws is None:
+            ws = self.workspace(T, top_k)
+        ri = rw = ro = rp = None
+        if routing:
+            ri = torch.empty((T, top_k), dtype=torch.int32, device=x.device)
+            rw = torch.empty((T, top_k), dtype=torch.float32, device=x.device)
+            ro = torch.empty((self.E + 1,), dtype=torch.int32, device=x.device)
+            rp = torch.empty((T * top_k,), dtype=torch.int32, device=x.device)
+        _check(lib().pw_moe_forward(self._t, layer, _ptr(x), _ptr(logits), T, top_k, int(renorm),
+                                    _ptr(residual), _ptr(out), _ptr(ri), _ptr(rw), _ptr(ro), _ptr(rp),
+                                    _ptr(ws), ws.numel(), _stream(stream)), "pw_moe_forward")
+        return (out, ri, rw, ro, rp) if routing else out
+
+    def pw_moe_forward_host(self, layer, x_host, logits_host, top_k, renorm, out_host,
+                            residual_host=None, ws=None, stream=None):
+        """Host (pinned) inputs and output; synchronises the stream."""
+        T = x_host.shape[0]
+        if ws is None:
+            ws = self.workspace(T, top_k)
+        _check(lib().pw_moe_forward_host(self._t, layer, _ptr(x_host), _ptr(logits_host), T, top_k,
+                                         int(renorm), _ptr(residual_host), _ptr(out_host), _ptr(ws),
+                                         ws.numel(), _stream(stream)), "pw_moe_forward_host")
+        return out_host
+
+    @staticmethod
+    def workspace_status(ws, stream=None) -> int:
+        st = _i()
+        _check(lib().pw_workspace_status(_ptr(ws), _stream(stream), ctypes.byref(st)),
+               "pw_workspace_status")
+        return st.value
+
+    def close(self):
+        if getattr(self, "_t", None):
+            lib().pw_table_destroy(self._t)
+            self._t = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,238 @@
+/*
+ * pw.h -- C ABI of the fused mixed-precision APL MoE expert layer (GB300, sm_103a).
+ *
+ * Method: PagedWeight ("PagedWeight: Efficient MoE LLM Serving with Dynamic
+ * Quality-Aware Weight Quantization").  Its technical summary's core components
+ * name the pieces behind these calls:
+ *   - section 1 "Paged Weight Representation": one unit per (layer, expert,
+ *     gate_up|down) linear block; weights in APL's layered bit-plane format with
+ *     associated lookup tables; a weight page table holding the desired (d_i) and
+ *     committed (q_i) bitwidth of every block; pages resident on the GPU, on the
+ *     CPU, or in transfer;
+ *   - section 3 "Asynchronous Page Movement": pages reloaded asynchronously, a
+ *     bitwidth commit applied only at a safe boundary so that inference never
+ *     stops;
+ *   - section 3 "Fused Mixed-Precision Kernel": one fused operation that reads
+ *     bit-planes and tables directly, with a different bitwidth per block.
+ *
+ * Bit-plane layout (fixed by this library; the pages print none):
+ *   parent index P[r][k] in [0, 2^n); plane p (p = 0 most significant) holds bit
+ *   (n-1-p) of P; planes are stored plane-major per block, planes[p][r][K/32] as
+ *   uint32, bit j of word w holding element k = 32w + j.  A b-bit weight uses the
+ *   top b planes (index P >> (n-b)) and the row's own 2^b-entry fp16 table LUT_b.
+ *   Each plane of a block is one page of R*K/8 bytes, so the planes below the
+ *   committed bitwidth form a tail that can live on the CPU and be reloaded.
+ *
+ * Block shapes: gate_up has R = 2I rows (rows [0, I) gate, [I, 2I) up) and
+ * K = H columns; down has R = H rows and K = I columns.  H, I multiples of 32.
+ *
+ * Conventions for every call:
+ *   - returns PW_OK (0) or a negative PW_E* status; nothing throws or exits;
+ *     pw_last_error() gives a message for the last failure on this thread;
+ *   - fp16 values are passed as uint16_t bit patterns or void*;
+ *   - the library allocates no device memory: the caller owns every device
+ *     buffer (plane pages, tables, descriptor array, workspace) and every stream;
+ *     the library owns only the small host-side table object;
+ *   - "device" pointers are CUDA device addresses on the current device; "host"
+ *     pointers are CPU addresses (pinned where stated).
+ */
+#ifndef PW_H
+#define PW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define PW_OK            0
+#define PW_EINVAL       (-1)  /* bad argument, shape or state                     */
+#define PW_ECUDA        (-2)  /* a CUDA runtime call or kernel launch failed      */
+#define PW_ENOTRESIDENT (-3)  /* commit above the resident planes, no reload      */
+#define PW_ERELOAD      (-4)  /* the reload this commit waits for has failed      */
+#define PW_ETIMEOUT     (-5)  /* a bounded wait ran out                           */
+#define PW_ENOMEM       (-6)  /* host allocation failed or workspace too small    */
+#define PW_EDEVICE      (-7)  /* a kernel reported an error through the workspace */
+
+/* Bits of the device status word (pw_workspace_status). */
+#define PW_STATUS_NAN_LOGIT  1  /* a router logit was NaN (treated as -inf)     */
+#define PW_STATUS_TIMEOUT    2  /* a bounded device-side wait gave up           */
+#define PW_STATUS_BAD_DESC   4  /* an active block had no usable descriptor     */
+
+#define PW_KIND_GATE_UP 0
+#define PW_KIND_DOWN    1
+#define PW_MAX_BITS     8
+
+typedef struct CUstream_st* pw_stream_t;   /* a cudaStream_t; NULL = default stream */
+typedef struct pw_table pw_table;          /* opaque host-side page table           */
+
+/* Message for the last failing call on this thread ("" if none). */
+const char* pw_last_error(void);
+
+/* ------------------------------------------------------------------ format (host) */
+
+/* Bytes of one plane page of an R x K block: R*K/8. */
+size_t pw_plane_bytes(int R, int K);
+
+/* Bytes of the concatenated tables LUT_b, b = b_min..n_bits, each [R][2^b] fp16. */
+size_t pw_lut_bytes(int R, int b_min, int n_bits);
+
+/* Byte offset of LUT_b inside that concatenation (b_min <= b). */
+size_t pw_lut_offset(int R, int b_min, int b);
+
+/*
+ * pw_pack -- bit-plane packer and table builder (host, CPU threads).
+ * Source: "Paged Weight Representation" (layered bit-planes with associated
+ * lookup tables).
+ *   idx        host [R][K] uint8 parent indices, each < 2^n_bits
+ *   parent_lut host [R][2^n_bits] fp16 table of the parent (n_bits-bit) weights
+ *   planes_out host [n_bits][R][K/32] uint32, written in the layout above
+ *   luts_out   host, pw_lut_bytes(R, b_min, n_bits) bytes: LUT_b for b = b_min..n_bits.
+ *              LUT_n is the parent table; for b < n, LUT_b[r][j] is the mean of the
+ *              2^(n-b) parent entries whose top b index bits equal j, computed in
+ *              fp64 and rounded once to fp16 (nearest, ties to even).
+ * Requirements: R >= 1, K >= 32, K % 32 == 0, 1 <= b_min <= n_bits <= 8.
+ * Errors: PW_EINVAL for a bad shape, a null pointer or an index >= 2^n_bits
+ * (nothing is guaranteed about the outputs then).
+ */
+int pw_pack(const uint8_t* idx, int R, int K, int n_bits, const uint16_t* parent_lut,
+            int b_min, uint32_t* planes_out, uint16_t* luts_out);
+
+/* ------------------------------------------------------------------ page table */
+
+/* Bytes of the device descriptor array for n_layers x n_experts x 2 blocks. */
+size_t pw_desc_bytes(int n_layers, int n_experts);
+
+/*
+ * pw_table_create -- the weight page table ("Paged Weight Representation":
+ * per-block desired d_i and committed q_i).
+ *   d_desc      device memory of at least pw_desc_bytes(n_layers, n_experts) bytes,
+ *               128-byte aligned, owned by the caller, alive until pw_table_destroy.
+ *               The kernels read each block's committed q_i and page addresses from
+ *               it, so a commit needs no recompile and no host round trip.
+ *   n_experts   1..256;  H, I: hidden and expert-intermediate sizes (multiples of 32).
+ *   s           stream on which the descriptors are cleared (asynchronous).
+ * Errors: PW_EINVAL (shapes, small or misaligned buffer), PW_ECUDA, PW_ENOMEM.
+ */
+int pw_table_create(pw_table** out, int n_layers, int n_experts, int H, int I,
+                    void* d_desc, size_t desc_bytes, pw_stream_t s);
+
+/*
+ * pw_block_register -- attach one linear block (layer, expert, kind).
+ *   host_planes  host [n_bits][R][K/32] uint32 (pw_pack output), the backing store
+ *                of every plane; pinned memory makes later reloads asynchronous.
+ *                Must stay valid until pw_table_destroy.
+ *   host_luts    host tables as written by pw_pack; same lifetime rule.
+ *   d_plane_pages n_bits device pointers, page p holding plane p (R*K/8 bytes,
+ *                16-byte aligned).  Pages for p >= q_init may be NULL if the block
+ *                will never be reloaded that far.
+ *   d_luts       device memory of pw_lut_bytes(R, b_min, n_bits) bytes (16-byte
+ *                aligned) holding the tables in the pw_pack layout.
+ *   q_init       committed bitwidth, b_min <= q_init <= n_bits.  Planes [0, q_init)
+ *                and tables b <= q_init are copied host->device on s, then the
+ *                descriptor is written on s; everything is ordered on s.
+ * Errors: PW_EINVAL, PW_ECUDA.
+ */
+int pw_block_register(pw_table* t, int layer, int expert, int kind, int n_bits, int b_min,
+                      const uint32_t* host_planes, const uint16_t* host_luts,
+                      void* const* d_plane_pages, void* d_luts, int q_init, pw_stream_t s);
+
+/*
+ * pw_reload_async -- bring planes [resident, q_target) and tables
+ * (resident, q_target] of one block from its host backing store to its device
+ * pages ("Asynchronous Page Movement").  Enqueues host->device copies on the
+ * copy stream and records an event after them; returns without waiting.  The
+ * copies touch only planes and tables that no kernel reads at the committed
+ * q <= resident, so they may overlap forward passes on another stream.
+ * q_target <= resident is a no-op.  One reload per block may be pending at a time.
+ * Errors: PW_EINVAL (q_target out of range, missing page, a reload already
+ * pending), PW_ECUDA (a copy could not be enqueued: the block is marked failed
+ * and a later commit above resident returns PW_ERELOAD).
+ */
+int pw_reload_async(pw_table* t, int layer, int expert, int kind, int q_target,
+                    pw_stream_t copy);
+
+/*
+ * pw_reload_query -- non-blocking completion check of a block's pending reload.
+ * Returns 1 when the reload has completed (or none is pending), 0 while it is
+ * in flight, PW_ERELOAD if it failed.
+ */
+int pw_reload_query(pw_table* t, int layer, int expert, int kind);
+
+/*
+ * pw_set_commit -- commit bitwidth q for one block at a stream-ordered safe
+ * boundary ("bitwidth commits only at safe boundaries").  The descriptor write
+ * is enqueued on the compute stream: forward passes enqueued on it before this
+ * call read the old q, those after read q.  Raising q above the resident planes
+ * requires a pending or completed reload to >= q: the compute stream then first
+ * waits on the reload's event (no host wait).  Lowering q needs no copy.
+ * Errors: PW_EINVAL (q outside [b_min, n_bits]), PW_ENOTRESIDENT (q above the
+ * resident planes and no reload to q), PW_ERELOAD (that reload failed; q is
+ * unchanged), PW_ECUDA.
+ */
+int pw_set_commit(pw_table* t, int layer, int expert, int kind, int q, pw_stream_t compute);
+
+/* Host view of one block: committed q, resident planes, pending reload target (0 if none). */
+int pw_block_state(pw_table* t, int layer, int expert, int kind, int* q, int* resident,
+                   int* reload_target);
+
+/* Destroys the host object (after synchronising its pending reload events). */
+int pw_table_destroy(pw_table* t);
+
+/* ------------------------------------------------------------------ forward */
+
+/* Bytes of device workspace pw_moe_forward needs (and pw_moe_forward_host). */
+size_t pw_workspace_bytes(int T, int E, int top_k, int H, int I);
+
+/*
+ * pw_moe_forward -- one fused MoE expert layer ("Fused Mixed-Precision Kernel"):
+ * top-k softmax routing, token->expert permutation (stable counting sort with
+ * per-expert offsets), per-block-bitwidth dequantised gate_up GEMV/GEMM with
+ * SiLU(gate)*up, down GEMV/GEMM, and the routing-weighted combine.
+ *   x        device [T][H] fp16 tokens (16-byte aligned)
+ *   logits   device [T][E] fp32 router logits (E = the table's n_experts)
+ *   top_k    1 <= top_k <= E;  renorm: nonzero divides the top-k weights by their sum
+ *   residual device [T][H] fp16 or NULL: added to the combined output
+ *   out      device [T][H] fp16: residual + sum_j w[t][j] * y(t, j), rounded once
+ *   topk_idx, topk_w  device [T][top_k] int32 / fp32 or NULL: experts in descending
+ *            logit order (ties to the lower index) and their weights
+ *   offsets  device [E+1] int32 or NULL: per-expert start of the permuted pairs
+ *   perm     device [T*top_k] int32 or NULL: pair ids t*top_k+j in (expert, token) order
+ *   workspace device, >= pw_workspace_bytes(T, E, top_k, H, I) bytes, 256-byte aligned;
+ *            must not be shared by two calls in flight at once.
+ * Every block (layer, e, kind) must be registered.  The call only enqueues work on
+ * `compute` and never waits.  Arithmetic: fp16 in, fp32 accumulate, h kept in fp16,
+ * y in fp32, out rounded to fp16.  A NaN logit is reported through the workspace
+ * status word (see pw_workspace_status), not through the return value.
+ * Errors: PW_EINVAL (shapes, unregistered block, misaligned pointer), PW_ENOMEM
+ * (workspace too small), PW_ECUDA.
+ */
+int pw_moe_forward(pw_table* t, int layer, const void* x, const float* logits, int T,
+                   int top_k, int renorm, const void* residual, void* out,
+                   int32_t* topk_idx, float* topk_w, int32_t* offsets, int32_t* perm,
+                   void* workspace, size_t ws_bytes, pw_stream_t compute);
+
+/*
+ * pw_moe_forward_host -- the same layer with HOST inputs and output: copies x,
+ * logits (and residual) host->device into the workspace on `compute`, runs
+ * pw_moe_forward, copies out device->host, and synchronises `compute` before
+ * returning.  Host buffers should be pinned for full copy speed.
+ * Errors: as pw_moe_forward, plus PW_EDEVICE when a kernel set a status bit.
+ */
+int pw_moe_forward_host(pw_table* t, int layer, const void* x_host, const float* logits_host,
+                        int T, int top_k, int renorm, const void* residual_host,
+                        void* out_host, void* workspace, size_t ws_bytes, pw_stream_t compute);
+
+/*
+ * pw_workspace_status -- reads the device status word of a workspace after the
+ * work already on stream s (synchronises s).  *status is 0 or an OR of the
+ * PW_STATUS_* bits set by the last forward that used this workspace.
+ */
+int pw_workspace_status(const void* workspace, pw_stream_t s, int* status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PW_H */

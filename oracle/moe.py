@@ -126,15 +126,18 @@ class Block:
         return apl.dequant(P, lut, self.q, self.n)
 
 
-def layer(x, logits, k, renorm, blocks, residual=None, out_rows=None):
+def layer(x, logits, k, renorm, blocks, residual=None, out_rows=None, out_tokens=None):
     """The whole layer.
 
     ``blocks(e)`` returns (gate_up Block, down Block) for expert e.
     ``out_rows``: optional list of hidden indices; when given, only those
     output columns are computed (h is still computed in full, as it must be).
+    ``out_tokens``: optional list of tokens; when given, routing and the
+    permutation still cover every token, but the expert MLPs and the combine
+    run only for the pairs of these tokens, and ``out`` has their rows.
     Returns a dict with idx, w, counts, offsets, perm, inv, h (per pair, in
-    perm order), y (per pair, in perm order, restricted to out_rows) and out
-    [T][len(out_rows) or H].
+    perm order; zero for pairs not computed), y (same, restricted to
+    out_rows) and out [len(out_tokens) or T][len(out_rows) or H].
     """
     x = np.asarray(x, dtype=np.float16).astype(np.float64)
     T, H = x.shape
@@ -142,24 +145,28 @@ def layer(x, logits, k, renorm, blocks, residual=None, out_rows=None):
     idx, w = route(logits, k, renorm)
     counts, offsets, perm, inv = permute(idx, E)
     cols = np.arange(H) if out_rows is None else np.asarray(out_rows)
+    toks_out = np.arange(T) if out_tokens is None else np.asarray(out_tokens)
+    wanted = np.zeros(T, dtype=bool)
+    wanted[toks_out] = True
     h_all = None
     y_all = np.zeros((T * k, len(cols)), dtype=np.float64)
     for e in range(E):
-        if counts[e] == 0:
+        pos = np.arange(offsets[e], offsets[e + 1])
+        pos = pos[wanted[perm[pos] // k]]
+        if len(pos) == 0:
             continue
-        pairs = perm[offsets[e]:offsets[e + 1]]
-        toks = pairs // k
+        toks = perm[pos] // k
         gu, dn = blocks(e)
         h = expert_h(gu.weights(), x[toks])
         if h_all is None:
             h_all = np.zeros((T * k, h.shape[1]), dtype=np.float64)
-        h_all[offsets[e]:offsets[e + 1]] = h
-        y_all[offsets[e]:offsets[e + 1]] = expert_y(dn.weights(cols), h)
-    out = np.zeros((T, len(cols)), dtype=np.float64)
+        h_all[pos] = h
+        y_all[pos] = expert_y(dn.weights(cols), h)
+    out = np.zeros((len(toks_out), len(cols)), dtype=np.float64)
     if residual is not None:
-        out += np.asarray(residual, dtype=np.float16).astype(np.float64)[:, cols]
-    for t in range(T):
+        out += np.asarray(residual, dtype=np.float16).astype(np.float64)[toks_out][:, cols]
+    for i, t in enumerate(toks_out):
         for j in range(k):
-            out[t] += w[t, j] * y_all[inv[t * k + j]]
+            out[i] += w[t, j] * y_all[inv[t * k + j]]
     return dict(idx=idx, w=w, counts=counts, offsets=offsets, perm=perm, inv=inv,
                 h=h_all, y=y_all, out=out)

@@ -132,6 +132,9 @@ def test_layer_brute_force_tiny(renorm):
     cols = [0, 5, 31]
     part = moe.layer(x, L, k, renorm, lambda e: blocks[e], out_rows=cols)
     assert np.allclose(part["out"], got["out"][:, cols], rtol=1e-14, atol=0)
+    # and sampled tokens
+    part = moe.layer(x, L, k, renorm, lambda e: blocks[e], out_rows=cols, out_tokens=[2, 0])
+    assert np.allclose(part["out"], got["out"][[2, 0]][:, cols], rtol=1e-14, atol=0)
 
 
 def test_layer_hand_case():
