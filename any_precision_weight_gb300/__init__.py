@@ -56,10 +56,12 @@ _SIGS = {
     "pw_reload_query": (_i, [_vp, _i, _i, _i]),
     "pw_block_state": (_i, [_vp, _i, _i, _i, _pi, _pi, _pi]),
     "pw_table_destroy": (_i, [_vp]),
+    "pw_debug_fail_next_reload": (_i, [_vp]),
     "pw_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "pw_moe_forward": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "pw_moe_forward_host": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "pw_workspace_status": (_i, [_vp, _vp, _pi]),
+    "pw_profile_attach": (_i, [ctypes.POINTER(_vp), _i]),
 }
 
 
@@ -144,6 +146,15 @@ def pw_pack(idx: np.ndarray, parent_lut: np.ndarray, n_bits: int = 8, b_min: int
     return planes_out, luts_out
 
 
+def pw_profile_attach(events):
+    """Next pw_moe_forward on this thread records these 5 torch.cuda.Events at its
+    kernel boundaries (before routing, after routing, gate_up, down, combine)."""
+    if not events:
+        return lib().pw_profile_attach(None, 0)
+    arr = (_vp * len(events))(*[e.cuda_event for e in events])
+    return _check(lib().pw_profile_attach(arr, len(events)), "pw_profile_attach")
+
+
 # ----------------------------------------------------------------------------- page table
 
 class PagedMoE:
@@ -210,6 +221,9 @@ class PagedMoE:
         _check(lib().pw_block_state(self._t, layer, expert, kind, ctypes.byref(q), ctypes.byref(res),
                                     ctypes.byref(tgt)), "pw_block_state")
         return q.value, res.value, tgt.value
+
+    def pw_debug_fail_next_reload(self):
+        return _check(lib().pw_debug_fail_next_reload(self._t), "pw_debug_fail_next_reload")
 
     def workspace(self, T: int, top_k: int):
         import torch

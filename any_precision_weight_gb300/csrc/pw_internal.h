@@ -93,6 +93,7 @@ struct ForwardArgs {
   int32_t* user_perm;
   unsigned char* ws;       // workspace base
   Workspace lay;
+  cudaEvent_t prof[5];     // boundary events (pw_profile_attach), or all null
 };
 
 // Kernel launchers (pw_kernels.cu).  Return cudaSuccess or the launch error.

@@ -324,14 +324,23 @@ static Fwd make_fwd(const ForwardArgs& a) {
   return p;
 }
 
+static inline void mark(const ForwardArgs& a, int i, cudaStream_t s) {
+  if (a.prof[i]) cudaEventRecord(a.prof[i], s);
+}
+
 cudaError_t launch_forward(const ForwardArgs& a, cudaStream_t s) {
   const Fwd p = make_fwd(a);
+  mark(a, 0, s);
   k_route_permute<<<1, kRouteThreads, 0, s>>>(p);
+  mark(a, 1, s);
   const int gx_gu = (p.I + kGemvWarps - 1) / kGemvWarps;
   const int gx_dn = (p.H + kGemvWarps - 1) / kGemvWarps;
   k_gemv_ref<PW_KIND_GATE_UP><<<dim3(min(gx_gu, 1024), p.E), kGemvWarps * 32, 0, s>>>(p);
+  mark(a, 2, s);
   k_gemv_ref<PW_KIND_DOWN><<<dim3(min(gx_dn, 1024), p.E), kGemvWarps * 32, 0, s>>>(p);
+  mark(a, 3, s);
   k_combine<<<dim3((p.H + 255) / 256, p.T), 256, 0, s>>>(p);
+  mark(a, 4, s);
   return cudaGetLastError();
 }
 

@@ -24,6 +24,7 @@
 namespace {
 
 thread_local std::string g_err;
+thread_local cudaEvent_t g_prof[5] = {};   // one-shot, see pw_profile_attach
 
 int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 int fail(int code, const char* fmt, ...) {
@@ -99,6 +100,7 @@ struct pw_table {
   pw::BlockDesc* d_desc = nullptr;
   std::vector<BlockState> blocks;
   std::mutex mu;
+  bool fail_next_reload = false;   // test hook, see pw_debug_fail_next_reload
 };
 
 namespace {
@@ -307,7 +309,13 @@ int pw_reload_async(pw_table* t, int layer, int expert, int kind, int q_target, 
   if (q_target < b->b_min || q_target > b->n_bits)
     return fail(PW_EINVAL, "pw_reload_async: q_target %d outside [%d, %d]", q_target, b->b_min,
                 b->n_bits);
-  if (b->pending) return fail(PW_EINVAL, "pw_reload_async: a reload of this block is pending");
+  if (b->pending && !b->failed)
+    return fail(PW_EINVAL, "pw_reload_async: a reload of this block is pending");
+  if (b->pending && b->failed) {     // retry after a failed reload: wait out its copies
+    if (b->ev) cudaEventSynchronize(b->ev);
+    b->pending = 0;
+    b->failed = false;
+  }
   if (q_target <= b->resident) return PW_OK;
   for (int p = b->resident; p < q_target; ++p)
     if (!b->pages[p]) return fail(PW_EINVAL, "pw_reload_async: no device page for plane %d", p);
@@ -319,6 +327,10 @@ int pw_reload_async(pw_table* t, int layer, int expert, int kind, int q_target, 
   b->failed = false;
   const size_t pb = pw_plane_bytes(b->R, b->K);
   cudaError_t e = cudaSuccess;
+  if (t->fail_next_reload) {          // injected failure: nothing is enqueued
+    t->fail_next_reload = false;
+    e = cudaErrorInvalidValue;
+  }
   for (int p = b->resident; p < q_target && e == cudaSuccess; ++p)
     e = cudaMemcpyAsync(b->pages[p], b->host_planes + p * (pb / 4), pb, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) {
@@ -392,6 +404,13 @@ int pw_block_state(pw_table* t, int layer, int expert, int kind, int* q, int* re
   return PW_OK;
 }
 
+int pw_debug_fail_next_reload(pw_table* t) {
+  if (!t) return fail(PW_EINVAL, "pw_debug_fail_next_reload: null table");
+  std::lock_guard<std::mutex> lk(t->mu);
+  t->fail_next_reload = true;
+  return PW_OK;
+}
+
 int pw_table_destroy(pw_table* t) {
   if (!t) return PW_OK;
   for (auto& b : t->blocks)
@@ -456,6 +475,10 @@ int pw_moe_forward(pw_table* t, int layer, const void* x, const float* logits, i
   a.user_perm = perm;
   a.ws = static_cast<unsigned char*>(workspace);
   a.lay = pw::workspace_layout(T, t->E, top_k, t->H, t->I);
+  for (int i = 0; i < 5; ++i) {
+    a.prof[i] = g_prof[i];
+    g_prof[i] = nullptr;
+  }
   const cudaError_t e = pw::launch_forward(a, reinterpret_cast<cudaStream_t>(compute));
   if (e != cudaSuccess) return cuda_fail(e, "pw_moe_forward: launch");
   return PW_OK;
@@ -491,6 +514,12 @@ int pw_moe_forward_host(pw_table* t, int layer, const void* x_host, const float*
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "pw_moe_forward_host: output copy");
   if (status) return fail(PW_EDEVICE, "pw_moe_forward_host: device status 0x%x", status);
+  return PW_OK;
+}
+
+int pw_profile_attach(void* const* events, int n_events) {
+  for (int i = 0; i < 5; ++i)
+    g_prof[i] = (events && n_events >= 5) ? static_cast<cudaEvent_t>(events[i]) : nullptr;
   return PW_OK;
 }
 

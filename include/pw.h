@@ -178,6 +178,15 @@ int pw_set_commit(pw_table* t, int layer, int expert, int kind, int q, pw_stream
 int pw_block_state(pw_table* t, int layer, int expert, int kind, int* q, int* resident,
                    int* reload_target);
 
+/*
+ * pw_debug_fail_next_reload -- test hook for the failure path of the reload
+ * protocol: the next pw_reload_async on this table behaves as if its first
+ * host->device copy could not be enqueued (no copy is issued, the block is
+ * marked failed, PW_ECUDA is returned).  Lets tests exercise PW_ERELOAD without
+ * disturbing the GPU.
+ */
+int pw_debug_fail_next_reload(pw_table* t);
+
 /* Destroys the host object (after synchronising its pending reload events). */
 int pw_table_destroy(pw_table* t);
 
@@ -231,6 +240,17 @@ int pw_moe_forward_host(pw_table* t, int layer, const void* x_host, const float*
  * PW_STATUS_* bits set by the last forward that used this workspace.
  */
 int pw_workspace_status(const void* workspace, pw_stream_t s, int* status);
+
+/*
+ * pw_profile_attach -- measurement hook: the NEXT pw_moe_forward called on this
+ * thread records the given CUDA events (cudaEvent_t handles created by the caller)
+ * on its stream at its kernel boundaries, then forgets them:
+ *   events[0] before the routing/permutation kernel, events[1] after it,
+ *   events[2] after the gate_up kernel, events[3] after the down kernel,
+ *   events[4] after the combine kernel.
+ * n_events < 5 (or NULL) detaches.  The kernels themselves are unchanged.
+ */
+int pw_profile_attach(void* const* events, int n_events);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,200 @@
+"""Parity of the fused layer on the GPU (through the C ABI) against the oracle.
+
+Bit-exact: routing indices, offsets, permutation; integer-table layers.
+Float outputs: rel L2 <= 1e-3 and max abs <= 2e-2 against fp64.
+"""
+import numpy as np
+import pytest
+
+import synth
+from oracle import moe as omoe
+
+from _layers import SynthBlocks, assert_close, gpu_layer, oracle_blocks, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(m, cfg, x, L, layer=0, k=None, renorm=None, residual=None):
+    import torch
+    k = cfg.top_k if k is None else k
+    renorm = cfg.renorm if renorm is None else renorm
+    xd = torch.from_numpy(x).cuda()
+    Ld = torch.from_numpy(L).cuda()
+    rd = None if residual is None else torch.from_numpy(residual).cuda()
+    out, ri, rw, ro, rp = m.pw_moe_forward(layer, xd, Ld, k, renorm, residual=rd, routing=True)
+    torch.cuda.synchronize()
+    return to_np(out), to_np(ri), to_np(rw), to_np(ro), to_np(rp)
+
+
+def _check_routing(ref, ri, rw, ro, rp):
+    assert np.array_equal(ri, ref["idx"])
+    assert np.allclose(rw, ref["w"], rtol=2e-6, atol=1e-7)
+    assert np.array_equal(ro, ref["offsets"])
+    assert np.array_equal(rp, ref["perm"])
+
+
+def test_tiny_layer_full():
+    cfg = synth.CONFIGS["tiny"]
+    m = gpu_layer(cfg)
+    x, L = synth.tokens(cfg), synth.logits(cfg)
+    out, ri, rw, ro, rp = _run(m, cfg, x, L)
+    ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg)))
+    _check_routing(ref, ri, rw, ro, rp)
+    assert_close(out, ref["out"])
+
+
+@pytest.mark.parametrize("q", [3, 4, 5, 6, 7, 8])
+def test_tiny_every_bitwidth(q):
+    cfg = synth.CONFIGS["tiny"]
+    bits = np.full((cfg.E, 2), q, dtype=np.int32)
+    m = gpu_layer(cfg, bits={0: bits})
+    x, L = synth.tokens(cfg, step=q), synth.logits(cfg, step=q)
+    out, *_ = _run(m, cfg, x, L)
+    ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), bits))
+    assert_close(out, ref["out"])
+
+
+def test_integer_tables_bit_exact():
+    """Integer tables whose child table at the committed q is integer, 0/1 tokens,
+    top-1 routing: gate sums lie in [32, 64] so silu(g) == g in fp32, every sum is
+    an exact integer, and out must equal the oracle's fp16 rounding bit for bit."""
+    cfg = synth.CONFIGS["tiny"].with_(T=16, top_k=1, renorm=1)
+    rng = np.random.default_rng(99)
+    E, H, I = cfg.E, cfg.H, cfg.I
+    bits = rng.integers(3, 9, size=(E, 2)).astype(np.int32)
+    blk = {}
+    for e in range(E):
+        for kind in (0, 1):
+            R, K = cfg.rows(kind), cfg.cols(kind)
+            q = int(bits[e, kind])
+            if kind == 0:
+                f = np.concatenate([rng.integers(1, 3, size=(I, 1 << q)),       # gate rows: 1 or 2
+                                    rng.integers(-1, 2, size=(I, 1 << q))])     # up rows: -1, 0, 1
+            else:
+                f = rng.integers(-1, 2, size=(R, 1 << q))
+            par = np.repeat(f, 1 << (8 - q), axis=1).astype(np.float16)        # child_q == f
+            blk[(e, kind)] = (rng.integers(0, 256, size=(R, K), dtype=np.uint8), par)
+    src = lambda e, kind: blk[(e, kind)]
+    m = gpu_layer(cfg, bits={0: bits}, blocks={0: src})
+    x = np.zeros((cfg.T, H), dtype=np.float16)
+    for t in range(cfg.T):
+        x[t, rng.choice(H, size=32, replace=False)] = 1
+    L = synth.logits(cfg)
+    out, *_ = _run(m, cfg, x, L)
+    ref = omoe.layer(x, L, 1, 1, oracle_blocks(src, bits))
+    assert np.array_equal(out.view(np.uint16), ref["out"].astype(np.float16).view(np.uint16))
+
+
+def test_qwen_decode_layer_full():
+    cfg = synth.CONFIGS["qwen_decode"]
+    m = gpu_layer(cfg)
+    x, L = synth.tokens(cfg), synth.logits(cfg)
+    out, ri, rw, ro, rp = _run(m, cfg, x, L)
+    ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg)))
+    _check_routing(ref, ri, rw, ro, rp)
+    assert_close(out, ref["out"])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mixtral_decode_t1", "mixtral_decode_t4"])
+def test_mixtral_decode_sampled(name):
+    cfg = synth.CONFIGS[name]
+    m = gpu_layer(cfg)
+    x, L = synth.tokens(cfg), synth.logits(cfg)
+    out, ri, rw, ro, rp = _run(m, cfg, x, L)
+    cols = np.sort(np.random.default_rng(5).choice(cfg.H, size=96, replace=False))
+    ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg)),
+                     out_rows=cols)
+    _check_routing(ref, ri, rw, ro, rp)
+    assert_close(out[:, cols], ref["out"])
+
+
+def test_prefill_shaped_small():
+    # many tokens per expert, ragged counts (Dirichlet mix), small hidden sizes
+    cfg = synth.CONFIGS["mixtral_prefill"].with_(T=300, H=256, I=512)
+    m = gpu_layer(cfg)
+    x, L = synth.tokens(cfg), synth.logits(cfg)
+    out, ri, rw, ro, rp = _run(m, cfg, x, L)
+    ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg)))
+    _check_routing(ref, ri, rw, ro, rp)
+    assert_close(out, ref["out"])
+
+
+def test_residual_topk_extremes_and_determinism():
+    import torch
+    cfg = synth.CONFIGS["tiny"].with_(T=7)
+    m = gpu_layer(cfg)
+    src = oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg))
+    x, L = synth.tokens(cfg), synth.logits(cfg)
+    res = synth.tokens(cfg, step=3)
+    for k, rn in ((1, 1), (1, 0), (cfg.E, 0), (3, 1)):
+        out, *_ = _run(m, cfg, x, L, k=k, renorm=rn, residual=res)
+        ref = omoe.layer(x, L, k, rn, src, residual=res)
+        assert_close(out, ref["out"])
+        again, *_ = _run(m, cfg, x, L, k=k, renorm=rn, residual=res)
+        assert np.array_equal(out.view(np.uint16), again.view(np.uint16))
+    # T = 0 is a no-op
+    ws = m.workspace(0, 2)
+    e = torch.empty((0, cfg.H), dtype=torch.float16, device="cuda")
+    m.pw_moe_forward(0, e, torch.empty((0, cfg.E), dtype=torch.float32, device="cuda"), 2, 1, ws=ws)
+
+
+def test_single_expert_layer():
+    cfg = synth.CONFIGS["tiny"].with_(E=1, top_k=1, renorm=1, T=5)
+    m = gpu_layer(cfg)
+    x, L = synth.tokens(cfg), synth.logits(cfg)
+    out, *_ = _run(m, cfg, x, L)
+    ref = omoe.layer(x, L, 1, 1, oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg)))
+    assert_close(out, ref["out"])
+
+
+def test_host_entry_matches_device_entry():
+    import torch
+    cfg = synth.CONFIGS["qwen_decode"]
+    m = gpu_layer(cfg)
+    x, L = synth.tokens(cfg), synth.logits(cfg)
+    dev, *_ = _run(m, cfg, x, L)
+    xh = torch.from_numpy(x).pin_memory()
+    Lh = torch.from_numpy(L).pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    m.pw_moe_forward_host(0, xh, Lh, cfg.top_k, cfg.renorm, oh)
+    assert np.array_equal(oh.numpy().view(np.uint16), dev.view(np.uint16))
+
+
+def test_nan_logit_sets_status_not_fault():
+    import torch
+    import any_precision_weight_gb300 as pw
+    cfg = synth.CONFIGS["tiny"]
+    m = gpu_layer(cfg)
+    x, L = synth.tokens(cfg), synth.logits(cfg)
+    L[3, 2] = np.nan
+    ws = m.workspace(cfg.T, cfg.top_k)
+    m.pw_moe_forward(0, torch.from_numpy(x).cuda(), torch.from_numpy(L).cuda(), cfg.top_k, cfg.renorm, ws=ws)
+    assert m.workspace_status(ws) & pw.PW_STATUS_NAN_LOGIT
+    L[3, 2] = 0.0
+    m.pw_moe_forward(0, torch.from_numpy(x).cuda(), torch.from_numpy(L).cuda(), cfg.top_k, cfg.renorm, ws=ws)
+    assert m.workspace_status(ws) == 0
+
+
+def test_forward_argument_errors():
+    import torch
+    import any_precision_weight_gb300 as pw
+    cfg = synth.CONFIGS["tiny"]
+    m = gpu_layer(cfg)
+    x = torch.from_numpy(synth.tokens(cfg)).cuda()
+    L = torch.from_numpy(synth.logits(cfg)).cuda()
+    with pytest.raises(pw.PWError) as e:
+        m.pw_moe_forward(0, x, L, cfg.E + 1, 1)
+    assert e.value.code == pw.PW_EINVAL
+    with pytest.raises(pw.PWError) as e:
+        m.pw_moe_forward(1, x, L, 2, 1)
+    assert e.value.code == pw.PW_EINVAL
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pw.PWError) as e:
+        m.pw_moe_forward(0, x, L, 2, 1, ws=small)
+    assert e.value.code == pw.PW_ENOMEM
+    # a table with an unregistered block refuses to run
+    m2 = pw.PagedMoE(1, cfg.E, cfg.H, cfg.I)
+    with pytest.raises(pw.PWError) as e:
+        m2.pw_moe_forward(0, x, L, 2, 1)
+    assert e.value.code == pw.PW_EINVAL
