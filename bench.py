@@ -293,6 +293,10 @@ def run_ours(args, cfg, rank, world, local):
     # per-kernel boundary events over a second region of the same steps
     kn = min(args.steps, 2000)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(kn)]
+    for row in evs:                 # torch creates the CUDA event at its first record
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
     for i in range(kn):
         pw.pw_profile_attach(evs[i])
         step(i)
