@@ -1,0 +1,353 @@
+// Decode-sized dequantised GEMV of the fused APL MoE layer (sm_103a, CUDA cores).
+//
+// Source: PagedWeight technical summary, core components section 3 ("Fused
+// Mixed-Precision Kernel": reads APL bit-planes and lookup tables directly,
+// a different committed bitwidth per linear block within one fused operation).
+//
+// Decode batches give each active expert a handful of tokens, so these
+// kernels stream each active block's q bit-planes and q-bit table from HBM
+// exactly once and keep the tokens on chip.  Design:
+//
+//  * persistent CTAs (one per SM) pull (active expert, 64-row tile) items from
+//    a device work queue, so the committed q of each block is read from the
+//    page table on the device and the grid never depends on the routing;
+//  * a tile is 64 rows x all of K; warps = 2 row groups x 4 K-warps; lane l of
+//    a row group owns row l, so the 64 rows' tables sit in shared memory as
+//    fp32 [v][64 rows]: the 32 lanes of a warp always hit 32 different banks,
+//    whatever their indices (conflict-free lookups at every q);
+//  * bit-planes are staged global->shared with cp.async in 16-word (512-k)
+//    chunks, double buffered, XOR-swizzled so the 128-bit reads of 32 rows
+//    are conflict-free; tokens are staged the same way (fp32);
+//  * per 32-bit plane word a lane turns q plane words into 32 q-bit indices
+//    with an 8x8 bit-matrix transpose done four bytes at a time (delta swaps),
+//    then one byte permute per element forms the table address
+//    (index * 256 + row * 4);
+//  * products accumulate in fp32 with packed two-wide FMAs; the four K-warps'
+//    partial sums are added in a fixed order (deterministic results).
+// gate_up tiles hold 32 gate rows and the 32 matching up rows and finish with
+// h = silu(gate) * up rounded to fp16; down tiles hold 64 rows of y (fp32).
+
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "pw_device.cuh"
+
+namespace pw {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kRows = 64;            // rows per tile
+constexpr int kStageWords = 16;      // plane words per row per stage (4 per K-warp)
+constexpr int kStageK = kStageWords * 32;
+constexpr int kTok = 4;              // tokens per pass over a tile
+constexpr int kLutBytes = 256 * kRows * 4;
+constexpr int kPlaneStageBytes = PW_MAX_BITS * kRows * kStageWords * 4;
+constexpr int kXStageBytes = kTok * kStageK * 4;
+constexpr int kRedBytes = 4 * kTok * kRows * 4;
+constexpr int kSmemBytes = kLutBytes + 2 * kPlaneStageBytes + 2 * kXStageBytes + kRedBytes + 64;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst)), "l"(src));
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+// a = a + w * x, two lanes at a time (packed fp32 FMA).
+__device__ __forceinline__ void ffma2(float& ax, float& ay, float wx, float wy, float xx, float xy) {
+  asm("{\n\t.reg .b64 a, w, x;\n\t"
+      "mov.b64 a, {%0, %1};\n\tmov.b64 w, {%2, %3};\n\tmov.b64 x, {%4, %5};\n\t"
+      "fma.rn.f32x2 a, w, x, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(ax), "+f"(ay)
+      : "f"(wx), "f"(wy), "f"(xx), "f"(xy));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Exchange the bits selected by `mask` in `lo >> s` with those of `hi`.
+__device__ __forceinline__ void delta_swap(uint32_t& lo, uint32_t& hi, int s, uint32_t mask) {
+  const uint32_t t = ((lo >> s) ^ hi) & mask;
+  hi ^= t;
+  lo ^= t << s;
+}
+
+// Row r of the transpose holds plane (Q-1-r).  After the three rounds, byte bb
+// of o[r] is the Q-bit index (plane 0 most significant) of element 8*bb + r.
+template <int Q>
+__device__ __forceinline__ void planes_to_indices(const uint32_t (&pw)[PW_MAX_BITS], uint32_t (&o)[8]) {
+#pragma unroll
+  for (int r = 0; r < 8; ++r) o[r] = (r < Q) ? pw[Q - 1 - r] : 0u;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) delta_swap(o[r], o[r + 4], 4, 0x0F0F0F0Fu);
+#pragma unroll
+  for (int r = 0; r < 8; r += 4) {
+    delta_swap(o[r], o[r + 2], 2, 0x33333333u);
+    delta_swap(o[r + 1], o[r + 3], 2, 0x33333333u);
+  }
+#pragma unroll
+  for (int r = 0; r < 8; r += 2) delta_swap(o[r], o[r + 1], 1, 0x55555555u);
+}
+
+struct Item {
+  int expert, tile, n, off;
+};
+
+// Global row of tile row i: gate_up tiles are 32 gate rows + the 32 matching
+// up rows; down tiles are 64 consecutive rows.  Returns -1 past the block.
+template <int KIND>
+__device__ __forceinline__ int global_row(const Fwd& p, int tile, int i) {
+  if (KIND == PW_KIND_GATE_UP) {
+    const int r = tile * 32 + (i & 31);
+    if (r >= p.I) return -1;
+    return (i < 32) ? r : p.I + r;
+  } else {
+    const int r = tile * kRows + i;
+    return (r < p.H) ? r : -1;
+  }
+}
+
+template <int KIND>
+__device__ __forceinline__ const float* token_row(const Fwd& p, int pos, int K) {
+  if (KIND == PW_KIND_GATE_UP) return p.xf + static_cast<size_t>(p.perm[pos] / p.k) * K;
+  return p.hf + static_cast<size_t>(pos) * K;
+}
+
+template <int Q, int KIND>
+__device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsigned char* smem) {
+  float* lut_s = reinterpret_cast<float*>(smem);
+  uint32_t* pl_s = reinterpret_cast<uint32_t*>(smem + kLutBytes);
+  float* x_s = reinterpret_cast<float*>(smem + kLutBytes + 2 * kPlaneStageBytes);
+  float* red_s = reinterpret_cast<float*>(smem + kLutBytes + 2 * kPlaneStageBytes + 2 * kXStageBytes);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rg = warp >> 2, kw = warp & 3;
+  const int K = d.K, W = K >> 5;
+  const int nchunk = (W + kStageWords - 1) / kStageWords;
+  constexpr int V = 1 << Q;
+
+  // ---- this tile's tables: LUT_q[row][v] fp16 -> lut_s[v][row] fp32
+  {
+    const int i = tid & 63;
+    const int gr = global_row<KIND>(p, it.tile, i);
+    for (int vc = tid >> 6; vc * 8 < V; vc += 4) {
+      float f[8];
+      if (gr >= 0) {
+        const uint16_t* src = d.lut + static_cast<size_t>(gr) * V + vc * 8;
+        if (V >= 8) {
+          const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
+          const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 ff = __half22float2(h2[e]);
+            f[2 * e] = ff.x;
+            f[2 * e + 1] = ff.y;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) lut_s[(vc * 8 + e) * kRows + i] = f[e];
+    }
+  }
+
+  const int row = rg * 32 + lane;
+  const uint32_t laneoff = static_cast<uint32_t>(row) * 4u;
+  const int swz = (row >> 1) & 3;
+  const unsigned char* lut_bytes = reinterpret_cast<const unsigned char*>(lut_s);
+
+  for (int t0 = 0; t0 < it.n; t0 += kTok) {
+    const int nt = min(kTok, it.n - t0);
+
+    auto fill = [&](int c, int s) {
+      // planes: thread -> (row, 16-byte chunk), one chunk per plane
+      const int fr = tid >> 2, c4 = tid & 3;
+      const int gr = global_row<KIND>(p, it.tile, fr);
+      const int wsrc = c * kStageWords + c4 * 4;
+      if (gr >= 0 && wsrc < W) {
+        uint32_t* dst = pl_s + s * (kPlaneStageBytes / 4) + fr * kStageWords + ((c4 ^ ((fr >> 1) & 3)) * 4);
+#pragma unroll
+        for (int pl = 0; pl < Q; ++pl)
+          cp_async16(dst + pl * kRows * kStageWords, d.planes[pl] + static_cast<size_t>(gr) * W + wsrc);
+      }
+      // tokens: nt x 512 floats
+      for (int q4 = tid; q4 < nt * (kStageK / 4); q4 += kThreads) {
+        const int tt = q4 / (kStageK / 4), cc = q4 % (kStageK / 4);
+        const int kk = c * kStageK + cc * 4;
+        if (kk < K)
+          cp_async16(x_s + s * (kXStageBytes / 4) + tt * kStageK + cc * 4,
+                     token_row<KIND>(p, it.off + t0 + tt, K) + kk);
+      }
+      cp_commit();
+    };
+
+    float ax[kTok], ay[kTok];
+#pragma unroll
+    for (int t = 0; t < kTok; ++t) ax[t] = ay[t] = 0.f;
+
+    fill(0, 0);
+    for (int c = 0; c < nchunk; ++c) {
+      const int s = c & 1;
+      if (c + 1 < nchunk) {
+        fill(c + 1, s ^ 1);
+        cp_wait<1>();
+      } else {
+        cp_wait<0>();
+      }
+      __syncthreads();
+
+      const int wbase = c * kStageWords + kw * 4;
+      const int nw = min(4, W - wbase);
+      if (nw > 0) {
+        const uint32_t* ps = pl_s + s * (kPlaneStageBytes / 4) + row * kStageWords + ((kw ^ swz) * 4);
+        uint4 pv[PW_MAX_BITS];
+#pragma unroll
+        for (int pl = 0; pl < Q; ++pl) pv[pl] = *reinterpret_cast<const uint4*>(ps + pl * kRows * kStageWords);
+        const float* xs = x_s + s * (kXStageBytes / 4) + kw * 128;
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+          if (wi < nw) {
+            uint32_t pw_[PW_MAX_BITS];
+#pragma unroll
+            for (int pl = 0; pl < PW_MAX_BITS; ++pl) {
+              if (pl < Q) {
+                const uint4 v = pv[pl];
+                pw_[pl] = wi == 0 ? v.x : wi == 1 ? v.y : wi == 2 ? v.z : v.w;
+              } else {
+                pw_[pl] = 0u;
+              }
+            }
+            uint32_t o[8];
+            planes_to_indices<Q>(pw_, o);
+            float wv[32];
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb)
+#pragma unroll
+              for (int r = 0; r < 8; ++r) {
+                const uint32_t a = prmt(o[r], laneoff, 0x5504u | (static_cast<uint32_t>(bb) << 4));
+                wv[8 * bb + r] = *reinterpret_cast<const float*>(lut_bytes + a);
+              }
+#pragma unroll
+            for (int t = 0; t < kTok; ++t) {
+              if (t < nt) {
+                const float4* xr = reinterpret_cast<const float4*>(xs + t * kStageK + wi * 32);
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                  const float4 xv = xr[j4];
+                  ffma2(ax[t], ay[t], wv[4 * j4], wv[4 * j4 + 1], xv.x, xv.y);
+                  ffma2(ax[t], ay[t], wv[4 * j4 + 2], wv[4 * j4 + 3], xv.z, xv.w);
+                }
+              }
+            }
+          }
+        }
+      }
+      __syncthreads();
+    }
+
+    // ---- partial sums of the four K-warps, added in a fixed order
+#pragma unroll
+    for (int t = 0; t < kTok; ++t)
+      if (t < nt) red_s[(kw * kTok + t) * kRows + row] = ax[t] + ay[t];
+    __syncthreads();
+    if (KIND == PW_KIND_GATE_UP) {
+      for (int q = tid; q < nt * 32; q += kThreads) {
+        const int t = q >> 5, i = q & 31;
+        const int r = it.tile * 32 + i;
+        float g = 0.f, u = 0.f;
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) {
+          g += red_s[(w4 * kTok + t) * kRows + i];
+          u += red_s[(w4 * kTok + t) * kRows + 32 + i];
+        }
+        if (r < p.I) {
+          const float hv = g / (1.f + expf(-g)) * u;
+          p.hf[static_cast<size_t>(it.off + t0 + t) * p.I + r] = __half2float(__float2half_rn(hv));
+        }
+      }
+    } else {
+      for (int q = tid; q < nt * kRows; q += kThreads) {
+        const int t = q >> 6, i = q & 63;
+        const int r = it.tile * kRows + i;
+        float yv = 0.f;
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) yv += red_s[(w4 * kTok + t) * kRows + i];
+        if (r < p.H) p.y[static_cast<size_t>(it.off + t0 + t) * p.H + r] = yv;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1) k_decode(Fwd p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  int* s_item = reinterpret_cast<int*>(smem + kSmemBytes - 64);
+  const int tiles = (KIND == PW_KIND_GATE_UP) ? p.I / 32 : (p.H + kRows - 1) / kRows;
+  const int nact = p.active[0];
+  const int total = nact * tiles;
+  int* ctr = reinterpret_cast<int*>(p.status) + (KIND == PW_KIND_GATE_UP ? kCtrGateUp : kCtrDown);
+  for (;;) {
+    if (threadIdx.x == 0) *s_item = atomicAdd(ctr, 1);
+    __syncthreads();
+    const int item = *s_item;
+    __syncthreads();
+    if (item >= total) break;
+    Item it;
+    it.expert = p.active[1 + item / tiles];
+    it.tile = item % tiles;
+    it.n = p.counts[it.expert];
+    it.off = p.offsets[it.expert];
+    const BlockDesc d = *block_desc(p, it.expert, KIND);
+    switch (d.q) {
+      case 3: run_tile<3, KIND>(p, d, it, smem); break;
+      case 4: run_tile<4, KIND>(p, d, it, smem); break;
+      case 5: run_tile<5, KIND>(p, d, it, smem); break;
+      case 6: run_tile<6, KIND>(p, d, it, smem); break;
+      case 7: run_tile<7, KIND>(p, d, it, smem); break;
+      case 8: run_tile<8, KIND>(p, d, it, smem); break;
+      default:
+        if (threadIdx.x == 0) atomicOr(p.status, PW_STATUS_BAD_DESC);
+        break;
+    }
+  }
+}
+
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices] = {};   // SM count per device once configured (0: not yet)
+
+}  // namespace
+
+cudaError_t launch_decode(const Fwd& p, int kind, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (g_sms[dev] == 0) {   // once per device: opt in to > 48 KB of shared memory
+    e = cudaFuncSetAttribute(k_decode<PW_KIND_GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_decode<PW_KIND_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes);
+    int sms = 0;
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_sms[dev] = sms > 0 ? sms : 1;
+  }
+  if (kind == PW_KIND_GATE_UP)
+    k_decode<PW_KIND_GATE_UP><<<g_sms[dev], kThreads, kSmemBytes, s>>>(p);
+  else
+    k_decode<PW_KIND_DOWN><<<g_sms[dev], kThreads, kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace pw

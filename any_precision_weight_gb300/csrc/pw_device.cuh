@@ -1,0 +1,47 @@
+// Device-side parameter block and helpers shared by the kernel files.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "pw_internal.h"
+
+namespace pw {
+
+// Everything one forward pass needs on the device, resolved by the host.
+struct Fwd {
+  const BlockDesc* desc;
+  int layer, E, H, I, T, k, renorm;
+  const __half* x;          // [T][H] fp16
+  const float* logits;      // [T][E]
+  const __half* residual;   // [T][H] or null
+  __half* out;              // [T][H]
+  int32_t* user_idx;
+  float* user_w;
+  int32_t* user_offsets;
+  int32_t* user_perm;
+  uint32_t* status;         // status word; counters follow
+  int32_t* idx;             // [T*k]
+  float* w;                 // [T*k]
+  int32_t* counts;          // [E]
+  int32_t* offsets;         // [E+1]
+  int32_t* perm;            // [T*k]
+  int32_t* inv;             // [T*k]
+  int32_t* active;          // [E+1]
+  float* xf;                // [T][H]   x as fp32
+  float* hf;                // [T*k][I] h rounded to fp16, held as fp32
+  float* y;                 // [T*k][H]
+};
+
+// Work-queue counters live right after the status word.
+constexpr int kCtrGateUp = 1;
+constexpr int kCtrDown = 2;
+
+__device__ __forceinline__ const BlockDesc* block_desc(const Fwd& p, int e, int kind) {
+  return p.desc + desc_index(p.layer, e, kind, p.E);
+}
+
+// Decode GEMV of one block kind (gate_up or down) over all active experts.
+cudaError_t launch_decode(const Fwd& p, int kind, cudaStream_t s);
+
+}  // namespace pw

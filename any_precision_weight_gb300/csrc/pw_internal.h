@@ -44,7 +44,8 @@ struct Workspace {
   size_t perm;       // int32 [T*k]
   size_t inv;        // int32 [T*k]
   size_t active;     // int32 [E+1]: number of active experts, then their ids
-  size_t h;          // fp16 [T*k][I] in perm order
+  size_t xf;         // f32 [T][H]: x converted once
+  size_t hf;         // f32 [T*k][I] in perm order: h rounded to fp16, held as fp32
   size_t y;          // f32 [T*k][H] in perm order
   size_t x_in;       // fp16 [T][H]   (host-input staging)
   size_t logits_in;  // f32 [T][E]
@@ -68,7 +69,8 @@ inline Workspace workspace_layout(int T, int E, int k, int H, int I) {
   w.perm = take(P * 4);
   w.inv = take(P * 4);
   w.active = take(static_cast<size_t>(E + 1) * 4);
-  w.h = take(P * I * 2);
+  w.xf = take(static_cast<size_t>(T) * H * 4);
+  w.hf = take(P * I * 4);
   w.y = take(P * H * 4);
   w.x_in = take(static_cast<size_t>(T) * H * 2);
   w.logits_in = take(static_cast<size_t>(T) * E * 4);

@@ -19,38 +19,9 @@
 #include <cuda_fp16.h>
 #include <cstdint>
 
-#include "pw_internal.h"
+#include "pw_device.cuh"
 
 namespace pw {
-
-// ------------------------------------------------------------------ device params
-
-struct Fwd {
-  const BlockDesc* desc;
-  int layer, E, H, I, T, k, renorm;
-  const __half* x;
-  const float* logits;
-  const __half* residual;
-  __half* out;
-  int32_t* user_idx;
-  float* user_w;
-  int32_t* user_offsets;
-  int32_t* user_perm;
-  uint32_t* status;
-  int32_t* idx;     // [T*k]
-  float* w;         // [T*k]
-  int32_t* counts;  // [E]
-  int32_t* offsets; // [E+1]
-  int32_t* perm;    // [T*k]
-  int32_t* inv;     // [T*k]
-  int32_t* active;  // [E+1]
-  __half* h;        // [T*k][I]
-  float* y;         // [T*k][H]
-};
-
-__device__ __forceinline__ const BlockDesc* block_desc(const Fwd& p, int e, int kind) {
-  return p.desc + desc_index(p.layer, e, kind, p.E);
-}
 
 // ------------------------------------------------------------------ commit
 
@@ -74,6 +45,27 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
+// x (fp16) -> xf (fp32), 8 elements per call.
+__device__ __forceinline__ void convert8(const Fwd& p, int i) {
+  const uint4 raw = reinterpret_cast<const uint4*>(p.x)[i];
+  const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+  float4 a, b;
+  float2 f;
+  f = __half22float2(h2[0]); a.x = f.x; a.y = f.y;
+  f = __half22float2(h2[1]); a.z = f.x; a.w = f.y;
+  f = __half22float2(h2[2]); b.x = f.x; b.y = f.y;
+  f = __half22float2(h2[3]); b.z = f.x; b.w = f.y;
+  reinterpret_cast<float4*>(p.xf)[2 * i] = a;
+  reinterpret_cast<float4*>(p.xf)[2 * i + 1] = b;
+}
+
+constexpr int kConvertInRoute = 64;   // larger batches convert x in their own kernel
+
+__global__ void k_convert_x(Fwd p) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < p.T * p.H / 8) convert8(p, i);
+}
+
 // One CTA for the whole batch.  Phase 1: warp per token, top-k over the fp32
 // logits and softmax weights.  Phase 2: per-expert counts and offsets.
 // Phase 3: warp per expert, ballot ranks give the stable (expert, token) order.
@@ -82,7 +74,9 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_permute(Fwd p) {
   __shared__ int s_off[kMaxE + 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
   const int E = p.E, k = p.k, T = p.T;
-  if (threadIdx.x == 0) *p.status = 0u;
+  if (threadIdx.x < 4) p.status[threadIdx.x] = 0u;   // status word and work-queue counters
+  if (T <= kConvertInRoute)
+    for (int i = threadIdx.x; i < T * p.H / 8; i += blockDim.x) convert8(p, i);
 
   for (int t = warp; t < T; t += nwarp) {
     float v[kPerLane];
@@ -188,93 +182,6 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_permute(Fwd p) {
     }
 }
 
-// ------------------------------------------------------------------ dequant GEMV (reference path)
-
-constexpr int kGemvWarps = 8;
-constexpr int kGemvTok = 8;      // tokens handled per pass over a row
-
-// Dot products of one block row with up to kGemvTok input rows.
-// Lane l handles plane words w = l, l+32, ...; element k = 32w + j takes the
-// q-bit index assembled MSB first from the top q planes and looks up LUT_q.
-__device__ __forceinline__ void row_dot(const BlockDesc& d, int row, const __half* const* xr, int nt,
-                                        float* acc) {
-  const int W = d.K >> 5;
-  const int q = d.q;
-  const uint16_t* lut = d.lut + (static_cast<size_t>(row) << q);
-  for (int t = 0; t < kGemvTok; ++t) acc[t] = 0.f;
-  for (int w = threadIdx.x & 31; w < W; w += 32) {
-    uint32_t pw[PW_MAX_BITS];
-#pragma unroll
-    for (int pl = 0; pl < PW_MAX_BITS; ++pl)
-      pw[pl] = (pl < q) ? __ldg(d.planes[pl] + static_cast<size_t>(row) * W + w) : 0u;
-    for (int j = 0; j < 32; ++j) {
-      uint32_t v = 0;
-#pragma unroll
-      for (int pl = 0; pl < PW_MAX_BITS; ++pl)
-        if (pl < q) v = (v << 1) | ((pw[pl] >> j) & 1u);
-      const float wt = __half2float(__ushort_as_half(__ldg(lut + v)));
-      const int kk = 32 * w + j;
-#pragma unroll
-      for (int t = 0; t < kGemvTok; ++t)
-        if (t < nt) acc[t] = fmaf(wt, __half2float(xr[t][kk]), acc[t]);
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < kGemvTok; ++t)
-#pragma unroll
-    for (int o = 16; o; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
-}
-
-template <int kKind>
-__global__ void __launch_bounds__(kGemvWarps * 32) k_gemv_ref(Fwd p) {
-  const int e = blockIdx.y;
-  const int cnt = p.counts[e];
-  if (cnt == 0) return;
-  const int off = p.offsets[e];
-  const BlockDesc d = *block_desc(p, e, kKind);
-  if (d.q < 1 || d.q > PW_MAX_BITS) {
-    if (threadIdx.x == 0) atomicOr(p.status, PW_STATUS_BAD_DESC);
-    return;
-  }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int rows = (kKind == PW_KIND_GATE_UP) ? p.I : p.H;
-  for (int r = blockIdx.x * kGemvWarps + warp; r < rows; r += gridDim.x * kGemvWarps) {
-    for (int t0 = 0; t0 < cnt; t0 += kGemvTok) {
-      const int nt = min(kGemvTok, cnt - t0);
-      const __half* xr[kGemvTok];
-#pragma unroll
-      for (int t = 0; t < kGemvTok; ++t) {
-        const int pos = off + t0 + min(t, nt - 1);
-        xr[t] = (kKind == PW_KIND_GATE_UP) ? p.x + static_cast<size_t>(p.perm[pos] / p.k) * p.H
-                                           : p.h + static_cast<size_t>(pos) * p.I;
-      }
-      if (kKind == PW_KIND_GATE_UP) {
-        float g[kGemvTok], u[kGemvTok];
-        row_dot(d, r, xr, nt, g);
-        row_dot(d, p.I + r, xr, nt, u);
-        if (lane < nt) {
-          float gv = g[0], uv = u[0];
-#pragma unroll
-          for (int t = 1; t < kGemvTok; ++t)
-            if (t == lane) { gv = g[t]; uv = u[t]; }
-          const float hv = gv / (1.f + expf(-gv)) * uv;
-          p.h[static_cast<size_t>(off + t0 + lane) * p.I + r] = __float2half_rn(hv);
-        }
-      } else {
-        float a[kGemvTok];
-        row_dot(d, r, xr, nt, a);
-        if (lane < nt) {
-          float av = a[0];
-#pragma unroll
-          for (int t = 1; t < kGemvTok; ++t)
-            if (t == lane) av = a[t];
-          p.y[static_cast<size_t>(off + t0 + lane) * p.H + r] = av;
-        }
-      }
-    }
-  }
-}
-
 // ------------------------------------------------------------------ combine
 
 __global__ void k_combine(Fwd p) {
@@ -319,7 +226,8 @@ static Fwd make_fwd(const ForwardArgs& a) {
   p.perm = reinterpret_cast<int32_t*>(ws + a.lay.perm);
   p.inv = reinterpret_cast<int32_t*>(ws + a.lay.inv);
   p.active = reinterpret_cast<int32_t*>(ws + a.lay.active);
-  p.h = reinterpret_cast<__half*>(ws + a.lay.h);
+  p.xf = reinterpret_cast<float*>(ws + a.lay.xf);
+  p.hf = reinterpret_cast<float*>(ws + a.lay.hf);
   p.y = reinterpret_cast<float*>(ws + a.lay.y);
   return p;
 }
@@ -331,13 +239,17 @@ static inline void mark(const ForwardArgs& a, int i, cudaStream_t s) {
 cudaError_t launch_forward(const ForwardArgs& a, cudaStream_t s) {
   const Fwd p = make_fwd(a);
   mark(a, 0, s);
+  if (p.T > kConvertInRoute) {
+    const int n8 = p.T * p.H / 8;
+    k_convert_x<<<(n8 + 255) / 256, 256, 0, s>>>(p);
+  }
   k_route_permute<<<1, kRouteThreads, 0, s>>>(p);
   mark(a, 1, s);
-  const int gx_gu = (p.I + kGemvWarps - 1) / kGemvWarps;
-  const int gx_dn = (p.H + kGemvWarps - 1) / kGemvWarps;
-  k_gemv_ref<PW_KIND_GATE_UP><<<dim3(min(gx_gu, 1024), p.E), kGemvWarps * 32, 0, s>>>(p);
+  cudaError_t e = launch_decode(p, PW_KIND_GATE_UP, s);
+  if (e != cudaSuccess) return e;
   mark(a, 2, s);
-  k_gemv_ref<PW_KIND_DOWN><<<dim3(min(gx_dn, 1024), p.E), kGemvWarps * 32, 0, s>>>(p);
+  e = launch_decode(p, PW_KIND_DOWN, s);
+  if (e != cudaSuccess) return e;
   mark(a, 3, s);
   k_combine<<<dim3((p.H + 255) / 256, p.T), 256, 0, s>>>(p);
   mark(a, 4, s);

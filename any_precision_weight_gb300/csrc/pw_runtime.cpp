@@ -223,8 +223,8 @@ int pw_table_create(pw_table** out, int n_layers, int n_experts, int H, int I, v
   *out = nullptr;
   if (n_layers < 1 || n_experts < 1 || n_experts > 256)
     return fail(PW_EINVAL, "pw_table_create: need n_layers >= 1, 1 <= n_experts <= 256");
-  if (H < 32 || I < 32 || H % 32 || I % 32)
-    return fail(PW_EINVAL, "pw_table_create: H and I must be positive multiples of 32");
+  if (H < 128 || I < 128 || H % 128 || I % 128)
+    return fail(PW_EINVAL, "pw_table_create: H and I must be positive multiples of 128");
   if (!d_desc || desc_bytes < pw_desc_bytes(n_layers, n_experts))
     return fail(PW_EINVAL, "pw_table_create: descriptor buffer smaller than pw_desc_bytes");
   if (reinterpret_cast<uintptr_t>(d_desc) % 128)

@@ -24,7 +24,7 @@
  *   committed bitwidth form a tail that can live on the CPU and be reloaded.
  *
  * Block shapes: gate_up has R = 2I rows (rows [0, I) gate, [I, 2I) up) and
- * K = H columns; down has R = H rows and K = I columns.  H, I multiples of 32.
+ * K = H columns; down has R = H rows and K = I columns.  H, I multiples of 128.
  *
  * Conventions for every call:
  *   - returns PW_OK (0) or a negative PW_E* status; nothing throws or exits;
@@ -112,7 +112,7 @@ size_t pw_desc_bytes(int n_layers, int n_experts);
  *               128-byte aligned, owned by the caller, alive until pw_table_destroy.
  *               The kernels read each block's committed q_i and page addresses from
  *               it, so a commit needs no recompile and no host round trip.
- *   n_experts   1..256;  H, I: hidden and expert-intermediate sizes (multiples of 32).
+ *   n_experts   1..256;  H, I: hidden and expert-intermediate sizes (multiples of 128).
  *   s           stream on which the descriptors are cleared (asynchronous).
  * Errors: PW_EINVAL (shapes, small or misaligned buffer), PW_ECUDA, PW_ENOMEM.
  */
