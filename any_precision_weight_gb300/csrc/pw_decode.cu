@@ -36,10 +36,11 @@ namespace pw {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kCtasPerSm = 1;
 constexpr int kRows = 64;            // rows per tile
 constexpr int kStageWords = 16;      // plane words per row per stage (4 per K-warp)
 constexpr int kStageK = kStageWords * 32;
-constexpr int kTok = 4;              // tokens per pass over a tile
+constexpr int kTok = 2;              // tokens per pass over a tile
 constexpr int kLutBytes = 256 * kRows * 4;
 constexpr int kPlaneStageBytes = PW_MAX_BITS * kRows * kStageWords * 4;
 constexpr int kXStageBytes = kTok * kStageK * 4;
@@ -72,19 +73,25 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// Exchange the bits selected by `mask` in `lo >> s` with those of `hi`.
+// (a & ~m) | (b & m) in one three-input logic op.
+__device__ __forceinline__ uint32_t bitsel(uint32_t a, uint32_t b, uint32_t m) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xCA;" : "=r"(d) : "r"(m), "r"(b), "r"(a));
+  return d;
+}
+// Exchange the bits of `hi` selected by `mask` with the bits of `lo` selected
+// by `mask << s`: two shifts and two logic ops.
 __device__ __forceinline__ void delta_swap(uint32_t& lo, uint32_t& hi, int s, uint32_t mask) {
-  const uint32_t t = ((lo >> s) ^ hi) & mask;
-  hi ^= t;
-  lo ^= t << s;
+  const uint32_t nlo = bitsel(lo, hi << s, mask << s);
+  const uint32_t nhi = bitsel(hi, lo >> s, mask);
+  lo = nlo;
+  hi = nhi;
 }
 
-// Row r of the transpose holds plane (Q-1-r).  After the three rounds, byte bb
-// of o[r] is the Q-bit index (plane 0 most significant) of element 8*bb + r.
-template <int Q>
-__device__ __forceinline__ void planes_to_indices(const uint32_t (&pw)[PW_MAX_BITS], uint32_t (&o)[8]) {
-#pragma unroll
-  for (int r = 0; r < 8; ++r) o[r] = (r < Q) ? pw[Q - 1 - r] : 0u;
+// 8x8 bit transposes, four byte lanes at once.  Row r of the input holds plane
+// (q-1-r) (zero for r >= q); after the three rounds, byte bb of o[r] is the
+// q-bit index (plane 0 most significant) of element 8*bb + r.
+__device__ __forceinline__ void planes_to_indices(uint32_t (&o)[8]) {
 #pragma unroll
   for (int r = 0; r < 4; ++r) delta_swap(o[r], o[r + 4], 4, 0x0F0F0F0Fu);
 #pragma unroll
@@ -120,7 +127,7 @@ __device__ __forceinline__ const float* token_row(const Fwd& p, int pos, int K) 
   return p.hf + static_cast<size_t>(pos) * K;
 }
 
-template <int Q, int KIND>
+template <int KIND>
 __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsigned char* smem) {
   float* lut_s = reinterpret_cast<float*>(smem);
   uint32_t* pl_s = reinterpret_cast<uint32_t*>(smem + kLutBytes);
@@ -130,19 +137,48 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rg = warp >> 2, kw = warp & 3;
   const int K = d.K, W = K >> 5;
+  const int Q = d.q, V = 1 << Q;
   const int nchunk = (W + kStageWords - 1) / kStageWords;
-  constexpr int V = 1 << Q;
 
-  // ---- this tile's tables: LUT_q[row][v] fp16 -> lut_s[v][row] fp32
-  {
-    const int i = tid & 63;
-    const int gr = global_row<KIND>(p, it.tile, i);
-    for (int vc = tid >> 6; vc * 8 < V; vc += 4) {
-      float f[8];
-      if (gr >= 0) {
-        const uint16_t* src = d.lut + static_cast<size_t>(gr) * V + vc * 8;
-        if (V >= 8) {
-          const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
+  // plane staging: thread -> (tile row, 16-byte chunk); chunks are XOR-swizzled
+  // by row so a warp's 32 rows read 128-bit words conflict-free
+  const int fr = tid >> 2, fc = tid & 3;
+  const int fgr = global_row<KIND>(p, it.tile, fr);
+  const int fdst = fr * kStageWords + ((fc ^ ((fr >> 1) & 3)) * 4);
+  const size_t fsrc = (fgr >= 0 ? static_cast<size_t>(fgr) * W : 0) + fc * 4;
+
+  const int row = rg * 32 + lane;
+  const uint32_t laneoff = static_cast<uint32_t>(row) * 4u;
+  const int rsw = (kw ^ ((row >> 1) & 3)) * 4;
+  const unsigned char* lut_bytes = reinterpret_cast<const unsigned char*>(lut_s);
+
+  for (int t0 = 0; t0 < it.n; t0 += kTok) {
+    const int nt = min(kTok, it.n - t0);
+    const int xt = tid >> 7, xc = tid & 127;        // token staging: thread -> (token, 16 B)
+    const float* trow = (xt < nt) ? token_row<KIND>(p, it.off + t0 + xt, K) : nullptr;
+
+    auto fill = [&](int c, int s) {
+      const int wsrc = c * kStageWords + fc * 4;
+      if (fgr >= 0 && wsrc < W) {
+        uint32_t* dst = pl_s + s * (kPlaneStageBytes / 4) + fdst;
+#pragma unroll
+        for (int pl = 0; pl < PW_MAX_BITS; ++pl)   // static indices keep the descriptor in registers
+          if (pl < Q) cp_async16(dst + pl * kRows * kStageWords, d.planes[pl] + fsrc + c * kStageWords);
+      }
+      const int kk = c * kStageK + xc * 4;
+      if (trow && kk < K) cp_async16(x_s + s * (kXStageBytes / 4) + xt * kStageK + xc * 4, trow + kk);
+      cp_commit();
+    };
+
+    fill(0, 0);
+    if (t0 == 0) {
+      // this tile's tables: LUT_q[row][v] fp16 -> lut_s[v][row] fp32 (overlaps stage 0)
+      const int i = tid & 63;
+      const int gr = global_row<KIND>(p, it.tile, i);
+      for (int vc = tid >> 6; vc * 8 < V; vc += 4) {
+        float f[8];
+        if (gr >= 0) {
+          const uint4 raw = __ldg(reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(gr) * V + vc * 8));
           const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -150,51 +186,22 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
             f[2 * e] = ff.x;
             f[2 * e + 1] = ff.y;
           }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] = 0.f;
         }
-      } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = 0.f;
+        for (int e = 0; e < 8; ++e) lut_s[(vc * 8 + e) * kRows + i] = f[e];
       }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) lut_s[(vc * 8 + e) * kRows + i] = f[e];
     }
-  }
 
-  const int row = rg * 32 + lane;
-  const uint32_t laneoff = static_cast<uint32_t>(row) * 4u;
-  const int swz = (row >> 1) & 3;
-  const unsigned char* lut_bytes = reinterpret_cast<const unsigned char*>(lut_s);
-
-  for (int t0 = 0; t0 < it.n; t0 += kTok) {
-    const int nt = min(kTok, it.n - t0);
-
-    auto fill = [&](int c, int s) {
-      // planes: thread -> (row, 16-byte chunk), one chunk per plane
-      const int fr = tid >> 2, c4 = tid & 3;
-      const int gr = global_row<KIND>(p, it.tile, fr);
-      const int wsrc = c * kStageWords + c4 * 4;
-      if (gr >= 0 && wsrc < W) {
-        uint32_t* dst = pl_s + s * (kPlaneStageBytes / 4) + fr * kStageWords + ((c4 ^ ((fr >> 1) & 3)) * 4);
+    // four independent accumulator pairs per token keep the FMA chains short
+    float ax[kTok][4], ay[kTok][4];
 #pragma unroll
-        for (int pl = 0; pl < Q; ++pl)
-          cp_async16(dst + pl * kRows * kStageWords, d.planes[pl] + static_cast<size_t>(gr) * W + wsrc);
-      }
-      // tokens: nt x 512 floats
-      for (int q4 = tid; q4 < nt * (kStageK / 4); q4 += kThreads) {
-        const int tt = q4 / (kStageK / 4), cc = q4 % (kStageK / 4);
-        const int kk = c * kStageK + cc * 4;
-        if (kk < K)
-          cp_async16(x_s + s * (kXStageBytes / 4) + tt * kStageK + cc * 4,
-                     token_row<KIND>(p, it.off + t0 + tt, K) + kk);
-      }
-      cp_commit();
-    };
-
-    float ax[kTok], ay[kTok];
+    for (int t = 0; t < kTok; ++t)
 #pragma unroll
-    for (int t = 0; t < kTok; ++t) ax[t] = ay[t] = 0.f;
+      for (int m = 0; m < 4; ++m) ax[t][m] = ay[t][m] = 0.f;
 
-    fill(0, 0);
     for (int c = 0; c < nchunk; ++c) {
       const int s = c & 1;
       if (c + 1 < nchunk) {
@@ -208,26 +215,20 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
       const int wbase = c * kStageWords + kw * 4;
       const int nw = min(4, W - wbase);
       if (nw > 0) {
-        const uint32_t* ps = pl_s + s * (kPlaneStageBytes / 4) + row * kStageWords + ((kw ^ swz) * 4);
+        const uint32_t* ps = pl_s + s * (kPlaneStageBytes / 4) + row * kStageWords + rsw;
         uint4 pv[PW_MAX_BITS];
 #pragma unroll
-        for (int pl = 0; pl < Q; ++pl) pv[pl] = *reinterpret_cast<const uint4*>(ps + pl * kRows * kStageWords);
+        for (int pl = 0; pl < PW_MAX_BITS; ++pl)
+          pv[pl] = (pl < Q) ? *reinterpret_cast<const uint4*>(ps + (Q - 1 - pl) * kRows * kStageWords)
+                            : make_uint4(0u, 0u, 0u, 0u);   // pv[r] = plane (q-1-r)
         const float* xs = x_s + s * (kXStageBytes / 4) + kw * 128;
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi) {
           if (wi < nw) {
-            uint32_t pw_[PW_MAX_BITS];
-#pragma unroll
-            for (int pl = 0; pl < PW_MAX_BITS; ++pl) {
-              if (pl < Q) {
-                const uint4 v = pv[pl];
-                pw_[pl] = wi == 0 ? v.x : wi == 1 ? v.y : wi == 2 ? v.z : v.w;
-              } else {
-                pw_[pl] = 0u;
-              }
-            }
             uint32_t o[8];
-            planes_to_indices<Q>(pw_, o);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) o[r] = wi == 0 ? pv[r].x : wi == 1 ? pv[r].y : wi == 2 ? pv[r].z : pv[r].w;
+            planes_to_indices(o);
             float wv[32];
 #pragma unroll
             for (int bb = 0; bb < 4; ++bb)
@@ -243,8 +244,9 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                   const float4 xv = xr[j4];
-                  ffma2(ax[t], ay[t], wv[4 * j4], wv[4 * j4 + 1], xv.x, xv.y);
-                  ffma2(ax[t], ay[t], wv[4 * j4 + 2], wv[4 * j4 + 3], xv.z, xv.w);
+                  const int m0 = (2 * j4) & 3, m1 = (2 * j4 + 1) & 3;
+                  ffma2(ax[t][m0], ay[t][m0], wv[4 * j4], wv[4 * j4 + 1], xv.x, xv.y);
+                  ffma2(ax[t][m1], ay[t][m1], wv[4 * j4 + 2], wv[4 * j4 + 3], xv.z, xv.w);
                 }
               }
             }
@@ -257,7 +259,9 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
     // ---- partial sums of the four K-warps, added in a fixed order
 #pragma unroll
     for (int t = 0; t < kTok; ++t)
-      if (t < nt) red_s[(kw * kTok + t) * kRows + row] = ax[t] + ay[t];
+      if (t < nt)
+        red_s[(kw * kTok + t) * kRows + row] =
+            ((ax[t][0] + ay[t][0]) + (ax[t][1] + ay[t][1])) + ((ax[t][2] + ay[t][2]) + (ax[t][3] + ay[t][3]));
     __syncthreads();
     if (KIND == PW_KIND_GATE_UP) {
       for (int q = tid; q < nt * 32; q += kThreads) {
@@ -296,29 +300,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(Fwd p) {
   const int nact = p.active[0];
   const int total = nact * tiles;
   int* ctr = reinterpret_cast<int*>(p.status) + (KIND == PW_KIND_GATE_UP ? kCtrGateUp : kCtrDown);
-  for (;;) {
-    if (threadIdx.x == 0) *s_item = atomicAdd(ctr, 1);
-    __syncthreads();
-    const int item = *s_item;
-    __syncthreads();
+  if (threadIdx.x == 0) s_item[0] = atomicAdd(ctr, 1);
+  __syncthreads();
+  for (int slot = 0;; slot ^= 1) {
+    const int item = s_item[slot];
     if (item >= total) break;
+    // claim the next item now; it is read after this item's barriers
+    if (threadIdx.x == 0) s_item[slot ^ 1] = atomicAdd(ctr, 1);
     Item it;
     it.expert = p.active[1 + item / tiles];
     it.tile = item % tiles;
     it.n = p.counts[it.expert];
     it.off = p.offsets[it.expert];
     const BlockDesc d = *block_desc(p, it.expert, KIND);
-    switch (d.q) {
-      case 3: run_tile<3, KIND>(p, d, it, smem); break;
-      case 4: run_tile<4, KIND>(p, d, it, smem); break;
-      case 5: run_tile<5, KIND>(p, d, it, smem); break;
-      case 6: run_tile<6, KIND>(p, d, it, smem); break;
-      case 7: run_tile<7, KIND>(p, d, it, smem); break;
-      case 8: run_tile<8, KIND>(p, d, it, smem); break;
-      default:
-        if (threadIdx.x == 0) atomicOr(p.status, PW_STATUS_BAD_DESC);
-        break;
+    if (d.q >= 1 && d.q <= PW_MAX_BITS && d.K == (KIND == PW_KIND_GATE_UP ? p.H : p.I)) {
+      run_tile<KIND>(p, d, it, smem);
+    } else if (threadIdx.x == 0) {
+      atomicOr(p.status, PW_STATUS_BAD_DESC);
     }
+    __syncthreads();
   }
 }
 
