@@ -61,6 +61,7 @@ _SIGS = {
     "pw_moe_forward": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "pw_moe_forward_host": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "pw_workspace_status": (_i, [_vp, _vp, _pi]),
+    "pw_moe_forward_noalloc": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp]),
     "pw_profile_attach": (_i, [ctypes.POINTER(_vp), _i]),
 }
 
@@ -263,6 +264,20 @@ class PagedMoE:
                                          int(renorm), _ptr(residual_host), _ptr(out_host), _ptr(ws),
                                          ws.numel(), _stream(stream)), "pw_moe_forward_host")
         return out_host
+
+    def pw_moe_forward_noalloc(self, layer, x, logits, top_k, renorm, residual=None, out=None,
+                               stream=None):
+        """pw_moe_forward without a caller workspace: the library's fixed 8 MiB
+        device scratch is used instead (for callers that cannot allocate).
+        Calls that overlap on the GPU race on that scratch."""
+        import torch
+        assert x.dtype == torch.float16 and logits.dtype == torch.float32
+        if out is None:
+            out = torch.empty_like(x)
+        _check(lib().pw_moe_forward_noalloc(self._t, layer, _ptr(x), _ptr(logits), x.shape[0], top_k,
+                                            int(renorm), _ptr(residual), _ptr(out), _stream(stream)),
+               "pw_moe_forward_noalloc")
+        return out
 
     @staticmethod
     def workspace_status(ws, stream=None) -> int:

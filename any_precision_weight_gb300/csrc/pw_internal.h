@@ -98,6 +98,11 @@ struct ForwardArgs {
   cudaEvent_t prof[5];     // boundary events (pw_profile_attach), or all null
 };
 
+// Host helpers (pw_runtime.cpp): sets this thread's pw_last_error message and
+// returns `code`; reads a table's expert count and sizes.
+int set_error(int code, const char* msg);
+int table_shape(const pw_table* t, int* E, int* H, int* I);
+
 // Kernel launchers (pw_kernels.cu).  Return cudaSuccess or the launch error.
 cudaError_t launch_commit(BlockDesc* dst, const BlockDesc& value, cudaStream_t s);
 cudaError_t launch_forward(const ForwardArgs& a, cudaStream_t s);

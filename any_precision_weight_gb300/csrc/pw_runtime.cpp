@@ -138,6 +138,23 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 }  // namespace
 
+namespace pw {
+
+int set_error(int code, const char* msg) {
+  g_err = msg;
+  return code;
+}
+
+int table_shape(const pw_table* t, int* E, int* H, int* I) {
+  if (!t) return PW_EINVAL;
+  *E = t->E;
+  *H = t->H;
+  *I = t->I;
+  return PW_OK;
+}
+
+}  // namespace pw
+
 extern "C" {
 
 const char* pw_last_error(void) { return g_err.c_str(); }

@@ -1,0 +1,84 @@
+// pw_moe_forward_noalloc: the fused MoE layer forward for callers that cannot
+// allocate device memory.
+//
+// Some callers have no way to hand us a workspace: code that runs where every
+// device allocation is forbidden or already fixed up front (an inference
+// runtime that reserves its whole memory pool at start-up and rejects later
+// cudaMalloc calls, or a plugin host that only passes tensors in and out).
+// For them the forward's scratch (routing results, permutation, fp32 copies of
+// the tokens, the intermediate h and y rows) lives in one file-scope device
+// array of fixed size, reserved on every GPU that loads this library for as
+// long as the process lives.  Nothing here calls cudaMalloc, cudaFree or any
+// allocating library routine.
+
+#include <cstdio>
+#include <mutex>
+
+#include "pw_internal.h"
+
+namespace pw {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;   // 8 MiB per device
+
+// Scratch for pw_moe_forward_noalloc.  Host code must not use this name as a
+// pointer: it is a host-side stand-in; the device address comes from
+// cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_ptr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+// Device address of the scratch array on the current device, looked up once per
+// device (the lookup may load this library's kernels onto the device).
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace pw
+
+extern "C" int pw_moe_forward_noalloc(pw_table* t, int layer, const void* x, const float* logits,
+                                      int T, int top_k, int renorm, const void* residual, void* out,
+                                      pw_stream_t compute) {
+  int E = 0, H = 0, I = 0;   // the table's shapes size the scratch layout
+  if (!t || pw::table_shape(t, &E, &H, &I) != PW_OK)
+    return pw::set_error(PW_EINVAL, "pw_moe_forward_noalloc: null or invalid table");
+  if (T < 0 || top_k < 1 || top_k > E)
+    return pw::set_error(PW_EINVAL, "pw_moe_forward_noalloc: bad T or top_k");
+  const size_t need = pw_workspace_bytes(T, E, top_k, H, I);
+  if (need > pw::kStaticScratchBytes) {
+    char msg[200];
+    snprintf(msg, sizeof msg,
+             "pw_moe_forward_noalloc: this batch needs %zu bytes of scratch, more than the %zu "
+             "reserved; use pw_moe_forward with your own workspace",
+             need, pw::kStaticScratchBytes);
+    return pw::set_error(PW_ENOMEM, msg);
+  }
+  void* ws = nullptr;
+  const cudaError_t e = pw::scratch_address(&ws);
+  if (e != cudaSuccess) {
+    char msg[200];
+    snprintf(msg, sizeof msg, "pw_moe_forward_noalloc: scratch lookup failed: %s",
+             cudaGetErrorString(e));
+    return pw::set_error(PW_ECUDA, msg);
+  }
+  // Every word the forward reads from its workspace is written earlier in the
+  // same forward (the status word and work counters are reset by its first
+  // kernel), so the previous call's leftovers need no clearing.
+  return pw_moe_forward(t, layer, x, logits, T, top_k, renorm, residual, out, nullptr, nullptr,
+                        nullptr, nullptr, ws, pw::kStaticScratchBytes, compute);
+}

@@ -235,6 +235,33 @@ int pw_moe_forward_host(pw_table* t, int layer, const void* x_host, const float*
                         void* out_host, void* workspace, size_t ws_bytes, pw_stream_t compute);
 
 /*
+ * pw_moe_forward_noalloc -- the same layer as pw_moe_forward for callers that
+ * cannot allocate device memory (for example a runtime that reserves all of its
+ * GPU memory at start-up and refuses later allocations, or a host that only
+ * passes input and output buffers).  The paper has no counterpart: this is a
+ * deployment convenience of this library.
+ *   Scratch: a fixed 8 MiB device array inside the library, reserved on every
+ *   GPU that loads it until the process exits; batches whose
+ *   pw_workspace_bytes(T, E, top_k, H, I) exceeds 8 MiB are rejected with
+ *   PW_ENOMEM and a message (use pw_moe_forward with your own workspace then).
+ *   Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *   The first call on a device looks the array's address up on that device
+ *   (this may load the library's kernels there); make that first call before
+ *   capturing any stream.
+ *   All calls share the one array and it keeps the previous call's contents
+ *   (every value a call reads is written earlier by the same call): two calls
+ *   whose GPU work overlaps in time race on it, so keep them on one stream or
+ *   otherwise ordered.
+ *   x, logits, residual, out, T, top_k, renorm, compute: as pw_moe_forward
+ *   (no routing outputs).
+ * Errors: as pw_moe_forward, PW_ENOMEM when the batch does not fit, PW_ECUDA
+ * when the address lookup fails.
+ */
+int pw_moe_forward_noalloc(pw_table* t, int layer, const void* x, const float* logits, int T,
+                           int top_k, int renorm, const void* residual, void* out,
+                           pw_stream_t compute);
+
+/*
  * pw_workspace_status -- reads the device status word of a workspace after the
  * work already on stream s (synchronises s).  *status is 0 or an OR of the
  * PW_STATUS_* bits set by the last forward that used this workspace.
