@@ -30,13 +30,14 @@
 #include <cuda_fp16.h>
 #include <cstdint>
 
-#include "pw_device.cuh"
+#include "pw_route.cuh"
 
 namespace pw {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kCtasPerSm = 1;
+constexpr int kCtasPerSm = 2;        // two CTAs overlap each other's loads
+constexpr int kStages = 1;           // plane/token stage buffers per CTA
 constexpr int kRows = 64;            // rows per tile
 constexpr int kStageWords = 16;      // plane words per row per stage (4 per K-warp)
 constexpr int kStageK = kStageWords * 32;
@@ -45,7 +46,7 @@ constexpr int kLutBytes = 256 * kRows * 4;
 constexpr int kPlaneStageBytes = PW_MAX_BITS * kRows * kStageWords * 4;
 constexpr int kXStageBytes = kTok * kStageK * 4;
 constexpr int kRedBytes = 4 * kTok * kRows * 4;
-constexpr int kSmemBytes = kLutBytes + 2 * kPlaneStageBytes + 2 * kXStageBytes + kRedBytes + 64;
+constexpr int kSmemBytes = kLutBytes + kStages * kPlaneStageBytes + kStages * kXStageBytes + kRedBytes + 64;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -131,8 +132,8 @@ template <int KIND>
 __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsigned char* smem) {
   float* lut_s = reinterpret_cast<float*>(smem);
   uint32_t* pl_s = reinterpret_cast<uint32_t*>(smem + kLutBytes);
-  float* x_s = reinterpret_cast<float*>(smem + kLutBytes + 2 * kPlaneStageBytes);
-  float* red_s = reinterpret_cast<float*>(smem + kLutBytes + 2 * kPlaneStageBytes + 2 * kXStageBytes);
+  float* x_s = reinterpret_cast<float*>(smem + kLutBytes + kStages * kPlaneStageBytes);
+  float* red_s = reinterpret_cast<float*>(smem + kLutBytes + kStages * kPlaneStageBytes + kStages * kXStageBytes);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rg = warp >> 2, kw = warp & 3;
@@ -203,8 +204,8 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
       for (int m = 0; m < 4; ++m) ax[t][m] = ay[t][m] = 0.f;
 
     for (int c = 0; c < nchunk; ++c) {
-      const int s = c & 1;
-      if (c + 1 < nchunk) {
+      const int s = (kStages == 2) ? (c & 1) : 0;
+      if (kStages == 2 && c + 1 < nchunk) {
         fill(c + 1, s ^ 1);
         cp_wait<1>();
       } else {
@@ -254,6 +255,7 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
         }
       }
       __syncthreads();
+      if (kStages == 1 && c + 1 < nchunk) fill(c + 1, 0);
     }
 
     // ---- partial sums of the four K-warps, added in a fixed order
@@ -293,7 +295,7 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1) k_decode(Fwd p) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) k_decode(Fwd p) {
   extern __shared__ __align__(128) unsigned char smem[];
   int* s_item = reinterpret_cast<int*>(smem + kSmemBytes - 64);
   const int tiles = (KIND == PW_KIND_GATE_UP) ? p.I / 32 : (p.H + kRows - 1) / kRows;
@@ -322,8 +324,135 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(Fwd p) {
   }
 }
 
+// ------------------------------------------------------------------ fused layer
+
+constexpr int kSpinLimit = 1 << 22;   // ~0.3 s of polling before a wait gives up
+
+__device__ __forceinline__ int ld_acquire(const int* ptr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int* ptr, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+// Bounded wait (one thread): true once *ptr == want, false when the limit runs out.
+__device__ bool wait_eq(const int* ptr, int want) {
+  for (int i = 0; i < kSpinLimit; ++i) {
+    if (ld_acquire(ptr) == want) return true;
+    __nanosleep(64);
+  }
+  return false;
+}
+
+// Active experts ordered by the cost of their gate_up work, largest first
+// (longest-processing-time order keeps the tail of the work queue short).
+__device__ void build_lpt(const Fwd& p) {
+  const int na = p.active[0];
+  p.act_lpt[0] = na;
+  for (int a = 0; a < na; ++a) {
+    const int e = p.active[1 + a];
+    const int cost = (block_desc(p, e, PW_KIND_GATE_UP)->q + 2) * ((p.counts[e] + kTok - 1) / kTok);
+    int b = a;
+    while (b > 0) {   // insertion sort: cost descending, expert ascending on ties
+      const int f = p.act_lpt[b];
+      const int cf = (block_desc(p, f, PW_KIND_GATE_UP)->q + 2) * ((p.counts[f] + kTok - 1) / kTok);
+      if (cf >= cost) break;
+      p.act_lpt[1 + b] = f;
+      --b;
+    }
+    p.act_lpt[1 + b] = e;
+  }
+}
+
+// One persistent cooperative launch for the whole decode layer.
+// CTA 0 routes the batch and publishes a ready epoch; then every CTA takes
+// items from one queue: first all (expert, gate_up tile) items, then all
+// (expert, down tile) items.  A down item first waits until its expert's
+// gate_up tiles are all done; the last down item of a 64-row tile of H (over
+// all active experts) combines that tile's output rows.  Every wait is bounded
+// and reports PW_STATUS_TIMEOUT instead of hanging.
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  int* s_int = reinterpret_cast<int*>(smem + kSmemBytes - 64);
+  const int tiles_gu = p.I / 32, tiles_dn = (p.H + kRows - 1) / kRows;
+  int* queue = p.sync + 1;
+  int* expert_done = p.sync + 2;
+  int* tile_done = p.sync + 2 + p.E;
+
+  if (blockIdx.x == 0) {
+    if (threadIdx.x == 0) p.status[0] = 0u;
+    for (int i = threadIdx.x; i < 1 + p.E + tiles_dn; i += blockDim.x) queue[i] = 0;
+    for (int i = threadIdx.x; i < p.T * p.H / 8; i += blockDim.x) convert8(p, i);
+    __syncthreads();
+    route_permute_block(p, reinterpret_cast<int*>(smem), reinterpret_cast<int*>(smem) + kMaxE);
+    __syncthreads();
+    if (threadIdx.x == 0) build_lpt(p);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) st_release(p.sync, static_cast<int>(p.epoch));
+  } else {
+    if (threadIdx.x == 0) {
+      const bool ok = wait_eq(p.sync, static_cast<int>(p.epoch));
+      if (!ok) atomicOr(p.status, PW_STATUS_TIMEOUT);
+      s_int[2] = ok;
+    }
+    __syncthreads();
+    if (!s_int[2]) return;
+  }
+
+  const int nact = p.act_lpt[0];
+  const int n_gu = nact * tiles_gu, total = n_gu + nact * tiles_dn;
+  if (threadIdx.x == 0) s_int[0] = atomicAdd(queue, 1);
+  __syncthreads();
+  for (int slot = 0;; slot ^= 1) {
+    const int item = s_int[slot];
+    if (item >= total) break;
+    if (threadIdx.x == 0) s_int[slot ^ 1] = atomicAdd(queue, 1);   // claim the next one now
+    const bool gu = item < n_gu;
+    const int rank = gu ? item / tiles_gu : (item - n_gu) / tiles_dn;
+    Item it;
+    it.expert = p.act_lpt[1 + rank];
+    it.tile = gu ? item % tiles_gu : (item - n_gu) % tiles_dn;
+    it.n = p.counts[it.expert];
+    it.off = p.offsets[it.expert];
+    const int kind = gu ? PW_KIND_GATE_UP : PW_KIND_DOWN;
+    const BlockDesc d = *block_desc(p, it.expert, kind);
+    const bool ok = d.q >= 1 && d.q <= PW_MAX_BITS && d.K == (gu ? p.H : p.I);
+    if (!gu) {
+      if (threadIdx.x == 0 && !wait_eq(&expert_done[it.expert], tiles_gu))
+        atomicOr(p.status, PW_STATUS_TIMEOUT);
+      __syncthreads();
+    }
+    if (ok) {
+      if (gu) run_tile<PW_KIND_GATE_UP>(p, d, it, smem);
+      else run_tile<PW_KIND_DOWN>(p, d, it, smem);
+    } else if (threadIdx.x == 0) {
+      atomicOr(p.status, PW_STATUS_BAD_DESC);
+    }
+    __threadfence();   // this thread's h / y writes before the counters below
+    __syncthreads();
+    if (gu) {
+      if (threadIdx.x == 0) atomicAdd(&expert_done[it.expert], 1);
+    } else {
+      if (threadIdx.x == 0) {
+        s_int[2] = (atomicAdd(&tile_done[it.tile], 1) == nact - 1);
+        __threadfence();
+      }
+      __syncthreads();
+      if (s_int[2]) {
+        __threadfence();
+        const int r0 = it.tile * kRows;
+        combine_rows(p, r0, min(r0 + kRows, p.H), 0, p.T, threadIdx.x, blockDim.x);
+      }
+    }
+    __syncthreads();
+  }
+}
+
 constexpr int kMaxDevices = 64;
-int g_sms[kMaxDevices] = {};   // SM count per device once configured (0: not yet)
+int g_sms[kMaxDevices] = {};     // decode grid per device once configured (0: not yet)
+int g_fused[kMaxDevices] = {};   // cooperative grid of the fused layer per device
 
 }  // namespace
 
@@ -341,13 +470,34 @@ cudaError_t launch_decode(const Fwd& p, int kind, cudaStream_t s) {
     int sms = 0;
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    g_sms[dev] = sms > 0 ? sms : 1;
+    g_sms[dev] = (sms > 0 ? sms : 1) * kCtasPerSm;
   }
   if (kind == PW_KIND_GATE_UP)
     k_decode<PW_KIND_GATE_UP><<<g_sms[dev], kThreads, kSmemBytes, s>>>(p);
   else
     k_decode<PW_KIND_DOWN><<<g_sms[dev], kThreads, kSmemBytes, s>>>(p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_layer_fused(const Fwd& p, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (g_fused[dev] == 0) {   // once per device: shared-memory opt-in and co-resident grid size
+    e = cudaFuncSetAttribute(k_layer, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    int per_sm = 0, sms = 0;
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_layer, kThreads, kSmemBytes);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    g_fused[dev] = per_sm * sms;
+  }
+  Fwd arg = p;
+  void* args[] = {&arg};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(k_layer), dim3(g_fused[dev]),
+                                     dim3(kThreads), args, kSmemBytes, s);
 }
 
 }  // namespace pw

@@ -27,7 +27,12 @@ struct Fwd {
   int32_t* offsets;         // [E+1]
   int32_t* perm;            // [T*k]
   int32_t* inv;             // [T*k]
-  int32_t* active;          // [E+1]
+  int32_t* active;          // [E+1] active experts: count, then ids (expert order)
+  int32_t* act_lpt;         // [E+1] the same, most expensive gate_up block first
+  int32_t* sync;            // fused path: [0] ready epoch, [1] work queue,
+                            // [2, 2+E) gate_up tiles done per expert, then
+                            // down items done per 64-row tile of H
+  uint32_t epoch;           // nonzero, differs between consecutive fused forwards
   float* xf;                // [T][H]   x as fp32
   float* hf;                // [T*k][I] h rounded to fp16, held as fp32
   float* y;                 // [T*k][H]
@@ -43,5 +48,9 @@ __device__ __forceinline__ const BlockDesc* block_desc(const Fwd& p, int e, int 
 
 // Decode GEMV of one block kind (gate_up or down) over all active experts.
 cudaError_t launch_decode(const Fwd& p, int kind, cudaStream_t s);
+// The whole decode layer (routing, gate_up, down, combine) in one cooperative
+// persistent launch; for batches of at most kFusedMaxT tokens.
+constexpr int kFusedMaxT = 64;
+cudaError_t launch_layer_fused(const Fwd& p, cudaStream_t s);
 
 }  // namespace pw

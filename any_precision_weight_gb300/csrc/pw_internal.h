@@ -43,7 +43,8 @@ struct Workspace {
   size_t offsets;    // int32 [E+1]
   size_t perm;       // int32 [T*k]
   size_t inv;        // int32 [T*k]
-  size_t active;     // int32 [E+1]: number of active experts, then their ids
+  size_t active;     // int32 [2][E+1]: active experts (count, ids); same, cost-sorted
+  size_t sync;       // int32: ready epoch, work queue, per-expert and per-row-tile counters
   size_t xf;         // f32 [T][H]: x converted once
   size_t hf;         // f32 [T*k][I] in perm order: h rounded to fp16, held as fp32
   size_t y;          // f32 [T*k][H] in perm order
@@ -68,7 +69,8 @@ inline Workspace workspace_layout(int T, int E, int k, int H, int I) {
   w.offsets = take(static_cast<size_t>(E + 1) * 4);
   w.perm = take(P * 4);
   w.inv = take(P * 4);
-  w.active = take(static_cast<size_t>(E + 1) * 4);
+  w.active = take(static_cast<size_t>(E + 1) * 2 * 4);
+  w.sync = take(static_cast<size_t>(8 + E + (H + 63) / 64) * 4);
   w.xf = take(static_cast<size_t>(T) * H * 4);
   w.hf = take(P * I * 4);
   w.y = take(P * H * 4);
