@@ -8,24 +8,24 @@
 // kernels stream each active block's q bit-planes and q-bit table from HBM
 // exactly once and keep the tokens on chip.  Design:
 //
-//  * persistent CTAs (one per SM) pull (active expert, 64-row tile) items from
+//  * persistent CTAs (two per SM) pull (active expert, 32-row tile) items from
 //    a device work queue, so the committed q of each block is read from the
 //    page table on the device and the grid never depends on the routing;
-//  * a tile is 64 rows x all of K; warps = 2 row groups x 4 K-warps; lane l of
-//    a row group owns row l, so the 64 rows' tables sit in shared memory as
-//    fp32 [v][64 rows]: the 32 lanes of a warp always hit 32 different banks,
+//  * a tile is 32 rows x all of K; lane l of each of the 8 warps owns row l,
+//    the warps split K; the 32 rows' tables sit in shared memory as fp32
+//    [v][row], so the 32 lanes of a warp always hit 32 different banks,
 //    whatever their indices (conflict-free lookups at every q);
 //  * bit-planes are staged global->shared with cp.async in 16-word (512-k)
-//    chunks, double buffered, XOR-swizzled so the 128-bit reads of 32 rows
-//    are conflict-free; tokens are staged the same way (fp32);
-//  * per 32-bit plane word a lane turns q plane words into 32 q-bit indices
-//    with an 8x8 bit-matrix transpose done four bytes at a time (delta swaps),
-//    then one byte permute per element forms the table address
+//    chunks, double buffered, with the 16-byte chunks XOR-swizzled by row;
+//    tokens are staged the same way (fp32), two tokens per pass;
+//  * per 32-bit plane word a lane turns the q plane words into 32 q-bit
+//    indices with an 8x8 bit-matrix transpose done four bytes at a time (delta
+//    swaps), then one byte permute per element forms the table address
 //    (index * 256 + row * 4);
-//  * products accumulate in fp32 with packed two-wide FMAs; the four K-warps'
+//  * products accumulate in fp32 with packed two-wide FMAs; the eight K-warps'
 //    partial sums are added in a fixed order (deterministic results).
-// gate_up tiles hold 32 gate rows and the 32 matching up rows and finish with
-// h = silu(gate) * up rounded to fp16; down tiles hold 64 rows of y (fp32).
+// gate_up tiles hold 16 gate rows and the 16 matching up rows and finish with
+// h = silu(gate) * up rounded to fp16; down tiles hold 32 rows of y (fp32).
 
 #include <cuda_fp16.h>
 #include <cstdint>
@@ -36,17 +36,17 @@ namespace pw {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kCtasPerSm = 2;        // two CTAs overlap each other's loads
-constexpr int kStages = 1;           // plane/token stage buffers per CTA
-constexpr int kRows = 64;            // rows per tile
-constexpr int kStageWords = 16;      // plane words per row per stage (4 per K-warp)
+constexpr int kCtasPerSm = 2;        // two CTAs per SM overlap each other's item start-up
+constexpr int kRows = 32;            // rows per tile: lane l of every warp owns row l
+constexpr int kKW = 8;               // K-warps: each warp takes 2 of a stage's 16 words per row
+constexpr int kStageWords = 16;      // plane words per row per stage
 constexpr int kStageK = kStageWords * 32;
 constexpr int kTok = 2;              // tokens per pass over a tile
-constexpr int kLutBytes = 256 * kRows * 4;
+constexpr int kLutBytes = 256 * 64 * 4;   // [v][64 slots] fp32; slot = row (byte-permute addressing)
 constexpr int kPlaneStageBytes = PW_MAX_BITS * kRows * kStageWords * 4;
 constexpr int kXStageBytes = kTok * kStageK * 4;
-constexpr int kRedBytes = 4 * kTok * kRows * 4;
-constexpr int kSmemBytes = kLutBytes + kStages * kPlaneStageBytes + kStages * kXStageBytes + kRedBytes + 64;
+constexpr int kRedBytes = kKW * kTok * kRows * 4;
+constexpr int kSmemBytes = kLutBytes + 2 * kPlaneStageBytes + 2 * kXStageBytes + kRedBytes + 64;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -108,14 +108,14 @@ struct Item {
   int expert, tile, n, off;
 };
 
-// Global row of tile row i: gate_up tiles are 32 gate rows + the 32 matching
-// up rows; down tiles are 64 consecutive rows.  Returns -1 past the block.
+// Global row of tile row i: gate_up tiles are 16 gate rows + the 16 matching
+// up rows; down tiles are 32 consecutive rows.  Returns -1 past the block.
 template <int KIND>
 __device__ __forceinline__ int global_row(const Fwd& p, int tile, int i) {
   if (KIND == PW_KIND_GATE_UP) {
-    const int r = tile * 32 + (i & 31);
+    const int r = tile * 16 + (i & 15);
     if (r >= p.I) return -1;
-    return (i < 32) ? r : p.I + r;
+    return (i < 16) ? r : p.I + r;
   } else {
     const int r = tile * kRows + i;
     return (r < p.H) ? r : -1;
@@ -132,25 +132,24 @@ template <int KIND>
 __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsigned char* smem) {
   float* lut_s = reinterpret_cast<float*>(smem);
   uint32_t* pl_s = reinterpret_cast<uint32_t*>(smem + kLutBytes);
-  float* x_s = reinterpret_cast<float*>(smem + kLutBytes + kStages * kPlaneStageBytes);
-  float* red_s = reinterpret_cast<float*>(smem + kLutBytes + kStages * kPlaneStageBytes + kStages * kXStageBytes);
+  float* x_s = reinterpret_cast<float*>(smem + kLutBytes + 2 * kPlaneStageBytes);
+  float* red_s = reinterpret_cast<float*>(smem + kLutBytes + 2 * kPlaneStageBytes + 2 * kXStageBytes);
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rg = warp >> 2, kw = warp & 3;
+  const int tid = threadIdx.x, lane = tid & 31, kw = tid >> 5;
   const int K = d.K, W = K >> 5;
   const int Q = d.q, V = 1 << Q;
   const int nchunk = (W + kStageWords - 1) / kStageWords;
 
-  // plane staging: thread -> (tile row, 16-byte chunk); chunks are XOR-swizzled
-  // by row so a warp's 32 rows read 128-bit words conflict-free
-  const int fr = tid >> 2, fc = tid & 3;
+  // plane staging: threads 0..127 and 128..255 each cover the 32 rows x four
+  // 16-byte chunks, taking even and odd planes; chunks are XOR-swizzled by row
+  const int fr = (tid & 127) >> 2, fc = tid & 3, fpl = tid >> 7;
   const int fgr = global_row<KIND>(p, it.tile, fr);
   const int fdst = fr * kStageWords + ((fc ^ ((fr >> 1) & 3)) * 4);
   const size_t fsrc = (fgr >= 0 ? static_cast<size_t>(fgr) * W : 0) + fc * 4;
 
-  const int row = rg * 32 + lane;
+  const int row = lane;
   const uint32_t laneoff = static_cast<uint32_t>(row) * 4u;
-  const int rsw = (kw ^ ((row >> 1) & 3)) * 4;
+  const int rsw = (((kw >> 1) ^ ((row >> 1) & 3)) * 4) + (kw & 1) * 2;
   const unsigned char* lut_bytes = reinterpret_cast<const unsigned char*>(lut_s);
 
   for (int t0 = 0; t0 < it.n; t0 += kTok) {
@@ -163,8 +162,11 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
       if (fgr >= 0 && wsrc < W) {
         uint32_t* dst = pl_s + s * (kPlaneStageBytes / 4) + fdst;
 #pragma unroll
-        for (int pl = 0; pl < PW_MAX_BITS; ++pl)   // static indices keep the descriptor in registers
-          if (pl < Q) cp_async16(dst + pl * kRows * kStageWords, d.planes[pl] + fsrc + c * kStageWords);
+        for (int j = 0; j < PW_MAX_BITS / 2; ++j) {   // static indices keep the descriptor in registers
+          const int pl = 2 * j + fpl;
+          const uint32_t* src = fpl ? d.planes[2 * j + 1] : d.planes[2 * j];
+          if (pl < Q) cp_async16(dst + pl * kRows * kStageWords, src + fsrc + c * kStageWords);
+        }
       }
       const int kk = c * kStageK + xc * 4;
       if (trow && kk < K) cp_async16(x_s + s * (kXStageBytes / 4) + xt * kStageK + xc * 4, trow + kk);
@@ -174,9 +176,9 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
     fill(0, 0);
     if (t0 == 0) {
       // this tile's tables: LUT_q[row][v] fp16 -> lut_s[v][row] fp32 (overlaps stage 0)
-      const int i = tid & 63;
+      const int i = tid & 31;
       const int gr = global_row<KIND>(p, it.tile, i);
-      for (int vc = tid >> 6; vc * 8 < V; vc += 4) {
+      for (int vc = tid >> 5; vc * 8 < V; vc += kThreads / 32) {
         float f[8];
         if (gr >= 0) {
           const uint4 raw = __ldg(reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(gr) * V + vc * 8));
@@ -192,7 +194,7 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
           for (int e = 0; e < 8; ++e) f[e] = 0.f;
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) lut_s[(vc * 8 + e) * kRows + i] = f[e];
+        for (int e = 0; e < 8; ++e) lut_s[(vc * 8 + e) * 64 + i] = f[e];
       }
     }
 
@@ -204,8 +206,8 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
       for (int m = 0; m < 4; ++m) ax[t][m] = ay[t][m] = 0.f;
 
     for (int c = 0; c < nchunk; ++c) {
-      const int s = (kStages == 2) ? (c & 1) : 0;
-      if (kStages == 2 && c + 1 < nchunk) {
+      const int s = c & 1;
+      if (c + 1 < nchunk) {
         fill(c + 1, s ^ 1);
         cp_wait<1>();
       } else {
@@ -213,22 +215,22 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
       }
       __syncthreads();
 
-      const int wbase = c * kStageWords + kw * 4;
-      const int nw = min(4, W - wbase);
+      const int wbase = c * kStageWords + kw * 2;
+      const int nw = min(2, W - wbase);
       if (nw > 0) {
         const uint32_t* ps = pl_s + s * (kPlaneStageBytes / 4) + row * kStageWords + rsw;
-        uint4 pv[PW_MAX_BITS];
+        uint2 pv[PW_MAX_BITS];
 #pragma unroll
-        for (int pl = 0; pl < PW_MAX_BITS; ++pl)
-          pv[pl] = (pl < Q) ? *reinterpret_cast<const uint4*>(ps + (Q - 1 - pl) * kRows * kStageWords)
-                            : make_uint4(0u, 0u, 0u, 0u);   // pv[r] = plane (q-1-r)
-        const float* xs = x_s + s * (kXStageBytes / 4) + kw * 128;
+        for (int pl = 0; pl < PW_MAX_BITS; ++pl)   // pv[r] = plane (q-1-r)
+          pv[pl] = (pl < Q) ? *reinterpret_cast<const uint2*>(ps + (Q - 1 - pl) * kRows * kStageWords)
+                            : make_uint2(0u, 0u);
+        const float* xs = x_s + s * (kXStageBytes / 4) + kw * 64;
 #pragma unroll
-        for (int wi = 0; wi < 4; ++wi) {
+        for (int wi = 0; wi < 2; ++wi) {
           if (wi < nw) {
             uint32_t o[8];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) o[r] = wi == 0 ? pv[r].x : wi == 1 ? pv[r].y : wi == 2 ? pv[r].z : pv[r].w;
+            for (int r = 0; r < 8; ++r) o[r] = wi == 0 ? pv[r].x : pv[r].y;
             planes_to_indices(o);
             float wv[32];
 #pragma unroll
@@ -255,10 +257,9 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
         }
       }
       __syncthreads();
-      if (kStages == 1 && c + 1 < nchunk) fill(c + 1, 0);
     }
 
-    // ---- partial sums of the four K-warps, added in a fixed order
+    // ---- partial sums of the eight K-warps, added in a fixed order
 #pragma unroll
     for (int t = 0; t < kTok; ++t)
       if (t < nt)
@@ -266,14 +267,14 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
             ((ax[t][0] + ay[t][0]) + (ax[t][1] + ay[t][1])) + ((ax[t][2] + ay[t][2]) + (ax[t][3] + ay[t][3]));
     __syncthreads();
     if (KIND == PW_KIND_GATE_UP) {
-      for (int q = tid; q < nt * 32; q += kThreads) {
-        const int t = q >> 5, i = q & 31;
-        const int r = it.tile * 32 + i;
+      if (tid < nt * 16) {
+        const int t = tid >> 4, i = tid & 15;
+        const int r = it.tile * 16 + i;
         float g = 0.f, u = 0.f;
 #pragma unroll
-        for (int w4 = 0; w4 < 4; ++w4) {
-          g += red_s[(w4 * kTok + t) * kRows + i];
-          u += red_s[(w4 * kTok + t) * kRows + 32 + i];
+        for (int w8 = 0; w8 < kKW; ++w8) {
+          g += red_s[(w8 * kTok + t) * kRows + i];
+          u += red_s[(w8 * kTok + t) * kRows + 16 + i];
         }
         if (r < p.I) {
           const float hv = g / (1.f + expf(-g)) * u;
@@ -281,12 +282,12 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
         }
       }
     } else {
-      for (int q = tid; q < nt * kRows; q += kThreads) {
-        const int t = q >> 6, i = q & 63;
+      if (tid < nt * kRows) {
+        const int t = tid >> 5, i = tid & 31;
         const int r = it.tile * kRows + i;
         float yv = 0.f;
 #pragma unroll
-        for (int w4 = 0; w4 < 4; ++w4) yv += red_s[(w4 * kTok + t) * kRows + i];
+        for (int w8 = 0; w8 < kKW; ++w8) yv += red_s[(w8 * kTok + t) * kRows + i];
         if (r < p.H) p.y[static_cast<size_t>(it.off + t0 + t) * p.H + r] = yv;
       }
     }
@@ -298,7 +299,7 @@ template <int KIND>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_decode(Fwd p) {
   extern __shared__ __align__(128) unsigned char smem[];
   int* s_item = reinterpret_cast<int*>(smem + kSmemBytes - 64);
-  const int tiles = (KIND == PW_KIND_GATE_UP) ? p.I / 32 : (p.H + kRows - 1) / kRows;
+  const int tiles = (KIND == PW_KIND_GATE_UP) ? p.I / 16 : (p.H + kRows - 1) / kRows;
   const int nact = p.active[0];
   const int total = nact * tiles;
   int* ctr = reinterpret_cast<int*>(p.status) + (KIND == PW_KIND_GATE_UP ? kCtrGateUp : kCtrDown);
@@ -346,23 +347,22 @@ __device__ bool wait_eq(const int* ptr, int want) {
 }
 
 // Active experts ordered by the cost of their gate_up work, largest first
-// (longest-processing-time order keeps the tail of the work queue short).
-__device__ void build_lpt(const Fwd& p) {
+// (longest-processing-time order keeps the tail of the work queue short);
+// ties keep expert order.  Thread a ranks active expert a (block-wide).
+__device__ void build_lpt(const Fwd& p, int* s_cost) {
   const int na = p.active[0];
-  p.act_lpt[0] = na;
-  for (int a = 0; a < na; ++a) {
+  for (int a = threadIdx.x; a < na; a += blockDim.x) {
     const int e = p.active[1 + a];
-    const int cost = (block_desc(p, e, PW_KIND_GATE_UP)->q + 2) * ((p.counts[e] + kTok - 1) / kTok);
-    int b = a;
-    while (b > 0) {   // insertion sort: cost descending, expert ascending on ties
-      const int f = p.act_lpt[b];
-      const int cf = (block_desc(p, f, PW_KIND_GATE_UP)->q + 2) * ((p.counts[f] + kTok - 1) / kTok);
-      if (cf >= cost) break;
-      p.act_lpt[1 + b] = f;
-      --b;
-    }
-    p.act_lpt[1 + b] = e;
+    s_cost[a] = (block_desc(p, e, PW_KIND_GATE_UP)->q + 2) * ((p.counts[e] + kTok - 1) / kTok);
   }
+  __syncthreads();
+  for (int a = threadIdx.x; a < na; a += blockDim.x) {
+    const int c = s_cost[a];
+    int rank = 0;
+    for (int b = 0; b < na; ++b) rank += (s_cost[b] > c) || (s_cost[b] == c && b < a);
+    p.act_lpt[1 + rank] = p.active[1 + a];
+  }
+  if (threadIdx.x == 0) p.act_lpt[0] = na;
 }
 
 // One persistent cooperative launch for the whole decode layer.
@@ -375,7 +375,7 @@ __device__ void build_lpt(const Fwd& p) {
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
   extern __shared__ __align__(128) unsigned char smem[];
   int* s_int = reinterpret_cast<int*>(smem + kSmemBytes - 64);
-  const int tiles_gu = p.I / 32, tiles_dn = (p.H + kRows - 1) / kRows;
+  const int tiles_gu = p.I / 16, tiles_dn = (p.H + kRows - 1) / kRows;
   int* queue = p.sync + 1;
   int* expert_done = p.sync + 2;
   int* tile_done = p.sync + 2 + p.E;
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
     __syncthreads();
     route_permute_block(p, reinterpret_cast<int*>(smem), reinterpret_cast<int*>(smem) + kMaxE);
     __syncthreads();
-    if (threadIdx.x == 0) build_lpt(p);
+    build_lpt(p, reinterpret_cast<int*>(smem) + 2 * kMaxE + 2);
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) st_release(p.sync, static_cast<int>(p.epoch));

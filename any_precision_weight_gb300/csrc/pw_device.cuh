@@ -31,7 +31,7 @@ struct Fwd {
   int32_t* act_lpt;         // [E+1] the same, most expensive gate_up block first
   int32_t* sync;            // fused path: [0] ready epoch, [1] work queue,
                             // [2, 2+E) gate_up tiles done per expert, then
-                            // down items done per 64-row tile of H
+                            // down items done per 32-row tile of H
   uint32_t epoch;           // nonzero, differs between consecutive fused forwards
   float* xf;                // [T][H]   x as fp32
   float* hf;                // [T*k][I] h rounded to fp16, held as fp32

@@ -70,7 +70,7 @@ inline Workspace workspace_layout(int T, int E, int k, int H, int I) {
   w.perm = take(P * 4);
   w.inv = take(P * 4);
   w.active = take(static_cast<size_t>(E + 1) * 2 * 4);
-  w.sync = take(static_cast<size_t>(8 + E + (H + 63) / 64) * 4);
+  w.sync = take(static_cast<size_t>(8 + E + (H + 31) / 32) * 4);
   w.xf = take(static_cast<size_t>(T) * H * 4);
   w.hf = take(P * I * 4);
   w.y = take(P * H * 4);

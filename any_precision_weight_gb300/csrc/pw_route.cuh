@@ -103,15 +103,29 @@ __device__ __forceinline__ void route_permute_block(const Fwd& p, int* s_cnt, in
   __syncthreads();
   for (int i = threadIdx.x; i < T * k; i += blockDim.x) atomicAdd(&s_cnt[p.idx[i]], 1);
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {   // warp-level exclusive scan of counts and of the active flags
     int run = 0, na = 0;
-    for (int e = 0; e < E; ++e) {
-      s_off[e] = run;
-      run += s_cnt[e];
-      if (s_cnt[e]) p.active[1 + na++] = e;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + threadIdx.x;
+      const int c = e < E ? s_cnt[e] : 0;
+      int incl = c, act = c > 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        const int a = __shfl_up_sync(0xffffffffu, act, o);
+        if (threadIdx.x >= o) { incl += v; act += a; }
+      }
+      if (e < E) {
+        s_off[e] = run + incl - c;
+        if (c) p.active[1 + na + act - 1] = e;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+      na += __shfl_sync(0xffffffffu, act, 31);
     }
-    s_off[E] = run;
-    p.active[0] = na;
+    if (threadIdx.x == 0) {
+      s_off[E] = run;
+      p.active[0] = na;
+    }
   }
   __syncthreads();
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
