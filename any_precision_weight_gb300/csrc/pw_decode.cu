@@ -205,15 +205,13 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
 #pragma unroll
       for (int m = 0; m < 4; ++m) ax[t][m] = ay[t][m] = 0.f;
 
+    // one barrier per stage: it publishes stage c and proves every warp is done
+    // with stage c-1, whose buffer the fill for stage c+1 then reuses
     for (int c = 0; c < nchunk; ++c) {
       const int s = c & 1;
-      if (c + 1 < nchunk) {
-        fill(c + 1, s ^ 1);
-        cp_wait<1>();
-      } else {
-        cp_wait<0>();
-      }
+      cp_wait<0>();
       __syncthreads();
+      if (c + 1 < nchunk) fill(c + 1, s ^ 1);
 
       const int wbase = c * kStageWords + kw * 2;
       const int nw = min(2, W - wbase);
@@ -256,7 +254,6 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
           }
         }
       }
-      __syncthreads();
     }
 
     // ---- partial sums of the eight K-warps, added in a fixed order
