@@ -42,11 +42,16 @@ constexpr int kKW = 8;               // K-warps: each warp takes 2 of a stage's 
 constexpr int kStageWords = 16;      // plane words per row per stage
 constexpr int kStageK = kStageWords * 32;
 constexpr int kTok = 2;              // tokens per pass over a tile
-constexpr int kLutBytes = 256 * 64 * 4;   // [v][64 slots] fp32; slot = row (byte-permute addressing)
+// Shared memory.  The tables take [v][64 slots] fp32 so that one byte permute
+// forms index*256 + row*4; rows use slots 0..31, and the other 128 bytes of
+// every 256-byte line ("pieces") hold the per-warp token scratch and the
+// K-warp partial sums.
+constexpr int kLutBytes = 256 * 64 * 4;
 constexpr int kPlaneStageBytes = PW_MAX_BITS * kRows * kStageWords * 4;
-constexpr int kXStageBytes = kTok * kStageK * 4;
-constexpr int kRedBytes = kKW * kTok * kRows * 4;
-constexpr int kSmemBytes = kLutBytes + 2 * kPlaneStageBytes + 2 * kXStageBytes + kRedBytes + 64;
+constexpr int kXStageBytes = kTok * kStageK * 2;            // fp16 tokens
+constexpr int kPieceRed = 0;                                // kKW * kTok pieces
+constexpr int kPieceXw = kPieceRed + kKW * kTok;            // 2 per (warp, token)
+constexpr int kSmemBytes = kLutBytes + 2 * kPlaneStageBytes + 2 * kXStageBytes + route_smem_bytes() + 64;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -59,14 +64,6 @@ __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_grou
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
 
-// a = a + w * x, two lanes at a time (packed fp32 FMA).
-__device__ __forceinline__ void ffma2(float& ax, float& ay, float wx, float wy, float xx, float xy) {
-  asm("{\n\t.reg .b64 a, w, x;\n\t"
-      "mov.b64 a, {%0, %1};\n\tmov.b64 w, {%2, %3};\n\tmov.b64 x, {%4, %5};\n\t"
-      "fma.rn.f32x2 a, w, x, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
-      : "+f"(ax), "+f"(ay)
-      : "f"(wx), "f"(wy), "f"(xx), "f"(xy));
-}
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
@@ -122,18 +119,25 @@ __device__ __forceinline__ int global_row(const Fwd& p, int tile, int i) {
   }
 }
 
+// fp16 input row of permuted position pos: the token's x for gate_up, the
+// pair's h for down.  perm may live in global or shared memory.
 template <int KIND>
-__device__ __forceinline__ const float* token_row(const Fwd& p, int pos, int K) {
-  if (KIND == PW_KIND_GATE_UP) return p.xf + static_cast<size_t>(p.perm[pos] / p.k) * K;
-  return p.hf + static_cast<size_t>(pos) * K;
+__device__ __forceinline__ const __half* token_row(const Fwd& p, const int* perm, int pos, int K) {
+  if (KIND == PW_KIND_GATE_UP) return p.x + static_cast<size_t>(perm[pos] / p.k) * K;
+  return p.hh + static_cast<size_t>(pos) * K;
+}
+
+// 128-byte piece n of the tables' unused half.
+__device__ __forceinline__ float* piece(unsigned char* smem, int n) {
+  return reinterpret_cast<float*>(smem + n * 256 + 128);
 }
 
 template <int KIND>
-__device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsigned char* smem) {
+__device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsigned char* smem,
+                         const int* perm) {
   float* lut_s = reinterpret_cast<float*>(smem);
   uint32_t* pl_s = reinterpret_cast<uint32_t*>(smem + kLutBytes);
-  float* x_s = reinterpret_cast<float*>(smem + kLutBytes + 2 * kPlaneStageBytes);
-  float* red_s = reinterpret_cast<float*>(smem + kLutBytes + 2 * kPlaneStageBytes + 2 * kXStageBytes);
+  __half* x_s = reinterpret_cast<__half*>(smem + kLutBytes + 2 * kPlaneStageBytes);
 
   const int tid = threadIdx.x, lane = tid & 31, kw = tid >> 5;
   const int K = d.K, W = K >> 5;
@@ -154,8 +158,8 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
 
   for (int t0 = 0; t0 < it.n; t0 += kTok) {
     const int nt = min(kTok, it.n - t0);
-    const int xt = tid >> 7, xc = tid & 127;        // token staging: thread -> (token, 16 B)
-    const float* trow = (xt < nt) ? token_row<KIND>(p, it.off + t0 + xt, K) : nullptr;
+    const int xt = tid >> 6, xc = tid & 63;         // token staging: thread -> (token, 16 B)
+    const __half* trow = (xt < nt) ? token_row<KIND>(p, perm, it.off + t0 + xt, K) : nullptr;
 
     auto fill = [&](int c, int s) {
       const int wsrc = c * kStageWords + fc * 4;
@@ -168,8 +172,8 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
           if (pl < Q) cp_async16(dst + pl * kRows * kStageWords, src + fsrc + c * kStageWords);
         }
       }
-      const int kk = c * kStageK + xc * 4;
-      if (trow && kk < K) cp_async16(x_s + s * (kXStageBytes / 4) + xt * kStageK + xc * 4, trow + kk);
+      const int kk = c * kStageK + xc * 8;
+      if (trow && kk < K) cp_async16(x_s + s * (kXStageBytes / 2) + xt * kStageK + xc * 8, trow + kk);
       cp_commit();
     };
 
@@ -198,12 +202,13 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
       }
     }
 
-    // four independent accumulator pairs per token keep the FMA chains short
-    float ax[kTok][4], ay[kTok][4];
+    // four independent packed (two-wide fp32) accumulators per token keep the
+    // FMA chains short
+    float2 acc[kTok][4];
 #pragma unroll
     for (int t = 0; t < kTok; ++t)
 #pragma unroll
-      for (int m = 0; m < 4; ++m) ax[t][m] = ay[t][m] = 0.f;
+      for (int m = 0; m < 4; ++m) acc[t][m] = make_float2(0.f, 0.f);
 
     // one barrier per stage: it publishes stage c and proves every warp is done
     // with stage c-1, whose buffer the fill for stage c+1 then reuses
@@ -216,13 +221,23 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
       const int wbase = c * kStageWords + kw * 2;
       const int nw = min(2, W - wbase);
       if (nw > 0) {
+        // this warp's 64 token values of the stage, fp16 -> fp32 scratch
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < kTok; ++t) {
+          if (t < nt) {
+            const __half2 h2 = reinterpret_cast<const __half2*>(x_s + s * (kXStageBytes / 2) + t * kStageK + kw * 64)[lane];
+            *reinterpret_cast<float2*>(piece(smem, kPieceXw + 2 * (kw * kTok + t) + (lane >> 4)) + ((2 * lane) & 31)) =
+                __half22float2(h2);
+          }
+        }
+        __syncwarp();
         const uint32_t* ps = pl_s + s * (kPlaneStageBytes / 4) + row * kStageWords + rsw;
         uint2 pv[PW_MAX_BITS];
 #pragma unroll
         for (int pl = 0; pl < PW_MAX_BITS; ++pl)   // pv[r] = plane (q-1-r)
           pv[pl] = (pl < Q) ? *reinterpret_cast<const uint2*>(ps + (Q - 1 - pl) * kRows * kStageWords)
                             : make_uint2(0u, 0u);
-        const float* xs = x_s + s * (kXStageBytes / 4) + kw * 64;
 #pragma unroll
         for (int wi = 0; wi < 2; ++wi) {
           if (wi < nw) {
@@ -241,13 +256,13 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
 #pragma unroll
             for (int t = 0; t < kTok; ++t) {
               if (t < nt) {
-                const float4* xr = reinterpret_cast<const float4*>(xs + t * kStageK + wi * 32);
+                const float4* xr = reinterpret_cast<const float4*>(piece(smem, kPieceXw + 2 * (kw * kTok + t) + wi));
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                   const float4 xv = xr[j4];
                   const int m0 = (2 * j4) & 3, m1 = (2 * j4 + 1) & 3;
-                  ffma2(ax[t][m0], ay[t][m0], wv[4 * j4], wv[4 * j4 + 1], xv.x, xv.y);
-                  ffma2(ax[t][m1], ay[t][m1], wv[4 * j4 + 2], wv[4 * j4 + 3], xv.z, xv.w);
+                  acc[t][m0] = __ffma2_rn(make_float2(wv[4 * j4], wv[4 * j4 + 1]), make_float2(xv.x, xv.y), acc[t][m0]);
+                  acc[t][m1] = __ffma2_rn(make_float2(wv[4 * j4 + 2], wv[4 * j4 + 3]), make_float2(xv.z, xv.w), acc[t][m1]);
                 }
               }
             }
@@ -260,8 +275,9 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
 #pragma unroll
     for (int t = 0; t < kTok; ++t)
       if (t < nt)
-        red_s[(kw * kTok + t) * kRows + row] =
-            ((ax[t][0] + ay[t][0]) + (ax[t][1] + ay[t][1])) + ((ax[t][2] + ay[t][2]) + (ax[t][3] + ay[t][3]));
+        piece(smem, kPieceRed + kw * kTok + t)[row] =
+            ((acc[t][0].x + acc[t][0].y) + (acc[t][1].x + acc[t][1].y)) +
+            ((acc[t][2].x + acc[t][2].y) + (acc[t][3].x + acc[t][3].y));
     __syncthreads();
     if (KIND == PW_KIND_GATE_UP) {
       if (tid < nt * 16) {
@@ -270,12 +286,12 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
         float g = 0.f, u = 0.f;
 #pragma unroll
         for (int w8 = 0; w8 < kKW; ++w8) {
-          g += red_s[(w8 * kTok + t) * kRows + i];
-          u += red_s[(w8 * kTok + t) * kRows + 16 + i];
+          g += piece(smem, kPieceRed + w8 * kTok + t)[i];
+          u += piece(smem, kPieceRed + w8 * kTok + t)[16 + i];
         }
         if (r < p.I) {
           const float hv = g / (1.f + expf(-g)) * u;
-          p.hf[static_cast<size_t>(it.off + t0 + t) * p.I + r] = __half2float(__float2half_rn(hv));
+          p.hh[static_cast<size_t>(it.off + t0 + t) * p.I + r] = __float2half_rn(hv);
         }
       }
     } else {
@@ -284,7 +300,7 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
         const int r = it.tile * kRows + i;
         float yv = 0.f;
 #pragma unroll
-        for (int w8 = 0; w8 < kKW; ++w8) yv += red_s[(w8 * kTok + t) * kRows + i];
+        for (int w8 = 0; w8 < kKW; ++w8) yv += piece(smem, kPieceRed + w8 * kTok + t)[i];
         if (r < p.H) p.y[static_cast<size_t>(it.off + t0 + t) * p.H + r] = yv;
       }
     }
@@ -314,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_decode(Fwd p) {
     it.off = p.offsets[it.expert];
     const BlockDesc d = *block_desc(p, it.expert, KIND);
     if (d.q >= 1 && d.q <= PW_MAX_BITS && d.K == (KIND == PW_KIND_GATE_UP ? p.H : p.I)) {
-      run_tile<KIND>(p, d, it, smem);
+      run_tile<KIND>(p, d, it, smem, p.perm);
     } else if (threadIdx.x == 0) {
       atomicOr(p.status, PW_STATUS_BAD_DESC);
     }
@@ -343,35 +359,30 @@ __device__ bool wait_eq(const int* ptr, int want) {
   return false;
 }
 
-// Active experts ordered by the cost of their gate_up work, largest first
-// (longest-processing-time order keeps the tail of the work queue short);
-// ties keep expert order.  Thread a ranks active expert a (block-wide).
-__device__ void build_lpt(const Fwd& p, int* s_cost) {
-  const int na = p.active[0];
-  for (int a = threadIdx.x; a < na; a += blockDim.x) {
-    const int e = p.active[1 + a];
-    s_cost[a] = (block_desc(p, e, PW_KIND_GATE_UP)->q + 2) * ((p.counts[e] + kTok - 1) / kTok);
-  }
-  __syncthreads();
-  for (int a = threadIdx.x; a < na; a += blockDim.x) {
-    const int c = s_cost[a];
-    int rank = 0;
-    for (int b = 0; b < na; ++b) rank += (s_cost[b] > c) || (s_cost[b] == c && b < a);
-    p.act_lpt[1 + rank] = p.active[1 + a];
-  }
-  if (threadIdx.x == 0) p.act_lpt[0] = na;
-}
-
 // One persistent cooperative launch for the whole decode layer.
-// CTA 0 routes the batch and publishes a ready epoch; then every CTA takes
-// items from one queue: first all (expert, gate_up tile) items, then all
-// (expert, down tile) items.  A down item first waits until its expert's
-// gate_up tiles are all done; the last down item of a 64-row tile of H (over
-// all active experts) combines that tile's output rows.  Every wait is bounded
-// and reports PW_STATUS_TIMEOUT instead of hanging.
+// CTA 0 clears the work-queue counters and publishes a ready epoch at once;
+// every CTA routes the batch itself into shared memory (a few hundred logits,
+// so no CTA waits for another's routing), then takes items from one queue:
+// first all (expert, gate_up tile) items, largest gate_up cost first, then all
+// (expert, down tile) items in the same expert order.  A down item first waits
+// until its expert's gate_up tiles are all done; the last down item of a
+// 32-row tile of H (over all active experts) combines that tile's output rows.
+// Every wait is bounded and reports PW_STATUS_TIMEOUT instead of hanging.
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
   extern __shared__ __align__(128) unsigned char smem[];
   int* s_int = reinterpret_cast<int*>(smem + kSmemBytes - 64);
+  int* rs = reinterpret_cast<int*>(smem + kLutBytes + 2 * kPlaneStageBytes + 2 * kXStageBytes);
+  RouteSmem r;
+  r.idx = rs;
+  r.w = reinterpret_cast<float*>(rs + kRouteSmemMaxPairs);
+  r.perm = rs + 2 * kRouteSmemMaxPairs;
+  r.inv = rs + 3 * kRouteSmemMaxPairs;
+  r.cnt = rs + 4 * kRouteSmemMaxPairs;
+  r.off = r.cnt + (kMaxE + 1);
+  r.act = r.off + (kMaxE + 1);
+  r.lpt = r.act + (kMaxE + 1);
+  r.qgu = r.lpt + (kMaxE + 1);
+
   const int tiles_gu = p.I / 16, tiles_dn = (p.H + kRows - 1) / kRows;
   int* queue = p.sync + 1;
   int* expert_done = p.sync + 2;
@@ -380,14 +391,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
   if (blockIdx.x == 0) {
     if (threadIdx.x == 0) p.status[0] = 0u;
     for (int i = threadIdx.x; i < 1 + p.E + tiles_dn; i += blockDim.x) queue[i] = 0;
-    for (int i = threadIdx.x; i < p.T * p.H / 8; i += blockDim.x) convert8(p, i);
-    __syncthreads();
-    route_permute_block(p, reinterpret_cast<int*>(smem), reinterpret_cast<int*>(smem) + kMaxE);
-    __syncthreads();
-    build_lpt(p, reinterpret_cast<int*>(smem) + 2 * kMaxE + 2);
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) st_release(p.sync, static_cast<int>(p.epoch));
+  }
+  route_local(p, r, blockIdx.x == 0, kTok);
+  if (blockIdx.x == 0) {   // the routing outputs the caller asked for
+    const int P = p.T * p.k;
+    for (int i = threadIdx.x; i < P; i += blockDim.x) {
+      if (p.user_idx) p.user_idx[i] = r.idx[i];
+      if (p.user_w) p.user_w[i] = r.w[i];
+      if (p.user_perm) p.user_perm[i] = r.perm[i];
+    }
+    if (p.user_offsets)
+      for (int e = threadIdx.x; e <= p.E; e += blockDim.x) p.user_offsets[e] = r.off[e];
   } else {
     if (threadIdx.x == 0) {
       const bool ok = wait_eq(p.sync, static_cast<int>(p.epoch));
@@ -398,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
     if (!s_int[2]) return;
   }
 
-  const int nact = p.act_lpt[0];
+  const int nact = r.lpt[0];
   const int n_gu = nact * tiles_gu, total = n_gu + nact * tiles_dn;
   if (threadIdx.x == 0) s_int[0] = atomicAdd(queue, 1);
   __syncthreads();
@@ -409,10 +426,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
     const bool gu = item < n_gu;
     const int rank = gu ? item / tiles_gu : (item - n_gu) / tiles_dn;
     Item it;
-    it.expert = p.act_lpt[1 + rank];
+    it.expert = r.lpt[1 + rank];
     it.tile = gu ? item % tiles_gu : (item - n_gu) % tiles_dn;
-    it.n = p.counts[it.expert];
-    it.off = p.offsets[it.expert];
+    it.n = r.cnt[it.expert];
+    it.off = r.off[it.expert];
     const int kind = gu ? PW_KIND_GATE_UP : PW_KIND_DOWN;
     const BlockDesc d = *block_desc(p, it.expert, kind);
     const bool ok = d.q >= 1 && d.q <= PW_MAX_BITS && d.K == (gu ? p.H : p.I);
@@ -422,8 +439,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
       __syncthreads();
     }
     if (ok) {
-      if (gu) run_tile<PW_KIND_GATE_UP>(p, d, it, smem);
-      else run_tile<PW_KIND_DOWN>(p, d, it, smem);
+      if (gu) run_tile<PW_KIND_GATE_UP>(p, d, it, smem, r.perm);
+      else run_tile<PW_KIND_DOWN>(p, d, it, smem, r.perm);
     } else if (threadIdx.x == 0) {
       atomicOr(p.status, PW_STATUS_BAD_DESC);
     }
@@ -440,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
       if (s_int[2]) {
         __threadfence();
         const int r0 = it.tile * kRows;
-        combine_rows(p, r0, min(r0 + kRows, p.H), 0, p.T, threadIdx.x, blockDim.x);
+        combine_rows(p, r.w, r.inv, r0, min(r0 + kRows, p.H), 0, p.T, threadIdx.x, blockDim.x);
       }
     }
     __syncthreads();

@@ -33,8 +33,7 @@ struct Fwd {
                             // [2, 2+E) gate_up tiles done per expert, then
                             // down items done per 32-row tile of H
   uint32_t epoch;           // nonzero, differs between consecutive fused forwards
-  float* xf;                // [T][H]   x as fp32
-  float* hf;                // [T*k][I] h rounded to fp16, held as fp32
+  __half* hh;               // [T*k][I] h (fp16) in permuted order
   float* y;                 // [T*k][H]
 };
 

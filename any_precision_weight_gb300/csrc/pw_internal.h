@@ -45,8 +45,7 @@ struct Workspace {
   size_t inv;        // int32 [T*k]
   size_t active;     // int32 [2][E+1]: active experts (count, ids); same, cost-sorted
   size_t sync;       // int32: ready epoch, work queue, per-expert and per-row-tile counters
-  size_t xf;         // f32 [T][H]: x converted once
-  size_t hf;         // f32 [T*k][I] in perm order: h rounded to fp16, held as fp32
+  size_t hh;         // fp16 [T*k][I] in perm order
   size_t y;          // f32 [T*k][H] in perm order
   size_t x_in;       // fp16 [T][H]   (host-input staging)
   size_t logits_in;  // f32 [T][E]
@@ -71,8 +70,7 @@ inline Workspace workspace_layout(int T, int E, int k, int H, int I) {
   w.inv = take(P * 4);
   w.active = take(static_cast<size_t>(E + 1) * 2 * 4);
   w.sync = take(static_cast<size_t>(8 + E + (H + 31) / 32) * 4);
-  w.xf = take(static_cast<size_t>(T) * H * 4);
-  w.hf = take(P * I * 4);
+  w.hh = take(P * I * 2);
   w.y = take(P * H * 4);
   w.x_in = take(static_cast<size_t>(T) * H * 2);
   w.logits_in = take(static_cast<size_t>(T) * E * 4);

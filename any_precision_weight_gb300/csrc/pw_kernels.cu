@@ -38,19 +38,10 @@ cudaError_t launch_commit(BlockDesc* dst, const BlockDesc& value, cudaStream_t s
 // ------------------------------------------------------------------ routing + permutation
 
 constexpr int kRouteThreads = 1024;
-constexpr int kConvertInRoute = 64;   // larger batches convert x in their own kernel
-
-__global__ void k_convert_x(Fwd p) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < p.T * p.H / 8) convert8(p, i);
-}
-
 __global__ void __launch_bounds__(kRouteThreads) k_route_permute(Fwd p) {
   __shared__ int s_cnt[kMaxE];
   __shared__ int s_off[kMaxE + 1];
   if (threadIdx.x < 4) p.status[threadIdx.x] = 0u;   // status word and work-queue counters
-  if (p.T <= kConvertInRoute)
-    for (int i = threadIdx.x; i < p.T * p.H / 8; i += blockDim.x) convert8(p, i);
   __syncthreads();
   route_permute_block(p, s_cnt, s_off);
 }
@@ -59,7 +50,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_permute(Fwd p) {
 
 __global__ void k_combine(Fwd p) {
   const int r0 = blockIdx.x * 256, t0 = blockIdx.y * 16;
-  combine_rows(p, r0, min(r0 + 256, p.H), t0, min(t0 + 16, p.T), threadIdx.x, blockDim.x);
+  combine_rows(p, p.w, p.inv, r0, min(r0 + 256, p.H), t0, min(t0 + 16, p.T), threadIdx.x, blockDim.x);
 }
 
 // ------------------------------------------------------------------ launcher
@@ -93,8 +84,7 @@ static Fwd make_fwd(const ForwardArgs& a) {
   p.active = reinterpret_cast<int32_t*>(ws + a.lay.active);
   p.act_lpt = p.active + (a.E + 1);
   p.sync = reinterpret_cast<int32_t*>(ws + a.lay.sync);
-  p.xf = reinterpret_cast<float*>(ws + a.lay.xf);
-  p.hf = reinterpret_cast<float*>(ws + a.lay.hf);
+  p.hh = reinterpret_cast<__half*>(ws + a.lay.hh);
   p.y = reinterpret_cast<float*>(ws + a.lay.y);
   return p;
 }
@@ -108,17 +98,13 @@ static std::atomic<uint32_t> g_epoch{0};
 cudaError_t launch_forward(const ForwardArgs& a, cudaStream_t s) {
   Fwd p = make_fwd(a);
   mark(a, 0, s);
-  if (p.T <= kFusedMaxT) {
+  if (p.T <= kFusedMaxT && p.T * p.k <= kRouteSmemMaxPairs) {
     uint32_t ep = ++g_epoch;
     if (ep == 0) ep = ++g_epoch;
     p.epoch = ep;
     const cudaError_t e = launch_layer_fused(p, s);
     for (int i = 1; i < 5; ++i) mark(a, i, s);
     return e;
-  }
-  if (p.T > kConvertInRoute) {
-    const int n8 = p.T * p.H / 8;
-    k_convert_x<<<(n8 + 255) / 256, 256, 0, s>>>(p);
   }
   k_route_permute<<<1, kRouteThreads, 0, s>>>(p);
   mark(a, 1, s);

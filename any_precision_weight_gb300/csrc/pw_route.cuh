@@ -17,20 +17,6 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
-// x (fp16) -> xf (fp32), 8 elements per call.
-__device__ __forceinline__ void convert8(const Fwd& p, int i) {
-  const uint4 raw = reinterpret_cast<const uint4*>(p.x)[i];
-  const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
-  float4 a, b;
-  float2 f;
-  f = __half22float2(h2[0]); a.x = f.x; a.y = f.y;
-  f = __half22float2(h2[1]); a.z = f.x; a.w = f.y;
-  f = __half22float2(h2[2]); b.x = f.x; b.y = f.y;
-  f = __half22float2(h2[3]); b.z = f.x; b.w = f.y;
-  reinterpret_cast<float4*>(p.xf)[2 * i] = a;
-  reinterpret_cast<float4*>(p.xf)[2 * i + 1] = b;
-}
-
 // Routing and permutation of the whole batch by one CTA (any block size that is
 // a multiple of 32).  Phase 1: warp per token, top-k over the fp32 logits and
 // softmax weights.  Phase 2: per-expert counts and offsets.  Phase 3: warp per
@@ -158,18 +144,178 @@ __device__ __forceinline__ void route_permute_block(const Fwd& p, int* s_cnt, in
     }
 }
 
+// ------------------------------------------------------------------ routing into shared memory
+
+// Routing results of a decode batch held in one CTA's shared memory.
+struct RouteSmem {
+  int* idx;    // [T*k] expert of (t, j), descending logit
+  float* w;    // [T*k] routing weight of (t, j)
+  int* perm;   // [T*k] pair id t*k+j at each permuted position
+  int* inv;    // [T*k] permuted position of each pair id
+  int* cnt;    // [E]   tokens per expert
+  int* off;    // [E+1] first permuted position of each expert
+  int* act;    // [E+1] number of active experts, then their ids (expert order)
+  int* lpt;    // [E+1] the same, largest gate_up cost first
+  int* qgu;    // [E]   committed q of each expert's gate_up block
+};
+constexpr int kRouteSmemMaxPairs = 256;   // T*k bound of the fused decode path
+__host__ __device__ constexpr int route_smem_bytes() {
+  return (4 * kRouteSmemMaxPairs + 5 * (kMaxE + 1)) * 4;
+}
+
+// Every CTA of the fused layer computes the same routing on its own (it is a
+// few hundred logits), so no CTA waits for another's results.  Same order of
+// results as route_permute_block.  `report` selects the one CTA that raises the
+// NaN status bit.  Needs T*k <= kRouteSmemMaxPairs and a block of >= 32 threads.
+// Top-k and softmax weights of the tokens t = warp, warp + nwarp, ... with
+// NPER logits per lane (E <= 32 * NPER); results into r.idx / r.w.
+template <int NPER>
+__device__ __forceinline__ void route_tokens(const Fwd& p, const RouteSmem& r, bool report) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  const int E = p.E, k = p.k, T = p.T;
+  for (int t = warp; t < T; t += nwarp) {
+    float v[NPER];
+    bool taken[NPER];
+    bool nan_seen = false;
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) {
+      const int e = lane + 32 * i;
+      float z = -INFINITY;
+      if (e < E) {
+        z = p.logits[static_cast<size_t>(t) * E + e];
+        if (isnan(z)) { nan_seen = true; z = -INFINITY; }
+      }
+      v[i] = z;
+      taken[i] = (e >= E);
+    }
+    if (__any_sync(0xffffffffu, nan_seen) && lane == 0 && report) atomicOr(p.status, PW_STATUS_NAN_LOGIT);
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) m = fmaxf(m, v[i]);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < NPER; ++i)
+      if (lane + 32 * i < E) s += expf(v[i] - m);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    float wsum = 0.f;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < NPER; ++i)
+        if (!taken[i] && better(v[i], lane + 32 * i, bv, bi)) { bv = v[i]; bi = lane + 32 * i; }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+#pragma unroll
+      for (int i = 0; i < NPER; ++i)
+        if (lane + 32 * i == bi) taken[i] = true;
+      const float wj = expf(bv - m) / s;
+      wsum += wj;
+      if (lane == 0) {
+        r.idx[t * k + j] = bi;
+        r.w[t * k + j] = wj;
+      }
+    }
+    __syncwarp();
+    if (p.renorm)
+      for (int j = lane; j < k; j += 32) r.w[t * k + j] /= wsum;
+  }
+}
+
+__device__ __forceinline__ void route_local(const Fwd& p, const RouteSmem& r, bool report,
+                                            int tok_cost) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  const int E = p.E, k = p.k, T = p.T;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {   // issued early: independent loads
+    r.qgu[e] = p.desc[desc_index(p.layer, e, PW_KIND_GATE_UP, E)].q;
+    r.cnt[e] = 0;
+  }
+  if (E <= 32) route_tokens<1>(p, r, report);
+  else if (E <= 64) route_tokens<2>(p, r, report);
+  else if (E <= 128) route_tokens<4>(p, r, report);
+  else route_tokens<8>(p, r, report);
+  __syncthreads();
+  for (int i = threadIdx.x; i < T * k; i += blockDim.x) atomicAdd(&r.cnt[r.idx[i]], 1);
+  __syncthreads();
+  if (threadIdx.x < 32) {   // warp-level exclusive scan of counts and of the active flags
+    int run = 0, na = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + threadIdx.x;
+      const int c = e < E ? r.cnt[e] : 0;
+      int incl = c, actv = c > 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        const int a = __shfl_up_sync(0xffffffffu, actv, o);
+        if (threadIdx.x >= o) { incl += v; actv += a; }
+      }
+      if (e < E) {
+        r.off[e] = run + incl - c;
+        if (c) r.act[1 + na + actv - 1] = e;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+      na += __shfl_sync(0xffffffffu, actv, 31);
+    }
+    if (threadIdx.x == 0) {
+      r.off[E] = run;
+      r.act[0] = na;
+      r.lpt[0] = na;
+    }
+  }
+  __syncthreads();
+  for (int e = warp; e < E; e += nwarp) {
+    int run = 0;
+    for (int base = 0; base < T; base += 32) {
+      const int t = base + lane;
+      int jsel = -1;
+      if (t < T)
+        for (int j = 0; j < k; ++j)
+          if (r.idx[t * k + j] == e) jsel = j;
+      const unsigned mask = __ballot_sync(0xffffffffu, jsel >= 0);
+      if (jsel >= 0) {
+        const int pos = r.off[e] + run + __popc(mask & ((1u << lane) - 1u));
+        r.perm[pos] = t * k + jsel;
+        r.inv[t * k + jsel] = pos;
+      }
+      run += __popc(mask);
+    }
+  }
+  // active experts by gate_up cost, largest first (ties keep expert order)
+  const int na = r.act[0];
+  for (int a = threadIdx.x; a < na; a += blockDim.x) {
+    const int ea = r.act[1 + a];
+    const int ca = (r.qgu[ea] + 2) * ((r.cnt[ea] + tok_cost - 1) / tok_cost);
+    int rank = 0;
+    for (int b = 0; b < na; ++b) {
+      const int eb = r.act[1 + b];
+      const int cb = (r.qgu[eb] + 2) * ((r.cnt[eb] + tok_cost - 1) / tok_cost);
+      rank += (cb > ca) || (cb == ca && b < a);
+    }
+    r.lpt[1 + rank] = ea;
+  }
+  __syncthreads();
+}
+
 // out[t][r] = residual[t][r] + sum_j w[t][j] * y(t, j)[r] for r in [r0, r1) and
 // t in [t0, t1), slots added in order j = 0..k-1 (deterministic), rounded once.
-__device__ __forceinline__ void combine_rows(const Fwd& p, int r0, int r1, int t0, int t1, int tid,
-                                             int nthr) {
+// w / inv may live in global or shared memory.
+__device__ __forceinline__ void combine_rows(const Fwd& p, const float* w, const int* inv, int r0,
+                                             int r1, int t0, int t1, int tid, int nthr) {
   const int n = r1 - r0;
   for (int q = tid; q < (t1 - t0) * n; q += nthr) {
     const int t = t0 + q / n, r = r0 + q % n;
     const float base = p.residual ? __half2float(p.residual[static_cast<size_t>(t) * p.H + r]) : 0.f;
     float mix = 0.f;
     for (int j = 0; j < p.k; ++j) {
-      const int pos = p.inv[t * p.k + j];
-      mix = fmaf(p.w[t * p.k + j], __ldcg(p.y + static_cast<size_t>(pos) * p.H + r), mix);   // L2: written by other SMs
+      const int pos = inv[t * p.k + j];
+      mix = fmaf(w[t * p.k + j], __ldcg(p.y + static_cast<size_t>(pos) * p.H + r), mix);   // L2: written by other SMs
     }
     p.out[static_cast<size_t>(t) * p.H + r] = __float2half_rn(base + mix);
   }

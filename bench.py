@@ -301,14 +301,21 @@ def run_ours(args, cfg, rank, world, local):
         pw.pw_profile_attach(evs[i])
         step(i)
     torch.cuda.synchronize()
-    names = ["route_permute", "gate_up", "down", "combine"]
-    tot = {n: 0.0 for n in names}
-    for i in range(kn):
-        for j, n in enumerate(names):
-            tot[n] += evs[i][j].elapsed_time(evs[i][j + 1])
+    fused = cfg.T <= 64 and cfg.T * cfg.top_k <= 256     # one persistent kernel per layer
+    if fused:
+        names = ["layer_fused"]
+        tot = {"layer_fused": sum(evs[i][0].elapsed_time(evs[i][4]) for i in range(kn))}
+        dom = "layer_fused"
+    else:
+        names = ["route_permute", "gate_up", "down", "combine"]
+        tot = {n: 0.0 for n in names}
+        for i in range(kn):
+            for j, n in enumerate(names):
+                tot[n] += evs[i][j].elapsed_time(evs[i][j + 1])
+        dom = max(("gate_up", "down"), key=lambda n: tot[n])
     avg_ms = {n: tot[n] / kn for n in names}
-    dom = max(("gate_up", "down"), key=lambda n: tot[n])
-    dom_bytes = sum(byt[i % n_inst][dom] for i in range(kn)) / kn
+    key = "layer" if fused else dom
+    dom_bytes = sum(byt[i % n_inst][key] for i in range(kn)) / kn
     achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
     layer_bytes = sum(byt[i % n_inst]["layer"] for i in range(args.steps)) / args.steps
@@ -354,7 +361,7 @@ def run_ours(args, cfg, rank, world, local):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4,
                 "d2h_bytes_per_step": cfg.T * cfg.H * 2 + 4},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (1 if fused else 4) * args.steps,
         "clocks": clk,
         "wall_s": wall,
     }
