@@ -129,6 +129,26 @@ class Clocks:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel, or
+    None when there is none or the kernel sources changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"k_layer_{workload}.md")
+    if kernel != "layer_fused" or not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    want = hashlib.sha256()
+    for f in ("pw_decode.cu", "pw_route.cuh"):
+        want.update(open(os.path.join(ROOT, "any_precision_weight_gb300", "csrc", f), "rb").read())
+    fields = dict(l.split(":", 1) for l in txt.splitlines() if ":" in l and " " not in l.split(":", 1)[0])
+    if fields.get("kernel_sources_sha256_16", "").strip() != want.hexdigest()[:16]:
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"].strip())
+    except (KeyError, ValueError):
+        return None
+
+
 def hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -356,7 +376,7 @@ def run_ours(args, cfg, rank, world, local):
                    "layer_weight_bytes_per_step": layer_bytes, "layer_gbs": layer_gbs,
                    "kernel_ms": avg_ms},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": profiled_traffic(dom, cfg.name),
                      "bytes_per_launch": dom_bytes},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4,
