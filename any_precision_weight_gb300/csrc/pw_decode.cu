@@ -308,36 +308,6 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
   }
 }
 
-template <int KIND>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) k_decode(Fwd p) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  int* s_item = reinterpret_cast<int*>(smem + kSmemBytes - 64);
-  const int tiles = (KIND == PW_KIND_GATE_UP) ? p.I / 16 : (p.H + kRows - 1) / kRows;
-  const int nact = p.active[0];
-  const int total = nact * tiles;
-  int* ctr = reinterpret_cast<int*>(p.status) + (KIND == PW_KIND_GATE_UP ? kCtrGateUp : kCtrDown);
-  if (threadIdx.x == 0) s_item[0] = atomicAdd(ctr, 1);
-  __syncthreads();
-  for (int slot = 0;; slot ^= 1) {
-    const int item = s_item[slot];
-    if (item >= total) break;
-    // claim the next item now; it is read after this item's barriers
-    if (threadIdx.x == 0) s_item[slot ^ 1] = atomicAdd(ctr, 1);
-    Item it;
-    it.expert = p.active[1 + item / tiles];
-    it.tile = item % tiles;
-    it.n = p.counts[it.expert];
-    it.off = p.offsets[it.expert];
-    const BlockDesc d = *block_desc(p, it.expert, KIND);
-    if (d.q >= 1 && d.q <= PW_MAX_BITS && d.K == (KIND == PW_KIND_GATE_UP ? p.H : p.I)) {
-      run_tile<KIND>(p, d, it, smem, p.perm);
-    } else if (threadIdx.x == 0) {
-      atomicOr(p.status, PW_STATUS_BAD_DESC);
-    }
-    __syncthreads();
-  }
-}
-
 // ------------------------------------------------------------------ fused layer
 
 constexpr int kSpinLimit = 1 << 22;   // ~0.3 s of polling before a wait gives up
@@ -465,33 +435,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
 }
 
 constexpr int kMaxDevices = 64;
-int g_sms[kMaxDevices] = {};     // decode grid per device once configured (0: not yet)
 int g_fused[kMaxDevices] = {};   // cooperative grid of the fused layer per device
 
 }  // namespace
-
-cudaError_t launch_decode(const Fwd& p, int kind, cudaStream_t s) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (g_sms[dev] == 0) {   // once per device: opt in to > 48 KB of shared memory
-    e = cudaFuncSetAttribute(k_decode<PW_KIND_GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_decode<PW_KIND_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemBytes);
-    int sms = 0;
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    g_sms[dev] = (sms > 0 ? sms : 1) * kCtasPerSm;
-  }
-  if (kind == PW_KIND_GATE_UP)
-    k_decode<PW_KIND_GATE_UP><<<g_sms[dev], kThreads, kSmemBytes, s>>>(p);
-  else
-    k_decode<PW_KIND_DOWN><<<g_sms[dev], kThreads, kSmemBytes, s>>>(p);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_layer_fused(const Fwd& p, cudaStream_t s) {
   int dev = 0;

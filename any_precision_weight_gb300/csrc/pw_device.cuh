@@ -34,6 +34,7 @@ struct Fwd {
                             // down items done per 32-row tile of H
   uint32_t epoch;           // nonzero, differs between consecutive fused forwards
   __half* hh;               // [T*k][I] h (fp16) in permuted order
+  __half* xp;               // [T*k][H] token rows in permuted (expert) order, prefill GEMMs
   float* y;                 // [T*k][H]
 };
 
@@ -45,11 +46,12 @@ __device__ __forceinline__ const BlockDesc* block_desc(const Fwd& p, int e, int 
   return p.desc + desc_index(p.layer, e, kind, p.E);
 }
 
-// Decode GEMV of one block kind (gate_up or down) over all active experts.
-cudaError_t launch_decode(const Fwd& p, int kind, cudaStream_t s);
 // The whole decode layer (routing, gate_up, down, combine) in one cooperative
 // persistent launch; for batches of at most kFusedMaxT tokens.
 constexpr int kFusedMaxT = 64;
 cudaError_t launch_layer_fused(const Fwd& p, cudaStream_t s);
+// Tensor-core GEMM of one block kind over all experts (prefill-sized batches);
+// gate_up also gathers the token rows into expert order first.
+cudaError_t launch_prefill(const Fwd& p, int kind, cudaStream_t s);
 
 }  // namespace pw

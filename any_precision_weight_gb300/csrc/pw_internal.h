@@ -46,6 +46,7 @@ struct Workspace {
   size_t active;     // int32 [2][E+1]: active experts (count, ids); same, cost-sorted
   size_t sync;       // int32: ready epoch, work queue, per-expert and per-row-tile counters
   size_t hh;         // fp16 [T*k][I] in perm order
+  size_t xp;         // fp16 [T*k][H] token rows in perm order (prefill GEMMs)
   size_t y;          // f32 [T*k][H] in perm order
   size_t x_in;       // fp16 [T][H]   (host-input staging)
   size_t logits_in;  // f32 [T][E]
@@ -71,6 +72,7 @@ inline Workspace workspace_layout(int T, int E, int k, int H, int I) {
   w.active = take(static_cast<size_t>(E + 1) * 2 * 4);
   w.sync = take(static_cast<size_t>(8 + E + (H + 31) / 32) * 4);
   w.hh = take(P * I * 2);
+  w.xp = take(P * H * 2);
   w.y = take(P * H * 4);
   w.x_in = take(static_cast<size_t>(T) * H * 2);
   w.logits_in = take(static_cast<size_t>(T) * E * 4);

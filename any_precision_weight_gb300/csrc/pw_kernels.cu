@@ -85,6 +85,7 @@ static Fwd make_fwd(const ForwardArgs& a) {
   p.act_lpt = p.active + (a.E + 1);
   p.sync = reinterpret_cast<int32_t*>(ws + a.lay.sync);
   p.hh = reinterpret_cast<__half*>(ws + a.lay.hh);
+  p.xp = reinterpret_cast<__half*>(ws + a.lay.xp);
   p.y = reinterpret_cast<float*>(ws + a.lay.y);
   return p;
 }
@@ -108,10 +109,10 @@ cudaError_t launch_forward(const ForwardArgs& a, cudaStream_t s) {
   }
   k_route_permute<<<1, kRouteThreads, 0, s>>>(p);
   mark(a, 1, s);
-  cudaError_t e = launch_decode(p, PW_KIND_GATE_UP, s);
+  cudaError_t e = launch_prefill(p, PW_KIND_GATE_UP, s);
   if (e != cudaSuccess) return e;
   mark(a, 2, s);
-  e = launch_decode(p, PW_KIND_DOWN, s);
+  e = launch_prefill(p, PW_KIND_DOWN, s);
   if (e != cudaSuccess) return e;
   mark(a, 3, s);
   k_combine<<<dim3((p.H + 255) / 256, (p.T + 15) / 16), 256, 0, s>>>(p);

@@ -1,0 +1,458 @@
+// Prefill-sized expert GEMMs of the fused APL MoE layer on the 5th-generation
+// tensor cores (sm_103a: TMA, mbarrier, tcgen05 MMA with the accumulator in TMEM).
+//
+// Source: PagedWeight technical summary, core components section 3 ("Fused
+// Mixed-Precision Kernel": the kernel reads APL bit-planes and lookup tables
+// directly, a different committed bitwidth per linear block).  With hundreds of
+// tokens per expert the layer is a dense contraction, so the weights are
+// dequantised once per tile into shared memory and multiplied on tensor cores.
+//
+// One CTA per SM, persistent over (expert, weight-row tile, token tile) items:
+//  * the expert's token rows (gathered into expert order, fp16) arrive by TMA in
+//    128 x 64 boxes with the 128-byte swizzle;
+//  * all 8 warps dequantise the 128 weight rows x 64 k of the same K step
+//    straight into the K-major 128-byte-swizzled layout the MMA reads (SWAR bit
+//    transpose of the plane words, byte-permute table addressing, fp16 table in
+//    shared memory), then fence the async proxy;
+//  * one thread issues tcgen05.mma kind::f16 (M = 128 tokens, N = 128 weight
+//    rows, K = 16 per instruction, fp32 accumulate in TMEM) and commits to the
+//    stage's mbarrier; two stages keep dequant, TMA and MMA overlapped;
+//  * the epilogue reads TMEM with tcgen05.ld: gate_up tiles (64 gate + 64 up
+//    rows) write h = silu(gate) * up in fp16, down tiles write y in fp32.
+// Every mbarrier wait is bounded and reports PW_STATUS_TIMEOUT.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "pw_route.cuh"
+
+namespace pw {
+namespace {
+
+constexpr int kPThreads = 256;
+constexpr int kBM = 128;                       // tokens per tile (MMA M)
+constexpr int kBN = 128;                       // weight rows per tile (MMA N)
+constexpr int kBK = 64;                        // K per stage: one 128-byte swizzle row of fp16
+constexpr int kPStages = 2;
+constexpr int kTileBytes = kBM * kBK * 2;      // 16 KB, A and B alike
+constexpr int kPLutBytes = 256 * kBN * 2;      // fp16 [v][128 rows]
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kPStages * kTileBytes;
+constexpr int kOffLut = kOffB + kPStages * kTileBytes;
+constexpr int kOffBar = kOffLut + kPLutBytes;
+constexpr int kMiscBytes = 64 + 16 + 4 * (256 + 1) + 64;   // barriers, TMEM address, item prefix per expert
+constexpr int kPSmemBytes = kOffBar + kMiscBytes + 1024;   // + slack to align the base to 1 KB
+constexpr uint32_t kTmemCols = 128;
+constexpr long long kWaitLimit = 1ll << 22;
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// Bounded wait for the phase of the given parity; false when the limit runs out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (long long i = 0; i < kWaitLimit; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
+// ---------------------------------------------------------------- TMA / tcgen05
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
+// groups 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFF) >> 4);          // start address      [0, 14)
+  d |= static_cast<uint64_t>(1) << 16;                        // leading byte offset [16, 30)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                // stride byte offset  [32, 46)
+  d |= static_cast<uint64_t>(1) << 46;                        // version             [46, 48)
+  d |= static_cast<uint64_t>(2) << 61;                        // 128-byte swizzle    [61, 64)
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D, M x N.
+constexpr uint32_t kIdesc = (1u << 4)                             // D format: f32
+                            | (0u << 7) | (0u << 10)              // A, B: f16
+                            | (static_cast<uint32_t>(kBN >> 3) << 17)
+                            | (static_cast<uint32_t>(kBM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void proxy_fence_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t prmt_p(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ uint32_t bitsel_p(uint32_t a, uint32_t b, uint32_t m) {   // (a & ~m) | (b & m)
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xCA;" : "=r"(d) : "r"(m), "r"(b), "r"(a));
+  return d;
+}
+__device__ __forceinline__ void swap_p(uint32_t& lo, uint32_t& hi, int s, uint32_t mask) {
+  const uint32_t nlo = bitsel_p(lo, hi << s, mask << s);
+  const uint32_t nhi = bitsel_p(hi, lo >> s, mask);
+  lo = nlo;
+  hi = nhi;
+}
+// Row r of o holds plane (q-1-r); afterwards byte bb of o[r] is element 8bb + r's index.
+__device__ __forceinline__ void transpose8(uint32_t (&o)[8]) {
+#pragma unroll
+  for (int r = 0; r < 4; ++r) swap_p(o[r], o[r + 4], 4, 0x0F0F0F0Fu);
+#pragma unroll
+  for (int r = 0; r < 8; r += 4) {
+    swap_p(o[r], o[r + 2], 2, 0x33333333u);
+    swap_p(o[r + 1], o[r + 3], 2, 0x33333333u);
+  }
+#pragma unroll
+  for (int r = 0; r < 8; r += 2) swap_p(o[r], o[r + 1], 1, 0x55555555u);
+}
+
+// Weight row of tile row i (-1 past the block).
+template <int KIND>
+__device__ __forceinline__ int wrow(const Fwd& p, int nt, int i) {
+  if (KIND == PW_KIND_GATE_UP) {
+    const int r = nt * (kBN / 2) + (i & 63);
+    if (r >= p.I) return -1;
+    return i < 64 ? r : p.I + r;
+  }
+  const int r = nt * kBN + i;
+  return r < p.H ? r : -1;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kPThreads, 1)
+k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = saddr(smem);
+  const uint32_t bar_full = sbase + kOffBar;          // [2] TMA of A arrived
+  const uint32_t bar_mma = sbase + kOffBar + 16;      // [2] MMAs of the stage done
+  int* s_misc = reinterpret_cast<int*>(smem + kOffBar + 64);   // [0] tmem addr, [1] abort, [2..] tiles
+  __half* lut_s = reinterpret_cast<__half*>(smem + kOffLut);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = p.E;
+  const int K = (KIND == PW_KIND_GATE_UP) ? p.H : p.I;
+  const int W = K >> 5;
+  const int nksteps = K / kBK;
+  const int ntiles = (KIND == PW_KIND_GATE_UP) ? p.I / (kBN / 2) : (p.H + kBN - 1) / kBN;
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(s_misc)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_mma + 8 * s, 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    s_misc[1] = 0;
+  }
+  // items: per expert ceil(n_e / 128) token tiles x ntiles weight tiles
+  int* s_start = s_misc + 4;   // [E+1] first item of each expert
+  if (tid == 0) {
+    int run = 0;
+    for (int e = 0; e < E; ++e) {
+      s_start[e] = run;
+      run += ((p.counts[e] + kBM - 1) / kBM) * ntiles;
+    }
+    s_start[E] = run;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = static_cast<uint32_t>(s_misc[0]);
+  const int total = s_start[E];
+
+  // dequant role: tile row and which 32-k half of the K step
+  const int row = tid & 127, half = tid >> 7;
+  const uint32_t rowoff = static_cast<uint32_t>(row) * 2u;     // byte offset of the row in a table line
+  uint32_t g = 0;                                              // K steps issued so far (stage ring)
+
+  for (int item = blockIdx.x; item < total && !s_misc[1]; item += gridDim.x) {
+    int e = 0;
+    while (s_start[e + 1] <= item) ++e;
+    const int local = item - s_start[e];
+    const int nmt = (p.counts[e] + kBM - 1) / kBM;
+    const int nt = local / nmt, mt = local % nmt;
+    const int row0 = p.offsets[e] + mt * kBM;                  // first permuted pair of the tile
+    const int nvalid = min(kBM, p.counts[e] - mt * kBM);
+    const BlockDesc d = *block_desc(p, e, KIND);
+    const int Q = d.q, V = 1 << Q;
+    if (Q < 1 || Q > PW_MAX_BITS || d.K != K) {
+      if (tid == 0) atomicOr(p.status, PW_STATUS_BAD_DESC);
+      continue;
+    }
+    const int grow = wrow<KIND>(p, nt, row);
+
+    // the tile's table: LUT_q[row][v] fp16 -> lut_s[v][row]
+    for (int vc = half; vc * 8 < V; vc += 2) {
+      uint4 raw = make_uint4(0, 0, 0, 0);
+      if (grow >= 0) raw = __ldg(reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(grow) * V + vc * 8));
+      const uint16_t* hv = reinterpret_cast<const uint16_t*>(&raw);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) reinterpret_cast<uint16_t*>(lut_s)[(vc * 8 + j) * kBN + row] = hv[j];
+    }
+    __syncthreads();
+
+    // plane words of K step ks for this thread: word 2*ks + half of its row
+    uint32_t cur[PW_MAX_BITS], nxt[PW_MAX_BITS];
+    auto load_words = [&](int ks, uint32_t (&w)[PW_MAX_BITS]) {
+#pragma unroll
+      for (int pl = 0; pl < PW_MAX_BITS; ++pl)
+        w[pl] = (pl < Q && grow >= 0 && ks < nksteps)
+                    ? __ldg(d.planes[pl] + static_cast<size_t>(grow) * W + 2 * ks + half)
+                    : 0u;
+    };
+    load_words(0, cur);
+
+    for (int ks = 0; ks < nksteps; ++ks, ++g) {
+      const int s = g & 1;
+      const uint32_t use = g >> 1;
+      load_words(ks + 1, nxt);
+      // stage s is free once the MMAs of its previous use are done
+      if (use > 0 && !mbar_wait(bar_mma + 8 * s, (use - 1) & 1)) {
+        atomicOr(p.status, PW_STATUS_TIMEOUT);
+        s_misc[1] = 1;
+      }
+      if (tid == 0) {
+        mbar_expect_tx(bar_full + 8 * s, kTileBytes);
+        tma_load_2d(sbase + kOffA + s * kTileBytes, &tmA, ks * kBK, row0, bar_full + 8 * s);
+      }
+      // dequantise 32 weights of this row into the swizzled B tile
+      {
+        uint32_t o[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          uint32_t w = 0;
+#pragma unroll
+          for (int pl = 0; pl < PW_MAX_BITS; ++pl)
+            if (pl == Q - 1 - r) w = cur[pl];
+          o[r] = (r < Q) ? w : 0u;
+        }
+        transpose8(o);
+        const uint32_t lut_base = saddr(lut_s);
+        unsigned char* tileB = smem + kOffB + s * kTileBytes + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb) {
+          uint32_t hv[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const uint32_t a = lut_base + prmt_p(o[r], rowoff, 0x5504u | (static_cast<uint32_t>(bb) << 4));
+            uint16_t v16;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v16) : "r"(a));
+            hv[r] = v16;
+          }
+          uint4 pk;
+          pk.x = hv[0] | (hv[1] << 16);
+          pk.y = hv[2] | (hv[3] << 16);
+          pk.z = hv[4] | (hv[5] << 16);
+          pk.w = hv[6] | (hv[7] << 16);
+          const int chunk = half * 4 + bb;
+          *reinterpret_cast<uint4*>(tileB + ((chunk ^ (row & 7)) << 4)) = pk;
+        }
+      }
+      proxy_fence_smem();   // generic-proxy writes of B visible to the tensor core
+      tc_fence_before();
+      __syncthreads();
+      if (s_misc[1]) break;   // a bounded wait gave up: stop issuing work
+      if (tid == 0) {
+        if (!mbar_wait(bar_full + 8 * s, use & 1)) {
+          atomicOr(p.status, PW_STATUS_TIMEOUT);
+          s_misc[1] = 1;
+        } else {
+          tc_fence_after();
+          const uint32_t a0 = sbase + kOffA + s * kTileBytes, b0 = sbase + kOffB + s * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_f16(tmem, smem_desc(a0 + kk * 32), smem_desc(b0 + kk * 32), (ks | kk) != 0);
+          mma_commit(bar_mma + 8 * s);
+        }
+      }
+#pragma unroll
+      for (int pl = 0; pl < PW_MAX_BITS; ++pl) cur[pl] = nxt[pl];
+    }
+
+    // ---- epilogue: wait for the tile's last MMAs, then TMEM -> registers -> global
+    {
+      const uint32_t gl = g - 1;
+      if (!mbar_wait(bar_mma + 8 * (gl & 1), (gl >> 1) & 1)) {
+        atomicOr(p.status, PW_STATUS_TIMEOUT);
+        s_misc[1] = 1;
+      }
+      tc_fence_after();
+      const int lg = warp & 3, ch = warp >> 2;
+      const int tok = lg * 32 + lane;                          // TMEM lane = token row of the tile
+      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(lg * 32) << 16);
+      if (KIND == PW_KIND_GATE_UP) {
+        float gv[32], uv[32];
+        tmem_ld32(lane_addr + ch * 32, gv);
+        tmem_ld32(lane_addr + 64 + ch * 32, uv);
+        if (tok < nvalid) {
+          __half* dst = p.hh + static_cast<size_t>(row0 + tok) * p.I + nt * 64 + ch * 32;
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            __half2 h2[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float a = gv[j + 2 * u], b = gv[j + 2 * u + 1];
+              const float ha = a / (1.f + expf(-a)) * uv[j + 2 * u];
+              const float hb = b / (1.f + expf(-b)) * uv[j + 2 * u + 1];
+              h2[u] = __floats2half2_rn(ha, hb);
+            }
+            *reinterpret_cast<uint4*>(dst + j) = *reinterpret_cast<const uint4*>(h2);
+          }
+        }
+      } else {
+        float yv[32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tmem_ld32(lane_addr + ch * 64 + c * 32, yv);
+          if (tok < nvalid) {
+            float* dst = p.y + static_cast<size_t>(row0 + tok) * p.H + nt * kBN + ch * 64 + c * 32;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(yv[j], yv[j + 1], yv[j + 2], yv[j + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncthreads();   // TMEM reads done before the next tile's first MMA overwrites D
+    }
+  }
+
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+}
+
+// X_perm[pos] = x[perm[pos] / k]: the expert-ordered token rows the GEMM reads by TMA.
+__global__ void k_gather_x(Fwd p) {
+  const int pos = blockIdx.x;
+  const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(p.perm[pos] / p.k) * p.H);
+  uint4* dst = reinterpret_cast<uint4*>(p.xp + static_cast<size_t>(pos) * p.H);
+  for (int i = threadIdx.x; i < p.H / 8; i += blockDim.x) dst[i] = src[i];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+constexpr int kMaxDevicesP = 64;
+int g_psms[kMaxDevicesP] = {};
+
+cudaError_t make_map(CUtensorMap* m, const void* base, int rows, int cols) {
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {kBK, kBM};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides,
+                              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const Fwd& p, int kind, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevicesP) return cudaErrorInvalidDevice;
+  if (g_psms[dev] == 0) {
+    e = cudaFuncSetAttribute(k_prefill<PW_KIND_GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_prefill<PW_KIND_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
+    int sms = 0;
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_psms[dev] = sms > 0 ? sms : 1;
+  }
+  const int P = p.T * p.k;
+  CUtensorMap map;
+  if (kind == PW_KIND_GATE_UP) {
+    k_gather_x<<<P, 128, 0, s>>>(p);
+    e = make_map(&map, p.xp, P, p.H);
+    if (e != cudaSuccess) return e;
+    k_prefill<PW_KIND_GATE_UP><<<g_psms[dev], kPThreads, kPSmemBytes, s>>>(p, map);
+  } else {
+    e = make_map(&map, p.hh, P, p.I);
+    if (e != cudaSuccess) return e;
+    k_prefill<PW_KIND_DOWN><<<g_psms[dev], kPThreads, kPSmemBytes, s>>>(p, map);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pw

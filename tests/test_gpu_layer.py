@@ -122,6 +122,53 @@ def test_prefill_shaped_small():
     assert_close(out, ref["out"])
 
 
+@pytest.mark.slow
+def test_mixtral_prefill_sampled():
+    """Full-size Mixtral-shaped prefill (2048 tokens) on the tensor-core path:
+    routing bit-exact for every token, outputs compared on sampled tokens and rows."""
+    cfg = synth.CONFIGS["mixtral_prefill"]
+    m = gpu_layer(cfg)
+    x, L = synth.tokens(cfg), synth.logits(cfg)
+    out, ri, rw, ro, rp = _run(m, cfg, x, L)
+    rng = np.random.default_rng(6)
+    toks = np.sort(rng.choice(cfg.T, size=12, replace=False))
+    cols = np.sort(rng.choice(cfg.H, size=64, replace=False))
+    ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg)),
+                     out_rows=cols, out_tokens=toks)
+    _check_routing(ref, ri, rw, ro, rp)
+    assert_close(out[toks][:, cols], ref["out"])
+
+
+def test_prefill_gemm_integer_tables_bit_exact():
+    """Tensor-core path with integer tables and 0/1 tokens (as in the decode
+    test): every product and sum is an exact integer in fp32, so the output must
+    equal the oracle's fp16 rounding bit for bit."""
+    cfg = synth.CONFIGS["tiny"].with_(T=200, top_k=1, renorm=1)
+    rng = np.random.default_rng(98)
+    E, H, I = cfg.E, cfg.H, cfg.I
+    bits = rng.integers(3, 9, size=(E, 2)).astype(np.int32)
+    blk = {}
+    for e in range(E):
+        for kind in (0, 1):
+            R, K = cfg.rows(kind), cfg.cols(kind)
+            q = int(bits[e, kind])
+            if kind == 0:
+                f = np.concatenate([rng.integers(2, 4, size=(I, 1 << q)), rng.integers(-1, 2, size=(I, 1 << q))])
+            else:
+                f = rng.integers(-1, 2, size=(R, 1 << q))
+            par = np.repeat(f, 1 << (8 - q), axis=1).astype(np.float16)
+            blk[(e, kind)] = (rng.integers(0, 256, size=(R, K), dtype=np.uint8), par)
+    src = lambda e, kind: blk[(e, kind)]
+    m = gpu_layer(cfg, bits={0: bits}, blocks={0: src})
+    x = np.zeros((cfg.T, H), dtype=np.float16)
+    for t in range(cfg.T):
+        x[t, rng.choice(H, size=19, replace=False)] = 1
+    L = synth.logits(cfg)
+    out, *_ = _run(m, cfg, x, L)
+    ref = omoe.layer(x, L, 1, 1, oracle_blocks(src, bits))
+    assert np.array_equal(out.view(np.uint16), ref["out"].astype(np.float16).view(np.uint16))
+
+
 def test_residual_topk_extremes_and_determinism():
     import torch
     cfg = synth.CONFIGS["tiny"].with_(T=7)
