@@ -7,7 +7,8 @@
 // tokens per expert the layer is a dense contraction, so the weights are
 // dequantised once per tile into shared memory and multiplied on tensor cores.
 //
-// One CTA per SM, persistent over (expert, weight-row tile, token tile) items:
+// One CTA per SM, persistent over (expert, weight-row tile, group of up to 4
+// token tiles) items, so each dequantised weight tile feeds up to 4 MMAs:
 //  * the expert's token rows (gathered into expert order, fp16) arrive by TMA in
 //    128 x 64 boxes with the 128-byte swizzle;
 //  * all 8 warps dequantise the 128 weight rows x 64 k of the same K step
@@ -36,15 +37,16 @@ constexpr int kBM = 128;                       // tokens per tile (MMA M)
 constexpr int kBN = 128;                       // weight rows per tile (MMA N)
 constexpr int kBK = 64;                        // K per stage: one 128-byte swizzle row of fp16
 constexpr int kPStages = 2;
+constexpr int kMT = 4;                         // token tiles sharing one dequantised weight tile
 constexpr int kTileBytes = kBM * kBK * 2;      // 16 KB, A and B alike
 constexpr int kPLutBytes = 256 * kBN * 2;      // fp16 [v][128 rows]
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kPStages * kTileBytes;
+constexpr int kOffA = 0;                       // [stage][token tile] 16 KB boxes
+constexpr int kOffB = kOffA + kPStages * kMT * kTileBytes;
 constexpr int kOffLut = kOffB + kPStages * kTileBytes;
 constexpr int kOffBar = kOffLut + kPLutBytes;
 constexpr int kMiscBytes = 64 + 16 + 4 * (256 + 1) + 64;   // barriers, TMEM address, item prefix per expert
 constexpr int kPSmemBytes = kOffBar + kMiscBytes + 1024;   // + slack to align the base to 1 KB
-constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kTmemCols = kMT * kBN;     // one 128-column fp32 accumulator per token tile
 constexpr long long kWaitLimit = 1ll << 22;
 
 __device__ __forceinline__ uint32_t saddr(const void* p) {
@@ -215,13 +217,13 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_misc[1] = 0;
   }
-  // items: per expert ceil(n_e / 128) token tiles x ntiles weight tiles
+  // items: per expert ceil(token tiles / kMT) groups x ntiles weight tiles
   int* s_start = s_misc + 4;   // [E+1] first item of each expert
   if (tid == 0) {
     int run = 0;
     for (int e = 0; e < E; ++e) {
       s_start[e] = run;
-      run += ((p.counts[e] + kBM - 1) / kBM) * ntiles;
+      run += ((p.counts[e] + kBM * kMT - 1) / (kBM * kMT)) * ntiles;
     }
     s_start[E] = run;
   }
@@ -240,10 +242,11 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
     int e = 0;
     while (s_start[e + 1] <= item) ++e;
     const int local = item - s_start[e];
-    const int nmt = (p.counts[e] + kBM - 1) / kBM;
-    const int nt = local / nmt, mt = local % nmt;
-    const int row0 = p.offsets[e] + mt * kBM;                  // first permuted pair of the tile
-    const int nvalid = min(kBM, p.counts[e] - mt * kBM);
+    const int ngroups = (p.counts[e] + kBM * kMT - 1) / (kBM * kMT);
+    const int nt = local / ngroups, mg = local % ngroups;
+    const int row0 = p.offsets[e] + mg * kBM * kMT;            // first permuted pair of the group
+    const int nvalid = min(kBM * kMT, p.counts[e] - mg * kBM * kMT);
+    const int nm = (nvalid + kBM - 1) / kBM;                   // token tiles in this group
     const BlockDesc d = *block_desc(p, e, KIND);
     const int Q = d.q, V = 1 << Q;
     if (Q < 1 || Q > PW_MAX_BITS || d.K != K) {
@@ -283,8 +286,10 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
         s_misc[1] = 1;
       }
       if (tid == 0) {
-        mbar_expect_tx(bar_full + 8 * s, kTileBytes);
-        tma_load_2d(sbase + kOffA + s * kTileBytes, &tmA, ks * kBK, row0, bar_full + 8 * s);
+        mbar_expect_tx(bar_full + 8 * s, nm * kTileBytes);
+        for (int m = 0; m < nm; ++m)
+          tma_load_2d(sbase + kOffA + (s * kMT + m) * kTileBytes, &tmA, ks * kBK, row0 + m * kBM,
+                      bar_full + 8 * s);
       }
       // dequantise 32 weights of this row into the swizzled B tile
       {
@@ -329,10 +334,13 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
           s_misc[1] = 1;
         } else {
           tc_fence_after();
-          const uint32_t a0 = sbase + kOffA + s * kTileBytes, b0 = sbase + kOffB + s * kTileBytes;
+          const uint32_t b0 = sbase + kOffB + s * kTileBytes;
+          for (int m = 0; m < nm; ++m) {
+            const uint32_t a0 = sbase + kOffA + (s * kMT + m) * kTileBytes;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_f16(tmem, smem_desc(a0 + kk * 32), smem_desc(b0 + kk * 32), (ks | kk) != 0);
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_f16(tmem + m * kBN, smem_desc(a0 + kk * 32), smem_desc(b0 + kk * 32), (ks | kk) != 0);
+          }
           mma_commit(bar_mma + 8 * s);
         }
       }
@@ -349,36 +357,39 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
       }
       tc_fence_after();
       const int lg = warp & 3, ch = warp >> 2;
-      const int tok = lg * 32 + lane;                          // TMEM lane = token row of the tile
-      const uint32_t lane_addr = tmem + (static_cast<uint32_t>(lg * 32) << 16);
-      if (KIND == PW_KIND_GATE_UP) {
-        float gv[32], uv[32];
-        tmem_ld32(lane_addr + ch * 32, gv);
-        tmem_ld32(lane_addr + 64 + ch * 32, uv);
-        if (tok < nvalid) {
-          __half* dst = p.hh + static_cast<size_t>(row0 + tok) * p.I + nt * 64 + ch * 32;
-#pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            __half2 h2[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float a = gv[j + 2 * u], b = gv[j + 2 * u + 1];
-              const float ha = a / (1.f + expf(-a)) * uv[j + 2 * u];
-              const float hb = b / (1.f + expf(-b)) * uv[j + 2 * u + 1];
-              h2[u] = __floats2half2_rn(ha, hb);
-            }
-            *reinterpret_cast<uint4*>(dst + j) = *reinterpret_cast<const uint4*>(h2);
-          }
-        }
-      } else {
-        float yv[32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          tmem_ld32(lane_addr + ch * 64 + c * 32, yv);
+      for (int m = 0; m < nm; ++m) {
+        const int tok = m * kBM + lg * 32 + lane;              // TMEM lane = token row of the tile
+        const uint32_t lane_addr = tmem + m * kBN + (static_cast<uint32_t>(lg * 32) << 16);
+        if (KIND == PW_KIND_GATE_UP) {
+          float gv[32], uv[32];
+          tmem_ld32(lane_addr + ch * 32, gv);
+          tmem_ld32(lane_addr + 64 + ch * 32, uv);
           if (tok < nvalid) {
-            float* dst = p.y + static_cast<size_t>(row0 + tok) * p.H + nt * kBN + ch * 64 + c * 32;
+            __half* dst = p.hh + static_cast<size_t>(row0 + tok) * p.I + nt * 64 + ch * 32;
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(yv[j], yv[j + 1], yv[j + 2], yv[j + 3]);
+            for (int j = 0; j < 32; j += 8) {
+              __half2 h2[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float a = gv[j + 2 * u], b = gv[j + 2 * u + 1];
+                const float ha = a / (1.f + expf(-a)) * uv[j + 2 * u];
+                const float hb = b / (1.f + expf(-b)) * uv[j + 2 * u + 1];
+                h2[u] = __floats2half2_rn(ha, hb);
+              }
+              *reinterpret_cast<uint4*>(dst + j) = *reinterpret_cast<const uint4*>(h2);
+            }
+          }
+        } else {
+          float yv[32];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            tmem_ld32(lane_addr + ch * 64 + c * 32, yv);
+            if (tok < nvalid) {
+              float* dst = p.y + static_cast<size_t>(row0 + tok) * p.H + nt * kBN + ch * 64 + c * 32;
+#pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(dst + j) = make_float4(yv[j], yv[j + 1], yv[j + 2], yv[j + 3]);
+            }
           }
         }
       }
