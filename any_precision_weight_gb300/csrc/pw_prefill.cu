@@ -7,17 +7,21 @@
 // tokens per expert the layer is a dense contraction, so the weights are
 // dequantised once per tile into shared memory and multiplied on tensor cores.
 //
-// One CTA per SM, persistent over (expert, weight-row tile, group of up to 4
-// token tiles) items, so each dequantised weight tile feeds up to 4 MMAs:
+// One CTA per SM, persistent over (expert, weight-row tile, group of up to 3
+// token tiles) items, so each dequantised weight tile feeds up to 3 MMAs:
 //  * the expert's token rows (gathered into expert order, fp16) arrive by TMA in
 //    128 x 64 boxes with the 128-byte swizzle;
+//  * bit-planes arrive by coalesced cp.async, two K steps (16 bytes per row and
+//    plane) at a time, double buffered;
 //  * all 8 warps dequantise the 128 weight rows x 64 k of the same K step
 //    straight into the K-major 128-byte-swizzled layout the MMA reads (SWAR bit
 //    transpose of the plane words, byte-permute table addressing, fp16 table in
 //    shared memory), then fence the async proxy;
 //  * one thread issues tcgen05.mma kind::f16 (M = 128 tokens, N = 128 weight
 //    rows, K = 16 per instruction, fp32 accumulate in TMEM) and commits to the
-//    stage's mbarrier; two stages keep dequant, TMA and MMA overlapped;
+//    stage's mbarrier; the token tiles of step k+1 are fetched while step k
+//    multiplies, so dequant, TMA and MMA overlap; only that thread waits on
+//    mbarriers;
 //  * the epilogue reads TMEM with tcgen05.ld: gate_up tiles (64 gate + 64 up
 //    rows) write h = silu(gate) * up in fp16, down tiles write y in fp32.
 // Every mbarrier wait is bounded and reports PW_STATUS_TIMEOUT.
@@ -37,16 +41,18 @@ constexpr int kBM = 128;                       // tokens per tile (MMA M)
 constexpr int kBN = 128;                       // weight rows per tile (MMA N)
 constexpr int kBK = 64;                        // K per stage: one 128-byte swizzle row of fp16
 constexpr int kPStages = 2;
-constexpr int kMT = 4;                         // token tiles sharing one dequantised weight tile
+constexpr int kMT = 3;                         // token tiles sharing one dequantised weight tile
 constexpr int kTileBytes = kBM * kBK * 2;      // 16 KB, A and B alike
 constexpr int kPLutBytes = 256 * kBN * 2;      // fp16 [v][128 rows]
 constexpr int kOffA = 0;                       // [stage][token tile] 16 KB boxes
 constexpr int kOffB = kOffA + kPStages * kMT * kTileBytes;
 constexpr int kOffLut = kOffB + kPStages * kTileBytes;
-constexpr int kOffBar = kOffLut + kPLutBytes;
+constexpr int kPlaneChunkBytes = PW_MAX_BITS * kBM * 16;   // 16 bytes (2 K steps) per row per plane
+constexpr int kOffPl = kOffLut + kPLutBytes;               // [2 chunks][plane][row][4 words]
+constexpr int kOffBar = kOffPl + 2 * kPlaneChunkBytes;
 constexpr int kMiscBytes = 64 + 16 + 4 * (256 + 1) + 64;   // barriers, TMEM address, item prefix per expert
 constexpr int kPSmemBytes = kOffBar + kMiscBytes + 1024;   // + slack to align the base to 1 KB
-constexpr uint32_t kTmemCols = kMT * kBN;     // one 128-column fp32 accumulator per token tile
+constexpr uint32_t kTmemCols = 512;           // kMT 128-column fp32 accumulators (power-of-two allocation)
 constexpr long long kWaitLimit = 1ll << 22;
 
 __device__ __forceinline__ uint32_t saddr(const void* p) {
@@ -265,41 +271,60 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
     }
     __syncthreads();
 
-    // plane words of K step ks for this thread: word 2*ks + half of its row
-    uint32_t cur[PW_MAX_BITS], nxt[PW_MAX_BITS];
-    auto load_words = [&](int ks, uint32_t (&w)[PW_MAX_BITS]) {
+    // plane chunks: 16 bytes (4 words = K steps 2j, 2j+1) per row and plane;
+    // thread (row, group) copies planes 4*group .. 4*group+3 of its row
+    const int cgrp = tid >> 7;
+    auto fetch_chunk = [&](int j) {
+      if (grow >= 0 && 2 * j < nksteps) {
+        unsigned char* dst = smem + kOffPl + (j & 1) * kPlaneChunkBytes + row * 16;
 #pragma unroll
-      for (int pl = 0; pl < PW_MAX_BITS; ++pl)
-        w[pl] = (pl < Q && grow >= 0 && ks < nksteps)
-                    ? __ldg(d.planes[pl] + static_cast<size_t>(grow) * W + 2 * ks + half)
-                    : 0u;
+        for (int u = 0; u < 4; ++u) {
+          const int pl = cgrp * 4 + u;
+          const uint32_t* src = cgrp ? d.planes[4 + u] : d.planes[u];
+          if (pl < Q) {
+            const uint32_t* gsrc = src + static_cast<size_t>(grow) * W + 4 * j;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr(dst + pl * kBM * 16)),
+                         "l"(gsrc));
+          }
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    load_words(0, cur);
+    const uint32_t g0 = g;
+    if (tid == 0) {   // token tiles of K step 0 (stage g0: free, the previous item's MMAs are done)
+      const int s0 = g0 & 1;
+      mbar_expect_tx(bar_full + 8 * s0, nm * kTileBytes);
+      for (int m = 0; m < nm; ++m)
+        tma_load_2d(sbase + kOffA + (s0 * kMT + m) * kTileBytes, &tmA, 0, row0 + m * kBM, bar_full + 8 * s0);
+    }
+    fetch_chunk(0);
+    fetch_chunk(1);
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    __syncthreads();
 
+    uint4 pw4[PW_MAX_BITS];
     for (int ks = 0; ks < nksteps; ++ks, ++g) {
       const int s = g & 1;
       const uint32_t use = g >> 1;
-      load_words(ks + 1, nxt);
-      // stage s is free once the MMAs of its previous use are done
-      if (use > 0 && !mbar_wait(bar_mma + 8 * s, (use - 1) & 1)) {
-        atomicOr(p.status, PW_STATUS_TIMEOUT);
-        s_misc[1] = 1;
-      }
-      if (tid == 0) {
-        mbar_expect_tx(bar_full + 8 * s, nm * kTileBytes);
-        for (int m = 0; m < nm; ++m)
-          tma_load_2d(sbase + kOffA + (s * kMT + m) * kTileBytes, &tmA, ks * kBK, row0 + m * kBM,
-                      bar_full + 8 * s);
+      if ((ks & 1) == 0) {   // a new plane chunk: its 4 words per plane into registers
+        const unsigned char* src = smem + kOffPl + ((ks >> 1) & 1) * kPlaneChunkBytes + row * 16;
+#pragma unroll
+        for (int pl = 0; pl < PW_MAX_BITS; ++pl)
+          pw4[pl] = (pl < Q) ? *reinterpret_cast<const uint4*>(src + pl * kBM * 16) : make_uint4(0, 0, 0, 0);
       }
       // dequantise 32 weights of this row into the swizzled B tile
       {
         uint32_t o[8];
+        const int wsel = (ks & 1) * 2 + half;
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
           uint32_t w = 0;
 #pragma unroll
           for (int pl = 0; pl < PW_MAX_BITS; ++pl)
-            if (pl == Q - 1 - r) w = cur[pl];
+            if (pl == Q - 1 - r) {
+              const uint4 v = pw4[pl];
+              w = wsel == 0 ? v.x : wsel == 1 ? v.y : wsel == 2 ? v.z : v.w;
+            }
           o[r] = (r < Q) ? w : 0u;
         }
         transpose8(o);
@@ -326,8 +351,9 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
       }
       proxy_fence_smem();   // generic-proxy writes of B visible to the tensor core
       tc_fence_before();
-      __syncthreads();
-      if (s_misc[1]) break;   // a bounded wait gave up: stop issuing work
+      __syncthreads();      // B(ks) complete; every thread is done reading the current chunk
+      if (s_misc[1]) break; // a bounded wait gave up: stop issuing work
+      if ((ks & 1) == 0) fetch_chunk((ks >> 1) + 2);   // refill the buffer just read
       if (tid == 0) {
         if (!mbar_wait(bar_full + 8 * s, use & 1)) {
           atomicOr(p.status, PW_STATUS_TIMEOUT);
@@ -342,19 +368,35 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
               mma_f16(tmem + m * kBN, smem_desc(a0 + kk * 32), smem_desc(b0 + kk * 32), (ks | kk) != 0);
           }
           mma_commit(bar_mma + 8 * s);
+          // stage s^1 frees once the MMAs of step ks-1 finish: then fetch step ks+1's tokens
+          if (ks + 1 < nksteps) {
+            if (g > g0 && !mbar_wait(bar_mma + 8 * (s ^ 1), ((g - 1) >> 1) & 1)) {
+              atomicOr(p.status, PW_STATUS_TIMEOUT);
+              s_misc[1] = 1;
+            } else {
+              mbar_expect_tx(bar_full + 8 * (s ^ 1), nm * kTileBytes);
+              for (int m = 0; m < nm; ++m)
+                tma_load_2d(sbase + kOffA + ((s ^ 1) * kMT + m) * kTileBytes, &tmA, (ks + 1) * kBK,
+                            row0 + m * kBM, bar_full + 8 * (s ^ 1));
+            }
+          }
         }
       }
-#pragma unroll
-      for (int pl = 0; pl < PW_MAX_BITS; ++pl) cur[pl] = nxt[pl];
+      if (ks & 1) asm volatile("cp.async.wait_group 1;" ::: "memory");   // next chunk landed
+      tc_fence_before();
+      __syncthreads();      // B(ks+1)'s buffer is free (step ks-1's MMAs done), next chunk visible
+      tc_fence_after();
     }
 
     // ---- epilogue: wait for the tile's last MMAs, then TMEM -> registers -> global
     {
       const uint32_t gl = g - 1;
-      if (!mbar_wait(bar_mma + 8 * (gl & 1), (gl >> 1) & 1)) {
+      if (tid == 0 && !mbar_wait(bar_mma + 8 * (gl & 1), (gl >> 1) & 1)) {
         atomicOr(p.status, PW_STATUS_TIMEOUT);
         s_misc[1] = 1;
       }
+      tc_fence_before();
+      __syncthreads();
       tc_fence_after();
       const int lg = warp & 3, ch = warp >> 2;
       for (int m = 0; m < nm; ++m) {
