@@ -54,6 +54,11 @@ _SIGS = {
     "pw_set_commit": (_i, [_vp, _i, _i, _i, _i, _vp]),
     "pw_reload_async": (_i, [_vp, _i, _i, _i, _i, _vp]),
     "pw_reload_query": (_i, [_vp, _i, _i, _i]),
+    "pw_reload_many": (_i, [_vp, _i, _pi, _pi, _pi, _pi, _vp, _pi]),
+    "pw_set_commit_many": (_i, [_vp, _i, _pi, _pi, _pi, _pi, _vp]),
+    "pw_mover_start": (_i, [_vp, _vp, _sz]),
+    "pw_mover_submit": (_i, [_vp, _i, _pi, _pi, _pi, _pi]),
+    "pw_commit_arrived": (_i, [_vp, _vp, _pi, _pi]),
     "pw_block_state": (_i, [_vp, _i, _i, _i, _pi, _pi, _pi]),
     "pw_table_destroy": (_i, [_vp]),
     "pw_debug_fail_next_reload": (_i, [_vp]),
@@ -213,6 +218,46 @@ class PagedMoE:
     def pw_reload_async(self, layer, expert, kind, q_target, stream=None):
         return _check(lib().pw_reload_async(self._t, layer, expert, kind, q_target, _stream(stream)),
                       "pw_reload_async")
+
+    @staticmethod
+    def _columns(items):
+        """[(layer, expert, kind, q), ...] -> four ctypes int arrays."""
+        n = len(items)
+        cols = [(ctypes.c_int * n)(*[int(it[j]) for it in items]) for j in range(4)]
+        return n, cols
+
+    def pw_reload_many(self, items, stream=None):
+        """items: [(layer, expert, kind, q_target)].  Returns the number enqueued;
+        raises PWError on the first failing block."""
+        n, (l, e, k, q) = self._columns(items)
+        done = _i()
+        rc = lib().pw_reload_many(self._t, n, l, e, k, q, _stream(stream), ctypes.byref(done))
+        _check(rc, "pw_reload_many")
+        return done.value
+
+    def pw_set_commit_many(self, items, stream=None):
+        """items: [(layer, expert, kind, q)], committed at one stream boundary."""
+        n, (l, e, k, q) = self._columns(items)
+        return _check(lib().pw_set_commit_many(self._t, n, l, e, k, q, _stream(stream)),
+                      "pw_set_commit_many")
+
+    def pw_mover_start(self, stream, max_inflight_bytes: int = 64 << 20):
+        """Starts the table's reload mover thread on the given copy stream."""
+        return _check(lib().pw_mover_start(self._t, _stream(stream), max_inflight_bytes),
+                      "pw_mover_start")
+
+    def pw_mover_submit(self, items):
+        """items: [(layer, expert, kind, q_target)], reloaded in order and
+        committed by pw_commit_arrived once landed."""
+        n, (l, e, k, q) = self._columns(items)
+        return _check(lib().pw_mover_submit(self._t, n, l, e, k, q), "pw_mover_submit")
+
+    def pw_commit_arrived(self, stream=None):
+        """Commits every landed mover reload; returns (committed, outstanding)."""
+        c, o = _i(), _i()
+        _check(lib().pw_commit_arrived(self._t, _stream(stream), ctypes.byref(c), ctypes.byref(o)),
+               "pw_commit_arrived")
+        return c.value, o.value
 
     def pw_reload_query(self, layer, expert, kind) -> int:
         return _check(lib().pw_reload_query(self._t, layer, expert, kind), "pw_reload_query")

@@ -107,6 +107,16 @@ int table_shape(const pw_table* t, int* E, int* H, int* I);
 
 // Kernel launchers (pw_kernels.cu).  Return cudaSuccess or the launch error.
 cudaError_t launch_commit(BlockDesc* dst, const BlockDesc& value, cudaStream_t s);
+
+// Up to kCommitBatch descriptor writes carried by value in one launch.
+constexpr int kCommitBatch = 192;
+struct CommitBatch {
+  int32_t n;
+  uint32_t index[kCommitBatch];       // desc_index of each block
+  uint32_t words[kCommitBatch][32];   // the 128-byte descriptors
+};
+static_assert(sizeof(CommitBatch) < 32000, "kernel parameter block limit");
+cudaError_t launch_commit_batch(BlockDesc* table, const CommitBatch& b, cudaStream_t s);
 cudaError_t launch_forward(const ForwardArgs& a, cudaStream_t s);
 
 }  // namespace pw

@@ -35,6 +35,20 @@ cudaError_t launch_commit(BlockDesc* dst, const BlockDesc& value, cudaStream_t s
   return cudaGetLastError();
 }
 
+// Many descriptors in one launch: they travel in the kernel's parameter block
+// (under the 32 KB limit), one warp per descriptor, one 4-byte word per lane.
+__global__ void __launch_bounds__(32) k_commit_batch(BlockDesc* table, CommitBatch b) {
+  const int i = blockIdx.x;
+  if (i >= b.n) return;
+  reinterpret_cast<uint32_t*>(table + b.index[i])[threadIdx.x] = b.words[i][threadIdx.x];
+}
+
+cudaError_t launch_commit_batch(BlockDesc* table, const CommitBatch& b, cudaStream_t s) {
+  if (b.n <= 0) return cudaSuccess;
+  k_commit_batch<<<b.n, 32, 0, s>>>(table, b);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ routing + permutation
 
 constexpr int kRouteThreads = 1024;

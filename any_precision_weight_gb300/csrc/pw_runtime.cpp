@@ -12,10 +12,14 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <algorithm>
+#include <condition_variable>
 #include <cstring>
+#include <deque>
 #include <mutex>
 #include <new>
 #include <string>
+#include <chrono>
 #include <thread>
 #include <vector>
 
@@ -90,7 +94,14 @@ struct BlockState {
   int resident = 0;          // planes [0, resident) and tables b <= resident on device
   int pending = 0;           // target of the reload in flight (0: none)
   bool failed = false;       // the pending reload could not be enqueued or failed
+  bool issued = false;       // the pending reload's copies and event are enqueued
+  int commit_to = 0;         // submitted through the mover: commit this q on arrival
   cudaEvent_t ev = nullptr;  // recorded after the reload's copies
+};
+
+// One reload submitted to the mover.
+struct MoveReq {
+  int layer, expert, kind, q;
 };
 
 }  // namespace
@@ -100,7 +111,25 @@ struct pw_table {
   pw::BlockDesc* d_desc = nullptr;
   std::vector<BlockState> blocks;
   std::mutex mu;
+  std::condition_variable enqueued;   // signalled when a reload's enqueue phase ends
   bool fail_next_reload = false;   // test hook, see pw_debug_fail_next_reload
+
+  // The reload mover (pw_mover_start): a host thread that takes submitted
+  // reloads in order and enqueues them with a bound on the bytes in flight.
+  // mover_mu guards the request queue and the mover's own fields; the table
+  // lock mu guards block state and the arrival list.
+  std::thread mover;
+  std::mutex mover_mu;
+  std::condition_variable mover_cv;
+  std::deque<MoveReq> requests;
+  bool mover_stop = false;
+  int mover_busy = 0;                 // requests taken off the queue, not yet enqueued
+  cudaStream_t mover_stream = nullptr;
+  size_t mover_limit = 0;
+  int mover_device = 0;
+  int mover_error = PW_OK;            // first failure of the mover, reported by pw_commit_arrived
+  std::string mover_error_msg;
+  std::deque<size_t> arrivals;        // block indices enqueued by the mover, issue order (under mu)
 };
 
 namespace {
@@ -135,6 +164,236 @@ int write_desc(pw_table* t, int layer, int expert, int kind, const BlockState& b
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// One block's reload.  The table lock is held only to check and claim the
+// block and to publish the outcome, not while the copies are enqueued (an
+// enqueue can block while the copy queue is full), so other host threads may
+// query, commit and launch forward passes meanwhile.  A claimed block reads
+// as in flight until its event is recorded.
+int reload_one(pw_table* t, int layer, int expert, int kind, int q_target, cudaStream_t st) {
+  BlockState c;               // what the enqueue phase needs, read under the lock
+  bool inject = false;
+  BlockState* b = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(t->mu);
+    b = block_of(t, layer, expert, kind);
+    if (!b || !b->registered) return fail(PW_EINVAL, "pw_reload_async: block not registered");
+    if (q_target < b->b_min || q_target > b->n_bits)
+      return fail(PW_EINVAL, "pw_reload_async: q_target %d outside [%d, %d]", q_target, b->b_min,
+                  b->n_bits);
+    if (b->pending && !b->failed)
+      return fail(PW_EINVAL, "pw_reload_async: a reload of this block is pending");
+    if (b->pending && b->failed) {     // retry after a failed reload: wait out its copies
+      if (b->ev) cudaEventSynchronize(b->ev);
+      b->pending = 0;
+      b->failed = false;
+    }
+    if (q_target <= b->resident) return PW_OK;
+    for (int p = b->resident; p < q_target; ++p)
+      if (!b->pages[p]) return fail(PW_EINVAL, "pw_reload_async: no device page for plane %d", p);
+    if (!b->ev) {
+      const cudaError_t e = cudaEventCreateWithFlags(&b->ev, cudaEventDisableTiming);
+      if (e != cudaSuccess) return cuda_fail(e, "pw_reload_async: event create");
+    }
+    inject = t->fail_next_reload;
+    t->fail_next_reload = false;
+    b->pending = q_target;
+    b->failed = false;
+    b->issued = false;
+    c = *b;
+  }
+  const size_t pb = pw_plane_bytes(c.R, c.K);
+  cudaError_t e = inject ? cudaErrorInvalidValue : cudaSuccess;   // injected: nothing enqueued
+  // Planes are contiguous in the host store; consecutive device pages that are
+  // also contiguous go in one copy.
+  for (int p = c.resident; p < q_target && e == cudaSuccess;) {
+    int p1 = p + 1;
+    while (p1 < q_target && static_cast<unsigned char*>(c.pages[p1]) ==
+                                static_cast<unsigned char*>(c.pages[p]) + (p1 - p) * pb)
+      ++p1;
+    e = cudaMemcpyAsync(c.pages[p], c.host_planes + p * (pb / 4), (p1 - p) * pb,
+                        cudaMemcpyHostToDevice, st);
+    p = p1;
+  }
+  if (e == cudaSuccess) {
+    const size_t lo = pw_lut_offset(c.R, c.b_min, c.resident + 1);
+    const size_t hi = pw_lut_offset(c.R, c.b_min, q_target + 1);
+    e = cudaMemcpyAsync(static_cast<unsigned char*>(c.d_luts) + lo,
+                        reinterpret_cast<const unsigned char*>(c.host_luts) + lo, hi - lo,
+                        cudaMemcpyHostToDevice, st);
+  }
+  if (e == cudaSuccess) e = cudaEventRecord(c.ev, st);
+  {
+    std::lock_guard<std::mutex> lk(t->mu);
+    if (e == cudaSuccess) b->issued = true;
+    else b->failed = true;
+  }
+  t->enqueued.notify_all();
+  if (e != cudaSuccess) return cuda_fail(e, "pw_reload_async: enqueue");
+  return PW_OK;
+}
+
+
+// Bytes a reload of b to q would copy (planes above resident and their tables).
+size_t reload_bytes(const BlockState& b, int q) {
+  if (q <= b.resident) return 0;
+  return static_cast<size_t>(q - b.resident) * pw_plane_bytes(b.R, b.K) +
+         pw_lut_offset(b.R, b.b_min, q + 1) - pw_lut_offset(b.R, b.b_min, b.resident + 1);
+}
+
+// The mover thread: takes requests in order, keeps at most mover_limit bytes
+// of copies in the copy queue (so that no enqueue blocks in the driver while
+// other threads launch), and lists each enqueued block for pw_commit_arrived.
+void mover_main(pw_table* t) {
+  cudaSetDevice(t->mover_device);
+  struct Flight {
+    size_t bytes;
+    cudaEvent_t ev;
+  };
+  std::deque<Flight> flight;
+  std::vector<cudaEvent_t> spare;
+  size_t inflight = 0;
+  auto note_error = [t](int rc, const char* msg) {
+    std::lock_guard<std::mutex> lk(t->mover_mu);
+    if (t->mover_error == PW_OK) {
+      t->mover_error = rc;
+      t->mover_error_msg = msg;
+    }
+  };
+  for (;;) {
+    MoveReq r;
+    {
+      std::unique_lock<std::mutex> lk(t->mover_mu);
+      t->mover_cv.wait(lk, [t] { return t->mover_stop || !t->requests.empty(); });
+      if (t->mover_stop) break;
+      r = t->requests.front();
+      t->requests.pop_front();
+      ++t->mover_busy;
+    }
+    size_t bytes = 0;
+    size_t idx = 0;
+    {
+      std::lock_guard<std::mutex> lk(t->mu);
+      BlockState* b = block_of(t, r.layer, r.expert, r.kind);
+      if (b) {
+        bytes = reload_bytes(*b, r.q);
+        idx = pw::desc_index(r.layer, r.expert, r.kind, t->E);
+      }
+    }
+    while (!flight.empty() && inflight + bytes > t->mover_limit) {
+      const cudaError_t q = cudaEventQuery(flight.front().ev);
+      if (q == cudaSuccess) {
+        inflight -= flight.front().bytes;
+        spare.push_back(flight.front().ev);
+        flight.pop_front();
+      } else if (q == cudaErrorNotReady) {
+        std::this_thread::sleep_for(std::chrono::microseconds(20));
+      } else {
+        note_error(PW_ECUDA, cudaGetErrorString(q));
+        break;
+      }
+    }
+    const int rc = reload_one(t, r.layer, r.expert, r.kind, r.q, t->mover_stream);
+    if (rc == PW_OK) {
+      {
+        std::lock_guard<std::mutex> lk(t->mu);
+        t->blocks[idx].commit_to = r.q;
+        t->arrivals.push_back(idx);
+      }
+      cudaEvent_t ev = nullptr;
+      if (!spare.empty()) {
+        ev = spare.back();
+        spare.pop_back();
+      } else if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+        ev = nullptr;
+      }
+      if (ev && cudaEventRecord(ev, t->mover_stream) == cudaSuccess) {
+        flight.push_back({bytes, ev});
+        inflight += bytes;
+      } else if (ev) {
+        spare.push_back(ev);
+      }
+    } else {
+      note_error(rc, pw_last_error());
+    }
+    {
+      std::lock_guard<std::mutex> lk(t->mover_mu);
+      --t->mover_busy;
+    }
+    t->mover_cv.notify_all();
+  }
+  for (auto& f : flight) {
+    cudaEventSynchronize(f.ev);
+    cudaEventDestroy(f.ev);
+  }
+  for (auto ev : spare) cudaEventDestroy(ev);
+}
+
+void mover_stop(pw_table* t) {
+  {
+    std::lock_guard<std::mutex> lk(t->mover_mu);
+    t->mover_stop = true;
+  }
+  t->mover_cv.notify_all();
+  if (t->mover.joinable()) t->mover.join();
+}
+
+// Writes n descriptors (block index, committed q) on s, one launch per batch.
+int commit_descs(pw_table* t, const std::vector<std::pair<size_t, int>>& list, cudaStream_t s) {
+  static thread_local pw::CommitBatch batch;
+  const size_t n = list.size();
+  for (size_t i0 = 0; i0 < n; i0 += pw::kCommitBatch) {
+    const int m = static_cast<int>(std::min<size_t>(pw::kCommitBatch, n - i0));
+    batch.n = m;
+    for (int j = 0; j < m; ++j) {
+      const auto& it = list[i0 + j];
+      const pw::BlockDesc d = make_desc(t->blocks[it.first], it.second);
+      batch.index[j] = static_cast<uint32_t>(it.first);
+      std::memcpy(batch.words[j], &d, sizeof d);
+    }
+    const cudaError_t e = pw::launch_commit_batch(t->d_desc, batch, s);
+    if (e != cudaSuccess) return cuda_fail(e, "commit launch");
+    for (int j = 0; j < m; ++j) t->blocks[list[i0 + j].first].q = list[i0 + j].second;
+  }
+  return PW_OK;
+}
+
+// Checks that q may be committed for one block; no state changes.  lk holds
+// t->mu; if another thread is still enqueueing the block's reload, waits for
+// that to finish (the wait releases the lock).
+int commit_check(pw_table* t, std::unique_lock<std::mutex>& lk, int layer, int expert, int kind,
+                 int q, BlockState** out) {
+  BlockState* b = block_of(t, layer, expert, kind);
+  if (!b || !b->registered) return fail(PW_EINVAL, "pw_set_commit: block not registered");
+  if (q < b->b_min || q > b->n_bits)
+    return fail(PW_EINVAL, "pw_set_commit: q %d outside [%d, %d]", q, b->b_min, b->n_bits);
+  if (q > b->resident) {
+    if (!b->pending || b->pending < q)
+      return fail(PW_ENOTRESIDENT, "pw_set_commit: q %d above the %d resident planes, no reload",
+                  q, b->resident);
+    t->enqueued.wait(lk, [b] { return b->issued || b->failed || !b->pending; });
+    if (q > b->resident) {
+      if (b->failed) return fail(PW_ERELOAD, "pw_set_commit: the reload to %d failed", b->pending);
+      if (!b->pending || b->pending < q)
+        return fail(PW_ENOTRESIDENT, "pw_set_commit: q %d above the %d resident planes, no reload",
+                    q, b->resident);
+    }
+  }
+  *out = b;
+  return PW_OK;
+}
+
+// Orders the compute stream after the block's reload when q needs its planes.
+int commit_order(BlockState* b, int q, cudaStream_t st) {
+  if (q <= b->resident) return PW_OK;
+  const cudaError_t e = cudaStreamWaitEvent(st, b->ev, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "pw_set_commit: stream wait");
+  // From here on the compute stream is ordered after the copies.
+  b->resident = b->pending;
+  b->pending = 0;
+  return PW_OK;
+}
+
 
 }  // namespace
 
@@ -190,30 +449,58 @@ int pw_pack(const uint8_t* idx, int R, int K, int n_bits, const uint16_t* parent
   if (static_cast<size_t>(R) * K < (1u << 20)) nthr = 1;
   if (nthr > 64) nthr = 64;
   std::vector<int> bad_row(nthr, -1);
+  // Bytes of an index that must be zero when n < 8, replicated over 8 indices.
+  const uint64_t high = 0x0101010101010101ull * ((0xFFu << n_bits) & 0xFFu);
   auto work = [&](unsigned tid) {
+    double sums[2 * 256];   // level b holds the 2^b sums of 2^(n-b) parents, at offset 2^b
     for (int r = static_cast<int>(tid); r < R; r += static_cast<int>(nthr)) {
       const uint8_t* row = idx + static_cast<size_t>(r) * K;
+      uint64_t seen = 0;
       for (int w = 0; w < W; ++w) {
-        uint32_t words[PW_MAX_BITS] = {};
-        for (int j = 0; j < 32; ++j) {
-          const unsigned v = row[32 * w + j];
-          if (static_cast<int>(v) >= limit) { bad_row[tid] = r; return; }
-          for (int p = 0; p < n_bits; ++p) words[p] |= ((v >> (n_bits - 1 - p)) & 1u) << j;
+        // Four 8x8 bit transposes: byte i of y[g] holds bit i of indices 8g..8g+7,
+        // index 8g+j at bit j, i.e. exactly byte g of the 32-bit word of bit i.
+        uint64_t y[4];
+        for (int g = 0; g < 4; ++g) {
+          const uint8_t* b = row + 32 * w + 8 * g;
+          uint64_t x = 0;
+          for (int j = 0; j < 8; ++j) x |= static_cast<uint64_t>(b[j]) << (8 * j);
+          seen |= x;
+          uint64_t t = (x ^ (x >> 7)) & 0x00AA00AA00AA00AAull;
+          x ^= t ^ (t << 7);
+          t = (x ^ (x >> 14)) & 0x0000CCCC0000CCCCull;
+          x ^= t ^ (t << 14);
+          t = (x ^ (x >> 28)) & 0x00000000F0F0F0F0ull;
+          x ^= t ^ (t << 28);
+          y[g] = x;
         }
-        for (int p = 0; p < n_bits; ++p)
-          planes_out[p * plane_words + static_cast<size_t>(r) * W + w] = words[p];
+        for (int p = 0; p < n_bits; ++p) {
+          const int sh = 8 * (n_bits - 1 - p);   // plane p holds bit n-1-p
+          const uint32_t word = static_cast<uint32_t>((y[0] >> sh) & 0xFF) |
+                                static_cast<uint32_t>((y[1] >> sh) & 0xFF) << 8 |
+                                static_cast<uint32_t>((y[2] >> sh) & 0xFF) << 16 |
+                                static_cast<uint32_t>((y[3] >> sh) & 0xFF) << 24;
+          planes_out[p * plane_words + static_cast<size_t>(r) * W + w] = word;
+        }
       }
-      // tables LUT_b for b = b_min..n_bits
+      if (seen & high) { bad_row[tid] = r; return; }
+      // Tables LUT_b for b = b_min..n.  Entry j of LUT_b is the mean of parents
+      // j*g .. j*g+g-1, g = 2^(n-b).  The sums are built level by level, each
+      // the sum of two sums one level up; every fp16 value is an integer
+      // multiple of 2^-24 below 2^16, so each partial sum is exact in fp64 and
+      // equals the sum taken in any order.
       const uint16_t* par = parent_lut + static_cast<size_t>(r) * limit;
+      for (int j = 0; j < limit; ++j) sums[limit + j] = half_to_double(par[j]);
+      for (int b = n_bits - 1; b >= b_min; --b)
+        for (int j = 0; j < (1 << b); ++j)
+          sums[(1 << b) + j] = sums[(2 << b) + 2 * j] + sums[(2 << b) + 2 * j + 1];
       for (int b = b_min; b <= n_bits; ++b) {
         uint16_t* dst = luts_out + pw_lut_offset(R, b_min, b) / 2 + static_cast<size_t>(r) * (1u << b);
         const int g = 1 << (n_bits - b);
-        for (int j = 0; j < (1 << b); ++j) {
-          if (g == 1) { dst[j] = par[j]; continue; }
-          double s = 0.0;   // exact: a few hundred fp16 values fit in fp64's significand
-          for (int i = 0; i < g; ++i) s += half_to_double(par[j * g + i]);
-          dst[j] = double_to_half(s / g);
+        if (g == 1) {
+          for (int j = 0; j < limit; ++j) dst[j] = par[j];
+          continue;
         }
+        for (int j = 0; j < (1 << b); ++j) dst[j] = double_to_half(sums[(1 << b) + j] / g);
       }
     }
   };
@@ -320,48 +607,20 @@ int pw_block_register(pw_table* t, int layer, int expert, int kind, int n_bits, 
 
 int pw_reload_async(pw_table* t, int layer, int expert, int kind, int q_target, pw_stream_t copy) {
   if (!t) return fail(PW_EINVAL, "pw_reload_async: null table");
-  std::lock_guard<std::mutex> lk(t->mu);
-  BlockState* b = block_of(t, layer, expert, kind);
-  if (!b || !b->registered) return fail(PW_EINVAL, "pw_reload_async: block not registered");
-  if (q_target < b->b_min || q_target > b->n_bits)
-    return fail(PW_EINVAL, "pw_reload_async: q_target %d outside [%d, %d]", q_target, b->b_min,
-                b->n_bits);
-  if (b->pending && !b->failed)
-    return fail(PW_EINVAL, "pw_reload_async: a reload of this block is pending");
-  if (b->pending && b->failed) {     // retry after a failed reload: wait out its copies
-    if (b->ev) cudaEventSynchronize(b->ev);
-    b->pending = 0;
-    b->failed = false;
-  }
-  if (q_target <= b->resident) return PW_OK;
-  for (int p = b->resident; p < q_target; ++p)
-    if (!b->pages[p]) return fail(PW_EINVAL, "pw_reload_async: no device page for plane %d", p);
+  return reload_one(t, layer, expert, kind, q_target, reinterpret_cast<cudaStream_t>(copy));
+}
+
+int pw_reload_many(pw_table* t, int n, const int* layer, const int* expert, const int* kind,
+                   const int* q_target, pw_stream_t copy, int* n_done) {
+  if (n_done) *n_done = 0;
+  if (!t) return fail(PW_EINVAL, "pw_reload_many: null table");
+  if (n < 0 || (n > 0 && (!layer || !expert || !kind || !q_target)))
+    return fail(PW_EINVAL, "pw_reload_many: bad count or null array");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(copy);
-  if (!b->ev) {
-    const cudaError_t e = cudaEventCreateWithFlags(&b->ev, cudaEventDisableTiming);
-    if (e != cudaSuccess) return cuda_fail(e, "pw_reload_async: event create");
-  }
-  b->failed = false;
-  const size_t pb = pw_plane_bytes(b->R, b->K);
-  cudaError_t e = cudaSuccess;
-  if (t->fail_next_reload) {          // injected failure: nothing is enqueued
-    t->fail_next_reload = false;
-    e = cudaErrorInvalidValue;
-  }
-  for (int p = b->resident; p < q_target && e == cudaSuccess; ++p)
-    e = cudaMemcpyAsync(b->pages[p], b->host_planes + p * (pb / 4), pb, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) {
-    const size_t lo = pw_lut_offset(b->R, b->b_min, b->resident + 1);
-    const size_t hi = pw_lut_offset(b->R, b->b_min, q_target + 1);
-    e = cudaMemcpyAsync(static_cast<unsigned char*>(b->d_luts) + lo,
-                        reinterpret_cast<const unsigned char*>(b->host_luts) + lo, hi - lo,
-                        cudaMemcpyHostToDevice, st);
-  }
-  if (e == cudaSuccess) e = cudaEventRecord(b->ev, st);
-  b->pending = q_target;
-  if (e != cudaSuccess) {
-    b->failed = true;
-    return cuda_fail(e, "pw_reload_async: enqueue");
+  for (int i = 0; i < n; ++i) {
+    const int rc = reload_one(t, layer[i], expert[i], kind[i], q_target[i], st);
+    if (rc != PW_OK) return rc;
+    if (n_done) *n_done = i + 1;
   }
   return PW_OK;
 }
@@ -373,6 +632,7 @@ int pw_reload_query(pw_table* t, int layer, int expert, int kind) {
   if (!b || !b->registered) return fail(PW_EINVAL, "pw_reload_query: block not registered");
   if (!b->pending) return 1;
   if (b->failed) return fail(PW_ERELOAD, "pw_reload_query: reload failed");
+  if (!b->issued) return 0;   // another thread is still enqueueing its copies
   const cudaError_t e = cudaEventQuery(b->ev);
   if (e == cudaSuccess) {
     b->resident = b->pending;   // copies done: visible to every later launch
@@ -386,27 +646,140 @@ int pw_reload_query(pw_table* t, int layer, int expert, int kind) {
 
 int pw_set_commit(pw_table* t, int layer, int expert, int kind, int q, pw_stream_t compute) {
   if (!t) return fail(PW_EINVAL, "pw_set_commit: null table");
-  std::lock_guard<std::mutex> lk(t->mu);
-  BlockState* b = block_of(t, layer, expert, kind);
-  if (!b || !b->registered) return fail(PW_EINVAL, "pw_set_commit: block not registered");
-  if (q < b->b_min || q > b->n_bits)
-    return fail(PW_EINVAL, "pw_set_commit: q %d outside [%d, %d]", q, b->b_min, b->n_bits);
+  std::unique_lock<std::mutex> lk(t->mu);
+  BlockState* b = nullptr;
+  int rc = commit_check(t, lk, layer, expert, kind, q, &b);
+  if (rc != PW_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(compute);
-  if (q > b->resident) {
-    if (!b->pending || b->pending < q)
-      return fail(PW_ENOTRESIDENT, "pw_set_commit: q %d above the %d resident planes, no reload",
-                  q, b->resident);
-    if (b->failed) return fail(PW_ERELOAD, "pw_set_commit: the reload to %d failed", b->pending);
-    const cudaError_t e = cudaStreamWaitEvent(st, b->ev, 0);
-    if (e != cudaSuccess) return cuda_fail(e, "pw_set_commit: stream wait");
-    // From here on the compute stream is ordered after the copies.
-    b->resident = b->pending;
-    b->pending = 0;
-  }
-  const int rc = write_desc(t, layer, expert, kind, *b, q, st);
+  rc = commit_order(b, q, st);
+  if (rc != PW_OK) return rc;
+  rc = write_desc(t, layer, expert, kind, *b, q, st);
   if (rc != PW_OK) return rc;
   b->q = q;
   return PW_OK;
+}
+
+int pw_set_commit_many(pw_table* t, int n, const int* layer, const int* expert, const int* kind,
+                       const int* q, pw_stream_t compute) {
+  if (!t) return fail(PW_EINVAL, "pw_set_commit_many: null table");
+  if (n < 0 || (n > 0 && (!layer || !expert || !kind || !q)))
+    return fail(PW_EINVAL, "pw_set_commit_many: bad count or null array");
+  std::unique_lock<std::mutex> lk(t->mu);
+  std::vector<BlockState*> bs(static_cast<size_t>(n));
+  for (int i = 0; i < n; ++i) {          // all or nothing: every entry is checked first
+    const int rc = commit_check(t, lk, layer[i], expert[i], kind[i], q[i], &bs[i]);
+    if (rc != PW_OK) return rc;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(compute);
+  for (int i = 0; i < n; ++i) {
+    const int rc = commit_order(bs[i], q[i], st);
+    if (rc != PW_OK) return rc;
+  }
+  std::vector<std::pair<size_t, int>> list(static_cast<size_t>(n));
+  for (int i = 0; i < n; ++i) list[i] = {pw::desc_index(layer[i], expert[i], kind[i], t->E), q[i]};
+  const int rc = commit_descs(t, list, st);
+  if (rc != PW_OK) return rc;
+  return PW_OK;
+}
+
+int pw_mover_start(pw_table* t, pw_stream_t copy, size_t max_inflight_bytes) {
+  if (!t) return fail(PW_EINVAL, "pw_mover_start: null table");
+  if (max_inflight_bytes == 0) return fail(PW_EINVAL, "pw_mover_start: max_inflight_bytes is 0");
+  std::lock_guard<std::mutex> lk(t->mover_mu);
+  if (t->mover.joinable()) return fail(PW_EINVAL, "pw_mover_start: the mover is already running");
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "pw_mover_start: current device");
+  t->mover_device = dev;
+  t->mover_stream = reinterpret_cast<cudaStream_t>(copy);
+  t->mover_limit = max_inflight_bytes;
+  t->mover_stop = false;
+  try {
+    t->mover = std::thread(mover_main, t);
+  } catch (...) {
+    return fail(PW_ENOMEM, "pw_mover_start: could not start the thread");
+  }
+  return PW_OK;
+}
+
+int pw_mover_submit(pw_table* t, int n, const int* layer, const int* expert, const int* kind,
+                    const int* q_target) {
+  if (!t) return fail(PW_EINVAL, "pw_mover_submit: null table");
+  if (n < 0 || (n > 0 && (!layer || !expert || !kind || !q_target)))
+    return fail(PW_EINVAL, "pw_mover_submit: bad count or null array");
+  {
+    std::lock_guard<std::mutex> lk(t->mu);   // checked up front: all or nothing
+    for (int i = 0; i < n; ++i) {
+      const BlockState* b = block_of(t, layer[i], expert[i], kind[i]);
+      if (!b || !b->registered)
+        return fail(PW_EINVAL, "pw_mover_submit: entry %d: block not registered", i);
+      if (q_target[i] < b->b_min || q_target[i] > b->n_bits)
+        return fail(PW_EINVAL, "pw_mover_submit: entry %d: q %d outside [%d, %d]", i, q_target[i],
+                    b->b_min, b->n_bits);
+      for (int p = 0; p < q_target[i]; ++p)
+        if (!b->pages[p])
+          return fail(PW_EINVAL, "pw_mover_submit: entry %d: no device page for plane %d", i, p);
+    }
+  }
+  {
+    std::lock_guard<std::mutex> lk(t->mover_mu);
+    if (!t->mover.joinable()) return fail(PW_EINVAL, "pw_mover_submit: the mover is not running");
+    for (int i = 0; i < n; ++i) t->requests.push_back({layer[i], expert[i], kind[i], q_target[i]});
+  }
+  t->mover_cv.notify_all();
+  return PW_OK;
+}
+
+int pw_commit_arrived(pw_table* t, pw_stream_t compute, int* n_committed, int* n_outstanding) {
+  if (n_committed) *n_committed = 0;
+  if (n_outstanding) *n_outstanding = 0;
+  if (!t) return fail(PW_EINVAL, "pw_commit_arrived: null table");
+  int rc = PW_OK;
+  std::vector<std::pair<size_t, int>> list;
+  size_t left = 0;
+  {
+    std::lock_guard<std::mutex> lk(t->mu);
+    while (!t->arrivals.empty()) {
+      BlockState& b = t->blocks[t->arrivals.front()];
+      if (b.pending) {
+        if (b.failed) {
+          rc = fail(PW_ERELOAD, "pw_commit_arrived: a reload failed; its block keeps q %d", b.q);
+          b.commit_to = 0;
+          t->arrivals.pop_front();
+          continue;
+        }
+        if (!b.issued) break;
+        const cudaError_t e = cudaEventQuery(b.ev);
+        if (e == cudaErrorNotReady) break;   // copies on one stream land in issue order
+        if (e != cudaSuccess) {
+          rc = cuda_fail(e, "pw_commit_arrived: event query");
+          break;
+        }
+        b.resident = b.pending;
+        b.pending = 0;
+      }
+      if (b.commit_to && b.commit_to <= b.resident) list.push_back({t->arrivals.front(), b.commit_to});
+      b.commit_to = 0;
+      t->arrivals.pop_front();
+    }
+    if (!list.empty()) {
+      const int c = commit_descs(t, list, reinterpret_cast<cudaStream_t>(compute));
+      if (c != PW_OK) return c;
+    }
+    left = t->arrivals.size();
+  }
+  {
+    std::lock_guard<std::mutex> lk(t->mover_mu);
+    left += t->requests.size() + static_cast<size_t>(t->mover_busy);
+    if (rc == PW_OK && t->mover_error != PW_OK) {
+      rc = fail(t->mover_error, "pw_commit_arrived: mover: %s", t->mover_error_msg.c_str());
+      t->mover_error = PW_OK;
+      t->mover_error_msg.clear();
+    }
+  }
+  if (n_committed) *n_committed = static_cast<int>(list.size());
+  if (n_outstanding) *n_outstanding = static_cast<int>(left);
+  return rc;
 }
 
 int pw_block_state(pw_table* t, int layer, int expert, int kind, int* q, int* resident,
@@ -430,6 +803,7 @@ int pw_debug_fail_next_reload(pw_table* t) {
 
 int pw_table_destroy(pw_table* t) {
   if (!t) return PW_OK;
+  mover_stop(t);
   for (auto& b : t->blocks)
     if (b.ev) {
       cudaEventSynchronize(b.ev);

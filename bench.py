@@ -46,6 +46,9 @@ def parse():
                     help="distinct layer instances cycled (default 8 for decode, 1 for prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--reload-at", type=int, default=100, help="stack workload: step of the mid-run reload")
+    ap.add_argument("--reload-inflight-mb", type=int, default=64,
+                    help="stack workload: bound on the mover's copies in flight")
     return ap.parse_args()
 
 
@@ -406,6 +409,138 @@ def run_ours(args, cfg, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def run_stack(args, cfg, rank, world, local):
+    """24-layer Qwen-shaped stack, decode batch 4: bits fitted to 40% of the fp16
+    bytes; at step --reload-at a seeded 25% of the blocks below 8 bits start an
+    asynchronous host->device reload of two more planes on a side stream, and
+    each is committed (stream ordered) at the first step boundary after its copy
+    completed.  Reports tokens/s before, during and after the reload window."""
+    import numpy as np
+    import torch
+    import any_precision_weight_gb300 as pw
+    from any_precision_weight_gb300.model import HostStore, load_expert_layer
+    import synth
+
+    dev = torch.device("cuda", local)
+    L = cfg.n_layers
+    bits = synth.stack_bits(cfg)
+    plan = synth.reload_plan(cfg, bits)
+    target = {(l, e, k): qn for (l, e, k, qo, qn) in plan}
+    m = pw.PagedMoE(L, cfg.E, cfg.H, cfg.I, device=dev)
+    store = HostStore()
+    for l in range(L):
+        src = lambda e, k, l=l: (synth.parent_indices(cfg, l, e, k), synth.parent_lut(cfg, l, e, k))
+        load_expert_layer(m, l, src, bits[l], store=store,
+                          alloc_planes=lambda e, k, l=l: target.get((l, e, k), int(bits[l, e, k])))
+    Lg = [torch.from_numpy(synth.logits(cfg, l)).to(dev) for l in range(L)]
+    X0 = [torch.from_numpy(synth.tokens(cfg, step=i)).to(dev) for i in range(8)]
+    bufs = [torch.empty((cfg.T, cfg.H), dtype=torch.float16, device=dev) for _ in range(2)]
+    ws = m.workspace(cfg.T, cfg.top_k)
+    stream = torch.cuda.current_stream()
+    copy = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        x = X0[i % len(X0)]
+        for l in range(L):
+            o = bufs[l & 1]
+            m.pw_moe_forward(l, x, Lg[l], cfg.top_k, cfg.renorm, residual=x, out=o, ws=ws)
+            x = o
+
+    # routing depends only on each layer's fixed logits: weight bytes per step
+    bits_after = bits.copy()
+    for (l, e, kind, qo, qn) in plan:
+        bits_after[l, e, kind] = qn
+    step_bytes = [0, 0]
+    for l in range(L):
+        _, _, _, off, _ = m.pw_moe_forward(l, X0[0], Lg[l], cfg.top_k, cfg.renorm, ws=ws, routing=True)
+        counts = np.diff(off.cpu().numpy())
+        step_bytes[0] += algorithmic_bytes(cfg, bits[l], counts)["layer"]
+        step_bytes[1] += algorithmic_bytes(cfg, bits_after[l], counts)["layer"]
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    n = args.steps
+    reload_at = min(args.reload_at, n - 1)
+    clocks = Clocks(local)
+    clocks.start()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    for e_ in ev + [c0, c1]:          # torch creates the CUDA event at its first record
+        e_.record(stream)
+    torch.cuda.synchronize()
+    reload_bytes = 0
+    for (l, e, kind, qo, qn) in plan:
+        R, K = m.rows_cols(kind)
+        reload_bytes += (qn - qo) * R * K // 8 + R * 2 * sum(1 << b for b in range(qo + 1, qn + 1))
+    items = [(l, e, kind, qn) for (l, e, kind, qo, qn) in plan]
+    m.pw_mover_start(copy, max_inflight_bytes=args.reload_inflight_mb << 20)
+    committed = 0
+    commit_launches = 0
+    last = reload_at
+    landed = False
+    w0 = time.perf_counter()
+    ev[0].record(stream)
+    for i in range(n):
+        if i >= 2:
+            ev[i - 1].synchronize()      # at most two steps in flight, as a decode loop that
+                                         # needs step i-2's tokens before launching step i
+        if i == reload_at:
+            c0.record(copy)
+            m.pw_mover_submit(items)
+        if i >= reload_at and committed < len(items):
+            c, left = m.pw_commit_arrived()
+            if c:
+                committed += c
+                commit_launches += -(-c // 192)
+                last = i
+            if left == 0:
+                c1.record(stream)        # the boundary at which the last block was committed
+                landed = True
+        step(args.warmup + i)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - w0
+    clk = clocks.stop()
+    t = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(n)])
+    copy_ms = c0.elapsed_time(c1) if landed else None
+    before = t[:reload_at]
+    during = t[reload_at:last + 1]
+    after = t[last + 1:]
+    tps = lambda a: float(cfg.T / (a.mean() / 1e3)) if len(a) else None
+    ms_total = float(t.sum())
+    ms_max = max_over_ranks(ms_total, world)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": world * cfg.T * n / (ms_max / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": n, "warmup": args.warmup, "ms_per_step": ms_max / n, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": cfg.name, "layers": L, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I,
+                   "top_k": cfg.top_k, "bits": "greedy fit to 40% of fp16 bytes",
+                   "device_weight_bytes": m.device_bytes(), "host_store_bytes": store.nbytes(),
+                   "l2": "24 layers of weights (about 10 GB) between reuses, larger than L2"},
+        "stack": {"tokens_per_s_before": tps(before), "tokens_per_s_during": tps(during),
+                  "tokens_per_s_after": tps(after),
+                  "loss_pct_during": (1 - tps(during) / tps(before)) * 100 if len(during) and len(before) else None,
+                  "reload_at_step": reload_at, "last_commit_step": last, "reloaded_blocks": len(plan),
+                  "reload_bytes": reload_bytes, "committed": committed, "submit_to_last_commit_ms": copy_ms,
+                  "mover": f"native mover thread, at most {args.reload_inflight_mb} MiB of copies in flight",
+                  "reload_gbs": reload_bytes / (copy_ms / 1e3) / 1e9 if copy_ms else None},
+        "roofline": {"bound": "hbm", "kernel": "layer_fused (whole step)",
+                     "achieved": step_bytes[0] / (before.mean() / 1e3) / 1e9 if len(before) else None,
+                     "peak": hbm_peak()[0], "unit": "GB/s", "peak_kind": hbm_peak()[1], "traffic": None,
+                     "bytes_per_step_before": step_bytes[0], "bytes_per_step_after": step_bytes[1],
+                     "achieved_after": step_bytes[1] / (after.mean() / 1e3) / 1e9 if len(after) else None},
+        "gpu_launches": n * L + commit_launches, "clocks": clk, "wall_s": wall,
+    }
+    r = line["roofline"]
+    if r["achieved"] is not None:
+        r["frac"] = r["achieved"] / r["peak"]
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     import synth
@@ -415,7 +550,10 @@ def main():
         run_reference(args, cfg, rank, int(os.environ.get("WORLD_SIZE", "1")))
         return
     rank, world, local = dist_init(args.gpus)
-    run_ours(args, cfg, rank, world, local)
+    if cfg.n_layers > 1:
+        run_stack(args, cfg, rank, world, local)
+    else:
+        run_ours(args, cfg, rank, world, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

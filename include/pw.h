@@ -155,6 +155,27 @@ int pw_reload_async(pw_table* t, int layer, int expert, int kind, int q_target,
                     pw_stream_t copy);
 
 /*
+ * pw_reload_many -- pw_reload_async for n blocks in one call: block i is
+ * (layer[i], expert[i], kind[i]) raised to q_target[i]; the four arrays are host
+ * memory of n ints, read only during the call.  The table's lock is taken per
+ * block, so another host thread may query and commit blocks while this call is
+ * still enqueueing later ones.  Stops at the first block that fails, returning
+ * its error code; *n_done (if not null) is the number of blocks enqueued
+ * before it (n on success).  A runtime addition for planners that raise many
+ * blocks at once; the pages describe per-block movement only.
+ *
+ * Threads: the table calls may be made from several host threads.  A reload
+ * holds the table lock only while it checks and claims the block and when it
+ * publishes the outcome, never while its copies are enqueued, so a planner
+ * thread can run this while the decode thread launches forward passes,
+ * queries and commits.  A block being enqueued reads as in flight
+ * (pw_reload_query returns 0); a commit that needs it waits on the host until
+ * its enqueue has finished.
+ */
+int pw_reload_many(pw_table* t, int n, const int* layer, const int* expert, const int* kind,
+                   const int* q_target, pw_stream_t copy, int* n_done);
+
+/*
  * pw_reload_query -- non-blocking completion check of a block's pending reload.
  * Returns 1 when the reload has completed (or none is pending), 0 while it is
  * in flight, PW_ERELOAD if it failed.
@@ -173,6 +194,63 @@ int pw_reload_query(pw_table* t, int layer, int expert, int kind);
  * unchanged), PW_ECUDA.
  */
 int pw_set_commit(pw_table* t, int layer, int expert, int kind, int q, pw_stream_t compute);
+
+/*
+ * pw_set_commit_many -- pw_set_commit for n blocks at one stream-ordered
+ * boundary: block i is (layer[i], expert[i], kind[i]) committed at q[i]; host
+ * arrays of n ints.  Every entry is checked before anything is enqueued, so on
+ * PW_EINVAL / PW_ENOTRESIDENT / PW_ERELOAD no block changes.  The compute
+ * stream waits on each raised block's reload event, then the descriptors are
+ * written by one small kernel per 192 blocks instead of one per block.  If a
+ * block appears twice, its last entry is the one that holds.  Errors as for
+ * pw_set_commit.
+ */
+int pw_set_commit_many(pw_table* t, int n, const int* layer, const int* expert, const int* kind,
+                       const int* q, pw_stream_t compute);
+
+/*
+ * The reload mover: a host thread owned by the table that carries out
+ * submitted reloads in submission order on one copy stream, and a call the
+ * decode loop makes at each step boundary to commit whatever has landed.
+ * This is the asynchronous page movement of the pages ("Asynchronous Page
+ * Movement": planes move while inference continues; a bitwidth is committed
+ * only at a safe boundary) with the policy of when to enqueue moved into
+ * native code: the decode thread makes one call per step instead of one per
+ * block, and never blocks behind a full copy queue.
+ *
+ * pw_mover_start -- starts the mover on `copy` (a stream of the current
+ * device).  It keeps at most max_inflight_bytes of reload copies enqueued and
+ * not yet finished, so that its enqueues never block in the driver while other
+ * threads launch.  Errors: PW_EINVAL (already running, zero limit), PW_ECUDA,
+ * PW_ENOMEM (no thread).  pw_table_destroy stops it (requests not yet taken
+ * are dropped; copies in flight are waited for).
+ */
+int pw_mover_start(pw_table* t, pw_stream_t copy, size_t max_inflight_bytes);
+
+/*
+ * pw_mover_submit -- queues reloads of n blocks (host arrays of n ints) to
+ * q_target[i]; each block is committed at q_target[i] by the first
+ * pw_commit_arrived after its copies have finished (a target at or below the
+ * resident planes needs no copy and is committed at the next call).  All
+ * entries are checked before any is queued.  Errors: PW_EINVAL (block not
+ * registered, q outside [b_min, n_bits], a plane below q_target without a
+ * device page, mover not running).  A failure later, in the mover, is
+ * reported by the next pw_commit_arrived.
+ */
+int pw_mover_submit(pw_table* t, int n, const int* layer, const int* expert, const int* kind,
+                    const int* q_target);
+
+/*
+ * pw_commit_arrived -- at a step boundary: commits, on the compute stream and
+ * in one small launch per 192 blocks, every mover-submitted block whose copies
+ * have finished (checked without waiting, in submission order, stopping at
+ * the first that has not).  *n_committed = blocks committed by this call;
+ * *n_outstanding = submitted blocks not yet committed (queued, being
+ * enqueued, or in flight); either pointer may be null.  Errors: PW_ERELOAD
+ * (a block's reload failed: it keeps its q; the others are still committed),
+ * an error the mover met since the last call, PW_ECUDA.
+ */
+int pw_commit_arrived(pw_table* t, pw_stream_t compute, int* n_committed, int* n_outstanding);
 
 /* Host view of one block: committed q, resident planes, pending reload target (0 if none). */
 int pw_block_state(pw_table* t, int layer, int expert, int kind, int* q, int* resident,

@@ -134,3 +134,210 @@ def test_failed_reload_refuses_commit_and_keeps_q():
     m.pw_reload_async(0, 2, 0, 6)
     m.pw_set_commit(0, 2, 0, 6)
     assert m.pw_block_state(0, 2, 0) == (6, 6, 0)
+
+
+def test_small_stack_recommit_midrun_matches_oracle_per_layer():
+    """Three stacked layers with the residual fused into the combine; some blocks
+    are reloaded on a side stream and re-committed between two passes.  Every
+    layer's output is checked against the oracle on the GPU's own input to that
+    layer, before (old bits) and after (new bits)."""
+    import torch
+    cfg = synth.CONFIGS["tiny"].with_(T=4, n_layers=3)
+    L = 3
+    bits = {l: synth.block_bits(cfg, l) for l in range(L)}
+    raised = {l: bits[l].copy() for l in range(L)}
+    plan = []
+    for l in range(L):
+        for e in range(cfg.E):
+            for k in range(2):
+                if (e + k + l) % 3 == 0 and bits[l][e, k] < 8:
+                    raised[l][e, k] = min(8, bits[l][e, k] + 2)
+                    plan.append((l, e, k, int(raised[l][e, k])))
+    m = gpu_layer(cfg, n_layers=L, bits=bits)
+    Ls = [synth.logits(cfg, l) for l in range(L)]
+    x0 = synth.tokens(cfg)
+
+    def run():
+        xs = [x0]
+        x = torch.from_numpy(x0).cuda()
+        for l in range(L):
+            out = m.pw_moe_forward(l, x, torch.from_numpy(Ls[l]).cuda(), cfg.top_k, cfg.renorm, residual=x)
+            xs.append(to_np(out))
+            x = out
+        torch.cuda.synchronize()
+        return xs
+
+    def check(xs, bb):
+        for l in range(L):
+            ref = omoe.layer(xs[l], Ls[l], cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, l), bb[l]),
+                             residual=xs[l])
+            assert_close(xs[l + 1], ref["out"])
+
+    check(run(), bits)
+    copy = torch.cuda.Stream()
+    for (l, e, k, q) in plan:
+        m.pw_reload_async(l, e, k, q, stream=copy)
+    for (l, e, k, q) in plan:
+        m.pw_set_commit(l, e, k, q)      # waits on the reload's event on the compute stream
+    check(run(), raised)
+
+
+def test_batched_reload_and_commit_match_per_block_calls():
+    """pw_reload_many + pw_set_commit_many leave the same pages, descriptors and
+    outputs as the per-block calls; a batch with one bad entry commits nothing."""
+    import torch
+    import any_precision_weight_gb300 as pw
+    cfg = synth.CONFIGS["tiny"]
+    lo = np.full((cfg.E, 2), 3, dtype=np.int32)
+    lo[:, 1] = 5
+    items = [(0, e, k, 8 if k == 0 else 7) for e in range(cfg.E) for k in range(2) if e % 2 == 0]
+    a = gpu_layer(cfg, bits={0: lo})
+    b = gpu_layer(cfg, bits={0: lo})
+    x = torch.from_numpy(synth.tokens(cfg)).cuda()
+    L = torch.from_numpy(synth.logits(cfg)).cuda()
+    copy = torch.cuda.Stream()
+    for (l, e, k, q) in items:
+        a.pw_reload_async(l, e, k, q, stream=copy)
+        a.pw_set_commit(l, e, k, q)
+    assert b.pw_reload_many(items, stream=copy) == len(items)
+    bad = items[:3] + [(0, 1, 0, 8)]            # expert 1 was not reloaded
+    with pytest.raises(pw.PWError) as err:
+        b.pw_set_commit_many(bad)
+    assert err.value.code == pw.PW_ENOTRESIDENT
+    for (l, e, k, q) in items:
+        assert b.pw_block_state(l, e, k)[0] == lo[e, k]
+    b.pw_set_commit_many(items)
+    for e in range(cfg.E):
+        for k in range(2):
+            assert a.pw_block_state(0, e, k)[:2] == b.pw_block_state(0, e, k)[:2]
+    assert np.array_equal(_fwd(a, cfg, x, L).view(np.uint16), _fwd(b, cfg, x, L).view(np.uint16))
+    hi = lo.copy()
+    for (l, e, k, q) in items:
+        hi[e, k] = q
+    ref = omoe.layer(to_np(x), to_np(L), cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), hi))
+    assert_close(_fwd(b, cfg, x, L), ref["out"])
+
+
+def test_commit_many_spans_several_launches():
+    """More blocks than one descriptor-batch launch carries (192)."""
+    import torch
+    cfg = synth.CONFIGS["tiny"]
+    L_ = 30
+    bits = {l: np.full((cfg.E, 2), 4, dtype=np.int32) for l in range(L_)}
+    m = gpu_layer(cfg, n_layers=L_, bits=bits)
+    items = [(l, e, k, 3 + (l + e + k) % 2) for l in range(L_) for e in range(cfg.E) for k in range(2)]
+    assert len(items) > 192
+    m.pw_set_commit_many(items)
+    torch.cuda.synchronize()
+    x = torch.from_numpy(synth.tokens(cfg)).cuda()
+    for l in (0, 17, 29):
+        Lg = torch.from_numpy(synth.logits(cfg, l)).cuda()
+        got = to_np(m.pw_moe_forward(l, x, Lg, cfg.top_k, cfg.renorm))
+        want_bits = np.array([[3 + (l + e + k) % 2 for k in range(2)] for e in range(cfg.E)], dtype=np.int32)
+        ref = omoe.layer(to_np(x), to_np(Lg), cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, l), want_bits))
+        assert_close(got, ref["out"])
+        for e in range(cfg.E):
+            for k in range(2):
+                assert m.pw_block_state(l, e, k)[0] == want_bits[e, k]
+
+
+def test_planner_thread_reloads_while_decode_thread_commits():
+    """A second host thread enqueues reloads (pw_reload_many, chunk by chunk)
+    while this thread runs forward passes, polls and commits whatever has
+    landed; afterwards every block is at its raised bitwidth and the layer
+    matches the oracle there."""
+    import threading
+    import torch
+    cfg = synth.CONFIGS["tiny"]
+    L_ = 6
+    bits = {l: np.full((cfg.E, 2), 3, dtype=np.int32) for l in range(L_)}
+    m = gpu_layer(cfg, n_layers=L_, bits=bits)
+    items = [(l, e, k, 5 + (e + k) % 4) for l in range(L_) for e in range(cfg.E) for k in range(2)]
+    issued, errors = [], []
+    copy = torch.cuda.Stream()
+
+    def planner():
+        try:
+            for j in range(0, len(items), 7):
+                m.pw_reload_many(items[j:j + 7], stream=copy)
+                issued.extend(items[j:j + 7])
+        except Exception as ex:
+            errors.append(ex)
+
+    x = torch.from_numpy(synth.tokens(cfg)).cuda()
+    Ls = [torch.from_numpy(synth.logits(cfg, l)).cuda() for l in range(L_)]
+    th = threading.Thread(target=planner)
+    th.start()
+    done = 0
+    for it in range(100000):
+        for l in range(L_):
+            m.pw_moe_forward(l, x, Ls[l], cfg.top_k, cfg.renorm)
+        j = done
+        while j < len(issued) and m.pw_reload_query(*items[j][:3]) == 1:
+            j += 1
+        if j > done:
+            m.pw_set_commit_many(items[done:j])
+            done = j
+        if done == len(items):
+            break
+    th.join()
+    assert not errors
+    assert done == len(items)
+    torch.cuda.synchronize()
+    for l in range(L_):
+        want = np.array([[5 + (e + k) % 4 for k in range(2)] for e in range(cfg.E)], dtype=np.int32)
+        got = to_np(m.pw_moe_forward(l, x, Ls[l], cfg.top_k, cfg.renorm))
+        ref = omoe.layer(to_np(x), to_np(Ls[l]), cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, l), want))
+        assert_close(got, ref["out"])
+
+
+def test_mover_commits_landed_reloads_at_step_boundaries():
+    """The native mover carries out submitted reloads with a small in-flight
+    bound while forward passes run; pw_commit_arrived commits what has landed.
+    Before the first commit the outputs are those of the old bits; at the end
+    every block is at its target and each layer matches the oracle there."""
+    import torch
+    import any_precision_weight_gb300 as pw
+    cfg = synth.CONFIGS["tiny"]
+    L_ = 6
+    bits = {l: np.full((cfg.E, 2), 3, dtype=np.int32) for l in range(L_)}
+    m = gpu_layer(cfg, n_layers=L_, bits=bits)
+    x = torch.from_numpy(synth.tokens(cfg)).cuda()
+    Ls = [torch.from_numpy(synth.logits(cfg, l)).cuda() for l in range(L_)]
+    before = [to_np(m.pw_moe_forward(l, x, Ls[l], cfg.top_k, cfg.renorm)) for l in range(L_)]
+    last = (L_ - 1, cfg.E - 1, 1)
+    items = [(l, e, k, 5 + (e + k) % 4) for l in range(L_) for e in range(cfg.E) for k in range(2)
+             if (l, e, k) != last]
+    items.append(last + (3,))                     # at the resident planes: committed without a copy
+    with pytest.raises(pw.PWError):
+        m.pw_mover_submit(items)                  # not started
+    copy = torch.cuda.Stream()
+    m.pw_mover_start(copy, max_inflight_bytes=256 << 10)
+    with pytest.raises(pw.PWError) as err:
+        m.pw_mover_submit([(0, 0, 0, 9)])         # q out of range: nothing queued
+    assert err.value.code == pw.PW_EINVAL
+    m.pw_mover_submit(items[:-1])
+    m.pw_mover_submit(items[-1:])
+    total, outstanding = 0, len(items)
+    for it in range(200000):
+        for l in range(L_):
+            m.pw_moe_forward(l, x, Ls[l], cfg.top_k, cfg.renorm)
+        c, outstanding = m.pw_commit_arrived()
+        total += c
+        if outstanding == 0:
+            break
+    assert outstanding == 0 and total == len(items)
+    torch.cuda.synchronize()
+    for l in range(L_):
+        want = np.array([[5 + (e + k) % 4 for k in range(2)] for e in range(cfg.E)], dtype=np.int32)
+        if l == last[0]:
+            want[last[1], last[2]] = 3
+        for e in range(cfg.E):
+            for k in range(2):
+                assert m.pw_block_state(l, e, k)[:2] == (want[e, k], want[e, k])
+        got = to_np(m.pw_moe_forward(l, x, Ls[l], cfg.top_k, cfg.renorm))
+        ref = omoe.layer(to_np(x), to_np(Ls[l]), cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, l), want))
+        assert_close(got, ref["out"])
+        assert not np.array_equal(got, before[l])
+    with pytest.raises(pw.PWError):
+        m.pw_mover_start(copy)                    # already running
