@@ -53,6 +53,11 @@ constexpr int kPieceRed = 0;                                // kKW * kTok pieces
 constexpr int kPieceXw = kPieceRed + kKW * kTok;            // 2 per (warp, token)
 constexpr int kSmemBytes = kLutBytes + 2 * kPlaneStageBytes + 2 * kXStageBytes + route_smem_bytes() + 64;
 
+// The kernel's dynamic shared memory.  Table reads index this symbol directly,
+// so its (link-time constant) shared address folds into the load's immediate
+// offset instead of costing an add per looked-up weight.
+extern __shared__ __align__(128) unsigned char g_smem[];
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -154,7 +159,7 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
   const int row = lane;
   const uint32_t laneoff = static_cast<uint32_t>(row) * 4u;
   const int rsw = (((kw >> 1) ^ ((row >> 1) & 3)) * 4) + (kw & 1) * 2;
-  const unsigned char* lut_bytes = reinterpret_cast<const unsigned char*>(lut_s);
+  const unsigned char* lut_bytes = g_smem;   // lut_s == g_smem
 
   for (int t0 = 0; t0 < it.n; t0 += kTok) {
     const int nt = min(kTok, it.n - t0);
@@ -245,24 +250,25 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
 #pragma unroll
             for (int r = 0; r < 8; ++r) o[r] = wi == 0 ? pv[r].x : pv[r].y;
             planes_to_indices(o);
-            float wv[32];
+            // eight weights at a time (byte lane bb of the transposed words),
+            // each multiplied into every token of the pass before the next eight
 #pragma unroll
-            for (int bb = 0; bb < 4; ++bb)
+            for (int bb = 0; bb < 4; ++bb) {
+              float w8[8];
 #pragma unroll
               for (int r = 0; r < 8; ++r) {
                 const uint32_t a = prmt(o[r], laneoff, 0x5504u | (static_cast<uint32_t>(bb) << 4));
-                wv[8 * bb + r] = *reinterpret_cast<const float*>(lut_bytes + a);
+                w8[r] = *reinterpret_cast<const float*>(lut_bytes + a);
               }
 #pragma unroll
-            for (int t = 0; t < kTok; ++t) {
-              if (t < nt) {
-                const float4* xr = reinterpret_cast<const float4*>(piece(smem, kPieceXw + 2 * (kw * kTok + t) + wi));
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                  const float4 xv = xr[j4];
-                  const int m0 = (2 * j4) & 3, m1 = (2 * j4 + 1) & 3;
-                  acc[t][m0] = __ffma2_rn(make_float2(wv[4 * j4], wv[4 * j4 + 1]), make_float2(xv.x, xv.y), acc[t][m0]);
-                  acc[t][m1] = __ffma2_rn(make_float2(wv[4 * j4 + 2], wv[4 * j4 + 3]), make_float2(xv.z, xv.w), acc[t][m1]);
+              for (int t = 0; t < kTok; ++t) {
+                if (t < nt) {
+                  const float4* xr = reinterpret_cast<const float4*>(piece(smem, kPieceXw + 2 * (kw * kTok + t) + wi));
+                  const float4 x0 = xr[2 * bb], x1 = xr[2 * bb + 1];
+                  acc[t][0] = __ffma2_rn(make_float2(w8[0], w8[1]), make_float2(x0.x, x0.y), acc[t][0]);
+                  acc[t][1] = __ffma2_rn(make_float2(w8[2], w8[3]), make_float2(x0.z, x0.w), acc[t][1]);
+                  acc[t][2] = __ffma2_rn(make_float2(w8[4], w8[5]), make_float2(x1.x, x1.y), acc[t][2]);
+                  acc[t][3] = __ffma2_rn(make_float2(w8[6], w8[7]), make_float2(x1.z, x1.w), acc[t][3]);
                 }
               }
             }
@@ -339,7 +345,7 @@ __device__ bool wait_eq(const int* ptr, int want) {
 // 32-row tile of H (over all active experts) combines that tile's output rows.
 // Every wait is bounded and reports PW_STATUS_TIMEOUT instead of hanging.
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
-  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* smem = g_smem;
   int* s_int = reinterpret_cast<int*>(smem + kSmemBytes - 64);
   int* rs = reinterpret_cast<int*>(smem + kLutBytes + 2 * kPlaneStageBytes + 2 * kXStageBytes);
   RouteSmem r;
