@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--instances", type=int, default=0,
                     help="distinct layer instances cycled (default 8 for decode, 1 for prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--uniform-bits", action="store_true",
+                    help="every block at the byte-weighted mean bitwidth (mixed vs uniform check)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reload-at", type=int, default=100, help="stack workload: step of the mid-run reload")
     ap.add_argument("--reload-inflight-mb", type=int, default=64,
@@ -172,7 +174,22 @@ def hbm_peak():
 
 # ----------------------------------------------------------------------------- workload
 
-def build_model(cfg, n_inst, device):
+def uniform_bits(cfg, n_inst):
+    """The byte-weighted mean committed bitwidth over the instances' blocks, rounded."""
+    import numpy as np
+    import synth
+    num = den = 0.0
+    for l in range(n_inst):
+        b = synth.block_bits(cfg, l)
+        for kind in (0, 1):
+            w = cfg.rows(kind) * cfg.cols(kind)
+            num += float(b[:, kind].sum()) * w
+            den += b.shape[0] * w
+    return int(np.floor(num / den + 0.5))
+
+
+def build_model(cfg, n_inst, device, uniform=None):
+    import numpy as np
     import any_precision_weight_gb300 as pw
     from any_precision_weight_gb300.model import load_expert_layer
     import synth
@@ -180,6 +197,8 @@ def build_model(cfg, n_inst, device):
     bits = {}
     for l in range(n_inst):
         bits[l] = synth.block_bits(cfg, l)
+        if uniform is not None:
+            bits[l] = np.full_like(bits[l], uniform)
         src = lambda e, k, l=l: (synth.parent_indices(cfg, l, e, k), synth.parent_lut(cfg, l, e, k))
         load_expert_layer(m, l, src, bits[l])
     return m, bits
@@ -281,7 +300,8 @@ def run_ours(args, cfg, rank, world, local):
 
     dev = torch.device("cuda", local)
     n_inst = args.instances or (8 if cfg.T <= 64 else 1)
-    m, bits = build_model(cfg, n_inst, dev)
+    uq = uniform_bits(cfg, n_inst) if args.uniform_bits else None
+    m, bits = build_model(cfg, n_inst, dev, uniform=uq)
     X = [torch.from_numpy(synth.tokens(cfg, step=l)).to(dev) for l in range(n_inst)]
     Lg = [torch.from_numpy(synth.logits(cfg, l)).to(dev) for l in range(n_inst)]
     out = torch.empty((cfg.T, cfg.H), dtype=torch.float16, device=dev)
@@ -391,7 +411,8 @@ def run_ours(args, cfg, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I,
-                   "top_k": cfg.top_k, "renorm": cfg.renorm, "bits": "per block in {3..8}, hot experts >= 6",
+                   "top_k": cfg.top_k, "renorm": cfg.renorm, "bits": (f"uniform q={uq} (byte-weighted mean of the mixed assignment)" if uq is not None
+                            else "per block in {3..8}, hot experts >= 6"),
                    "accumulate": "f32", "parallelism": f"replicas x{world}",
                    "l2": f"{n_inst} distinct layer instances cycled; inputs larger than L2 between reuses",
                    "layer_weight_bytes_per_step": layer_bytes, "layer_gbs": layer_gbs,
