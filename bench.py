@@ -77,11 +77,13 @@ def barrier(world):
 
 
 def max_over_ranks(v, world):
+    """The maximum of v over all ranks (a host value: one small all-reduce)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -262,6 +264,20 @@ def oracle_rate(cfg, layer, seconds, sample_pairs=None):
     return toks / dt, reps, dt
 
 
+def oracle_rate_one_thread(cfg, seconds):
+    """oracle_rate in a child process whose BLAS and OpenMP pools have one thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json, sys; sys.path.insert(0, %r); import bench, synth; "
+            "print(json.dumps(bench.oracle_rate(synth.CONFIGS[%r], 0, %r)))" % (ROOT, cfg.name, seconds))
+    try:
+        out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                             timeout=seconds * 4 + 120)
+        rate, reps, dt = json.loads(out.stdout.strip().splitlines()[-1])
+        return rate
+    except Exception:
+        return None
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -401,6 +417,7 @@ def run_ours(args, cfg, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, reps, dt = oracle_rate(cfg, 0, args.cpu_seconds)
         cpu = {"value": rate, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+               "value_1_thread": oracle_rate_one_thread(cfg, min(10.0, args.cpu_seconds)),
                "sample": f"{reps} full layer forwards (batch {cfg.T}) of layer instance 0 in {dt:.1f} s, "
                          "fp64 numpy (BLAS matmuls threaded, gathers single-threaded)"}
 
