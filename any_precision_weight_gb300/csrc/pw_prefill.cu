@@ -12,7 +12,8 @@
 //  * the expert's token rows (gathered into expert order, fp16) arrive by TMA in
 //    128 x 64 boxes with the 128-byte swizzle;
 //  * bit-planes arrive by coalesced cp.async, two K steps (16 bytes per row and
-//    plane) at a time, double buffered;
+//    plane) at a time, double buffered; each K step reads its q words per row
+//    straight from the staged chunk;
 //  * all 8 warps dequantise the 128 weight rows x 64 k of the same K step
 //    straight into the K-major 128-byte-swizzled layout the MMA reads (SWAR bit
 //    transpose of the plane words, byte-permute table addressing, fp16 table in
@@ -302,43 +303,28 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
     asm volatile("cp.async.wait_group 1;" ::: "memory");
     __syncthreads();
 
-    uint4 pw4[PW_MAX_BITS];
     for (int ks = 0; ks < nksteps; ++ks, ++g) {
       const int s = g & 1;
       const uint32_t use = g >> 1;
-      if ((ks & 1) == 0) {   // a new plane chunk: its 4 words per plane into registers
-        const unsigned char* src = smem + kOffPl + ((ks >> 1) & 1) * kPlaneChunkBytes + row * 16;
-#pragma unroll
-        for (int pl = 0; pl < PW_MAX_BITS; ++pl)
-          pw4[pl] = (pl < Q) ? *reinterpret_cast<const uint4*>(src + pl * kBM * 16) : make_uint4(0, 0, 0, 0);
-      }
       // dequantise 32 weights of this row into the swizzled B tile
       {
+        // the row's plane words of this K step and half: word (ks & 1) * 2 + half of
+        // the staged 16-byte chunk, plane q-1-r into o[r]
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(
+            smem + kOffPl + ((ks >> 1) & 1) * kPlaneChunkBytes + row * 16) + (ks & 1) * 2 + half;
         uint32_t o[8];
-        const int wsel = (ks & 1) * 2 + half;
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          uint32_t w = 0;
-#pragma unroll
-          for (int pl = 0; pl < PW_MAX_BITS; ++pl)
-            if (pl == Q - 1 - r) {
-              const uint4 v = pw4[pl];
-              w = wsel == 0 ? v.x : wsel == 1 ? v.y : wsel == 2 ? v.z : v.w;
-            }
-          o[r] = (r < Q) ? w : 0u;
-        }
+        for (int r = 0; r < 8; ++r) o[r] = (r < Q) ? src[(Q - 1 - r) * (kBM * 4)] : 0u;
         transpose8(o);
-        const uint32_t lut_base = saddr(lut_s);
+        const unsigned char* lutb = reinterpret_cast<const unsigned char*>(lut_s);
         unsigned char* tileB = smem + kOffB + s * kTileBytes + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
         for (int bb = 0; bb < 4; ++bb) {
           uint32_t hv[8];
 #pragma unroll
           for (int r = 0; r < 8; ++r) {
-            const uint32_t a = lut_base + prmt_p(o[r], rowoff, 0x5504u | (static_cast<uint32_t>(bb) << 4));
-            uint16_t v16;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v16) : "r"(a));
-            hv[r] = v16;
+            const uint32_t a = prmt_p(o[r], rowoff, 0x5504u | (static_cast<uint32_t>(bb) << 4));
+            hv[r] = *reinterpret_cast<const uint16_t*>(lutb + a);
           }
           uint4 pk;
           pk.x = hv[0] | (hv[1] << 16);
@@ -353,7 +339,7 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
       tc_fence_before();
       __syncthreads();      // B(ks) complete; every thread is done reading the current chunk
       if (s_misc[1]) break; // a bounded wait gave up: stop issuing work
-      if ((ks & 1) == 0) fetch_chunk((ks >> 1) + 2);   // refill the buffer just read
+      if (ks & 1) fetch_chunk((ks >> 1) + 2);   // both K steps of the chunk done: refill its buffer
       if (tid == 0) {
         if (!mbar_wait(bar_full + 8 * s, use & 1)) {
           atomicOr(p.status, PW_STATUS_TIMEOUT);
