@@ -68,6 +68,7 @@ _SIGS = {
     "pw_workspace_status": (_i, [_vp, _vp, _pi]),
     "pw_moe_forward_noalloc": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp]),
     "pw_profile_attach": (_i, [ctypes.POINTER(_vp), _i]),
+    "pw_stats_attach": (_i, [_vp, _vp, ctypes.c_float]),
 }
 
 
@@ -258,6 +259,16 @@ class PagedMoE:
         _check(lib().pw_commit_arrived(self._t, _stream(stream), ctypes.byref(c), ctypes.byref(o)),
                "pw_commit_arrived")
         return c.value, o.value
+
+    def pw_stats_attach(self, stats=None, alpha: float = 0.05):
+        """Attaches a float32 CUDA tensor [L][E] of routing-mass moving averages
+        (updated by every forward), or detaches with None."""
+        if stats is not None:
+            import torch
+            assert stats.dtype == torch.float32 and stats.is_contiguous()
+            assert stats.numel() == self.L * self.E
+        self._stats = stats
+        return _check(lib().pw_stats_attach(self._t, _ptr(stats), float(alpha)), "pw_stats_attach")
 
     def pw_reload_query(self, layer, expert, kind) -> int:
         return _check(lib().pw_reload_query(self._t, layer, expert, kind), "pw_reload_query")

@@ -381,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
     }
     if (p.user_offsets)
       for (int e = threadIdx.x; e <= p.E; e += blockDim.x) p.user_offsets[e] = r.off[e];
+    update_route_stats(p, r.perm, r.w, r.off);
   } else {
     if (threadIdx.x == 0) {
       const bool ok = wait_eq(p.sync, static_cast<int>(p.epoch));

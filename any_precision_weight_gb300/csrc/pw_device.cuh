@@ -36,6 +36,8 @@ struct Fwd {
   __half* hh;               // [T*k][I] h (fp16) in permuted order
   __half* xp;               // [T*k][H] token rows in permuted (expert) order, prefill GEMMs
   float* y;                 // [T*k][H]
+  float* stats;             // [L][E] routing-mass moving average, or null
+  float stats_alpha;        // its update weight
 };
 
 // Work-queue counters live right after the status word.

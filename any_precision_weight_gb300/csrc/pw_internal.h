@@ -98,6 +98,8 @@ struct ForwardArgs {
   unsigned char* ws;       // workspace base
   Workspace lay;
   cudaEvent_t prof[5];     // boundary events (pw_profile_attach), or all null
+  float* stats;            // routing-mass statistics [L][E] (pw_stats_attach), or null
+  float stats_alpha;
 };
 
 // Host helpers (pw_runtime.cpp): sets this thread's pw_last_error message and

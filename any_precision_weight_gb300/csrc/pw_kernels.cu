@@ -58,6 +58,10 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_permute(Fwd p) {
   if (threadIdx.x < 4) p.status[threadIdx.x] = 0u;   // status word and work-queue counters
   __syncthreads();
   route_permute_block(p, s_cnt, s_off);
+  if (p.stats) {
+    __syncthreads();
+    update_route_stats(p, p.perm, p.w, p.offsets);
+  }
 }
 
 // ------------------------------------------------------------------ combine
@@ -101,6 +105,8 @@ static Fwd make_fwd(const ForwardArgs& a) {
   p.hh = reinterpret_cast<__half*>(ws + a.lay.hh);
   p.xp = reinterpret_cast<__half*>(ws + a.lay.xp);
   p.y = reinterpret_cast<float*>(ws + a.lay.y);
+  p.stats = a.stats;
+  p.stats_alpha = a.stats_alpha;
   return p;
 }
 

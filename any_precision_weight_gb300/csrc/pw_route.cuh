@@ -303,6 +303,28 @@ __device__ __forceinline__ void route_local(const Fwd& p, const RouteSmem& r, bo
   __syncthreads();
 }
 
+// Routing statistics, a by-product of the routing step (the runtime planner's
+// routing-mass input): for each expert e, the batch mass
+// M_e = (1/T) * sum of the routing weights of the pairs routed to e, and
+// stats[layer][e] <- (1 - alpha) * stats[layer][e] + alpha * M_e.  One CTA; a warp
+// per expert sums its pairs (expert order from the permutation) in a fixed
+// order, so the result is the same on every run.  perm / w / off may live in
+// global or shared memory; the caller synchronises the block before and after.
+__device__ __forceinline__ void update_route_stats(const Fwd& p, const int* perm, const float* w,
+                                                   const int* off) {
+  if (!p.stats || p.T <= 0) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  float* m = p.stats + static_cast<size_t>(p.layer) * p.E;
+  const float a = p.stats_alpha, invT = 1.f / static_cast<float>(p.T);
+  for (int e = warp; e < p.E; e += nwarp) {
+    float s = 0.f;
+    for (int pos = off[e] + lane; pos < off[e + 1]; pos += 32) s += w[perm[pos]];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) m[e] = (1.f - a) * m[e] + a * (s * invT);
+  }
+}
+
 // out[t][r] = residual[t][r] + sum_j w[t][j] * y(t, j)[r] for r in [r0, r1) and
 // t in [t0, t1), slots added in order j = 0..k-1 (deterministic), rounded once.
 // w / inv may live in global or shared memory.

@@ -113,6 +113,8 @@ struct pw_table {
   std::mutex mu;
   std::condition_variable enqueued;   // signalled when a reload's enqueue phase ends
   bool fail_next_reload = false;   // test hook, see pw_debug_fail_next_reload
+  float* stats = nullptr;          // routing-mass statistics [L][E] (pw_stats_attach)
+  float stats_alpha = 0.f;
 
   // The reload mover (pw_mover_start): a host thread that takes submitted
   // reloads in order and enqueues them with a bound on the bytes in flight.
@@ -870,6 +872,11 @@ int pw_moe_forward(pw_table* t, int layer, const void* x, const float* logits, i
     a.prof[i] = g_prof[i];
     g_prof[i] = nullptr;
   }
+  {
+    std::lock_guard<std::mutex> lk(t->mu);
+    a.stats = t->stats;
+    a.stats_alpha = t->stats_alpha;
+  }
   const cudaError_t e = pw::launch_forward(a, reinterpret_cast<cudaStream_t>(compute));
   if (e != cudaSuccess) return cuda_fail(e, "pw_moe_forward: launch");
   return PW_OK;
@@ -905,6 +912,18 @@ int pw_moe_forward_host(pw_table* t, int layer, const void* x_host, const float*
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "pw_moe_forward_host: output copy");
   if (status) return fail(PW_EDEVICE, "pw_moe_forward_host: device status 0x%x", status);
+  return PW_OK;
+}
+
+int pw_stats_attach(pw_table* t, float* d_stats, float alpha) {
+  if (!t) return fail(PW_EINVAL, "pw_stats_attach: null table");
+  if (d_stats && !(alpha > 0.f && alpha <= 1.f))
+    return fail(PW_EINVAL, "pw_stats_attach: alpha must be in (0, 1]");
+  if (d_stats && (reinterpret_cast<uintptr_t>(d_stats) & 3))
+    return fail(PW_EINVAL, "pw_stats_attach: statistics buffer not 4-byte aligned");
+  std::lock_guard<std::mutex> lk(t->mu);
+  t->stats = d_stats;
+  t->stats_alpha = d_stats ? alpha : 0.f;
   return PW_OK;
 }
 

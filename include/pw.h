@@ -252,6 +252,22 @@ int pw_mover_submit(pw_table* t, int n, const int* layer, const int* expert, con
  */
 int pw_commit_arrived(pw_table* t, pw_stream_t compute, int* n_committed, int* n_outstanding);
 
+/*
+ * pw_stats_attach -- routing statistics as a by-product of the routing step
+ * (the routing-mass input of the pages' runtime planner, "Quality-Aware Runtime
+ * Planner": experts that receive more routing mass matter more).  d_stats is a
+ * caller-owned device array of n_layers * n_experts floats, initialised by the
+ * caller (zeros, or 1/E for a uniform prior).  Once attached, every forward
+ * of layer l updates, on its stream and inside its routing kernel (no extra
+ * launch), for every expert e:
+ *   stats[l][e] <- (1 - alpha) * stats[l][e] + alpha * M_e,
+ *   M_e = (1/T) * sum of the routing weights of the (token, slot) pairs routed to e,
+ * summed in a fixed order (the same result on every run).  With renorm the
+ * M_e of a batch sum to 1.  d_stats = null detaches.  Attach between forwards.
+ * Errors: PW_EINVAL (null table, alpha outside (0, 1], misaligned buffer).
+ */
+int pw_stats_attach(pw_table* t, float* d_stats, float alpha);
+
 /* Host view of one block: committed q, resident planes, pending reload target (0 if none). */
 int pw_block_state(pw_table* t, int layer, int expert, int kind, int* q, int* resident,
                    int* reload_target);

@@ -20,6 +20,10 @@ as:
    silu(z) = z / (1 + e^-z); y = W_down . h;
 4. combine: out[t] = residual[t] (if given) + sum_j w[t][j] * y(t, j).
 
+Routing statistics (the planner's routing-mass input) are the plain
+per-expert sum of routing weights divided by the batch size, folded into an
+exponential moving average.
+
 Every step is fp64 from the fp16 / fp32 inputs; the GPU's fp16 intermediates
 are not modelled.
 """
@@ -57,6 +61,25 @@ def route(logits: np.ndarray, k: int, renorm: int):
         idx[t] = top
         w[t] = wt
     return idx, w
+
+
+def routing_mass(idx: np.ndarray, w: np.ndarray, E: int):
+    """Per-expert routing mass of one batch: M[e] = (1/T) * sum of w[t][j] over
+    the pairs with idx[t][j] == e (the routing-mass signal of the runtime
+    planner, "Quality-Aware Runtime Planner").  fp64 [E]."""
+    idx = np.asarray(idx)
+    w = np.asarray(w, dtype=np.float64)
+    T, k = idx.shape
+    M = np.zeros(E, dtype=np.float64)
+    for t in range(T):
+        for j in range(k):
+            M[idx[t, j]] += w[t, j]
+    return M / T if T else M
+
+
+def stats_update(m: np.ndarray, idx: np.ndarray, w: np.ndarray, E: int, alpha: float):
+    """One step of the routing-mass moving average: (1 - alpha) * m + alpha * M."""
+    return (1.0 - alpha) * np.asarray(m, dtype=np.float64) + alpha * routing_mass(idx, w, E)
 
 
 def permute(idx: np.ndarray, E: int):

@@ -247,3 +247,43 @@ def test_forward_argument_errors():
     with pytest.raises(pw.PWError) as e:
         m2.pw_moe_forward(0, x, L, 2, 1)
     assert e.value.code == pw.PW_EINVAL
+
+
+@pytest.mark.parametrize("T", [16, 300])   # the fused decode kernel and the separate routing kernel
+def test_routing_statistics_follow_the_oracle_moving_average(T):
+    import torch
+    cfg = synth.CONFIGS["tiny"]
+    m = gpu_layer(cfg, n_layers=2, bits={0: synth.block_bits(cfg, 0), 1: synth.block_bits(cfg, 1)})
+    stats = torch.full((2, cfg.E), 1.0 / cfg.E, dtype=torch.float32, device="cuda")
+    alpha = 0.2
+    m.pw_stats_attach(stats, alpha)
+    want = np.full((2, cfg.E), 1.0 / cfg.E)
+    for step in range(4):
+        for l in range(2):
+            x = torch.from_numpy(synth.tokens(cfg, step=step, T=T)).cuda()
+            L = synth.logits(cfg, l, step=step, T=T)
+            m.pw_moe_forward(l, x, torch.from_numpy(L).cuda(), cfg.top_k, cfg.renorm)
+            idx, w = omoe.route(L, cfg.top_k, cfg.renorm)
+            want[l] = omoe.stats_update(want[l], idx, w, cfg.E, alpha)
+    torch.cuda.synchronize()
+    got = stats.cpu().numpy().astype(np.float64)
+    assert np.allclose(got, want, rtol=1e-5, atol=1e-7)
+    assert np.allclose(got.sum(axis=1), 1.0, atol=1e-5)      # renorm: every batch adds mass 1
+    # detached: forwards leave the statistics alone
+    m.pw_stats_attach(None)
+    before = stats.clone()
+    m.pw_moe_forward(0, x, torch.from_numpy(L).cuda(), cfg.top_k, cfg.renorm)
+    torch.cuda.synchronize()
+    assert torch.equal(stats, before)
+
+
+def test_stats_attach_rejects_bad_alpha():
+    import torch
+    import any_precision_weight_gb300 as pw
+    cfg = synth.CONFIGS["tiny"]
+    m = gpu_layer(cfg)
+    s = torch.zeros((1, cfg.E), dtype=torch.float32, device="cuda")
+    for a in (0.0, -0.5, 1.5):
+        with pytest.raises(pw.PWError) as e:
+            m.pw_stats_attach(s, a)
+        assert e.value.code == pw.PW_EINVAL

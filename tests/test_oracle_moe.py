@@ -221,3 +221,60 @@ def test_residual_added_once():
     a = moe.layer(x, L, 2, 0, lambda e: blocks[e])["out"]
     b = moe.layer(x, L, 2, 0, lambda e: blocks[e], residual=x)["out"]
     assert np.allclose(b - a, x.astype(np.float64), rtol=0, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- routing statistics
+
+def _stats_gold():
+    d = {}
+    for line in open(os.path.join(GOLD, "stats_hand.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, vals = (x.strip() for x in line.split("|"))
+        d[key] = np.array([float(v) for v in vals.split()])
+    return d
+
+
+def test_routing_mass_hand_case():
+    g = _stats_gold()
+    L = np.stack([g["logits_t0"], g["logits_t1"]]).astype(np.float32)
+    idx, w = moe.route(L, 2, 1)
+    assert np.array_equal(moe.routing_mass(idx, w, 4), g["M"])
+    m1 = moe.stats_update(np.full(4, 0.25), idx, w, 4, 0.25)
+    assert np.array_equal(m1, g["m1"])
+    assert np.array_equal(moe.stats_update(m1, idx, w, 4, 0.25), g["m2"])
+
+
+def test_routing_mass_sums_to_one_with_renorm_and_to_the_kept_mass_without():
+    rng = np.random.default_rng(5)
+    L = rng.standard_normal((37, 9)).astype(np.float32)
+    idx, w = moe.route(L, 3, 1)
+    assert abs(moe.routing_mass(idx, w, 9).sum() - 1.0) < 1e-12
+    idx0, w0 = moe.route(L, 3, 0)
+    # the mass kept by the top 3 of a softmax, averaged over tokens (scipy's softmax)
+    from scipy.special import softmax
+    p = np.sort(softmax(L.astype(np.float64), axis=1), axis=1)[:, ::-1]
+    assert abs(moe.routing_mass(idx0, w0, 9).sum() - p[:, :3].sum(axis=1).mean()) < 1e-12
+
+
+def test_routing_mass_with_all_experts_is_the_mean_softmax():
+    from scipy.special import softmax
+    rng = np.random.default_rng(6)
+    L = rng.standard_normal((11, 6)).astype(np.float32)
+    idx, w = moe.route(L, 6, 0)
+    want = softmax(L.astype(np.float64), axis=1).mean(axis=0)
+    assert np.allclose(moe.routing_mass(idx, w, 6), want, rtol=0, atol=1e-14)
+
+
+def test_repeated_batch_follows_the_geometric_closed_form():
+    rng = np.random.default_rng(7)
+    L = rng.standard_normal((8, 5)).astype(np.float32)
+    idx, w = moe.route(L, 2, 1)
+    M = moe.routing_mass(idx, w, 5)
+    m0 = rng.random(5)
+    a, m = 0.1, m0.copy()
+    for n in range(1, 30):
+        m = moe.stats_update(m, idx, w, 5, a)
+        closed = (1 - a) ** n * m0 + (1 - (1 - a) ** n) * M
+        assert np.allclose(m, closed, rtol=0, atol=1e-14)
