@@ -69,6 +69,9 @@ _SIGS = {
     "pw_moe_forward_noalloc": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp]),
     "pw_profile_attach": (_i, [ctypes.POINTER(_vp), _i]),
     "pw_stats_attach": (_i, [_vp, _vp, ctypes.c_float]),
+    "pw_plan_bits": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _i, ctypes.c_double, _i, _i, _i, ctypes.c_double,
+                          _vp, ctypes.POINTER(ctypes.c_int64)]),
+    "pw_plan_apply": (_i, [_vp, _vp, _vp, _pi, _pi]),
 }
 
 
@@ -163,6 +166,23 @@ def pw_profile_attach(events):
 
 
 # ----------------------------------------------------------------------------- page table
+
+def pw_plan_bits(R, K, sens, mass, n_experts, hot_mass, hot_floor, target_bytes, resid=None,
+                 b_min: int = 3, n_bits: int = MAX_BITS):
+    """The native planner on host arrays (one entry per block).  Returns
+    (bits int32 array, resident bytes of the plan)."""
+    R = np.ascontiguousarray(R, dtype=np.int32)
+    K = np.ascontiguousarray(K, dtype=np.int32)
+    sens = np.ascontiguousarray(sens, dtype=np.float64)
+    mass = np.ascontiguousarray(mass, dtype=np.float64)
+    rs = None if resid is None else np.ascontiguousarray(resid, dtype=np.float64)
+    out = np.empty(len(R), dtype=np.int32)
+    res = ctypes.c_int64()
+    _check(lib().pw_plan_bits(len(R), _ptr(R), _ptr(K), _ptr(sens), _ptr(rs), _ptr(mass), int(n_experts),
+                              float(hot_mass), int(hot_floor), int(b_min), int(n_bits), float(target_bytes),
+                              _ptr(out), ctypes.byref(res)), "pw_plan_bits")
+    return out, res.value
+
 
 class PagedMoE:
     """Owns the device memory of one model's MoE blocks and the C page table.
@@ -269,6 +289,16 @@ class PagedMoE:
             assert stats.numel() == self.L * self.E
         self._stats = stats
         return _check(lib().pw_stats_attach(self._t, _ptr(stats), float(alpha)), "pw_stats_attach")
+
+    def pw_plan_apply(self, desired, stream=None):
+        """desired: int array [L][E][2] (0 = leave alone).  Returns (committed now,
+        handed to the mover)."""
+        d = np.ascontiguousarray(desired, dtype=np.int32).reshape(-1)
+        assert d.size == self.L * self.E * 2
+        a, b = _i(), _i()
+        _check(lib().pw_plan_apply(self._t, _ptr(d), _stream(stream), ctypes.byref(a), ctypes.byref(b)),
+               "pw_plan_apply")
+        return a.value, b.value
 
     def pw_reload_query(self, layer, expert, kind) -> int:
         return _check(lib().pw_reload_query(self._t, layer, expert, kind), "pw_reload_query")

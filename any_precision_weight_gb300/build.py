@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpw.so")
 
-SOURCES = ["pw_runtime.cpp", "pw_kernels.cu", "pw_decode.cu", "pw_prefill.cu", "pw_static.cu"]
+SOURCES = ["pw_runtime.cpp", "pw_planner.cpp", "pw_kernels.cu", "pw_decode.cu", "pw_prefill.cu", "pw_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -732,6 +732,56 @@ int pw_mover_submit(pw_table* t, int n, const int* layer, const int* expert, con
   return PW_OK;
 }
 
+int pw_plan_apply(pw_table* t, const int* desired, pw_stream_t compute, int* n_now, int* n_moved) {
+  if (n_now) *n_now = 0;
+  if (n_moved) *n_moved = 0;
+  if (!t || !desired) return fail(PW_EINVAL, "pw_plan_apply: null table or plan");
+  std::vector<std::pair<size_t, int>> now;
+  std::vector<MoveReq> moves;
+  {
+    std::lock_guard<std::mutex> lk(t->mu);
+    for (size_t i = 0; i < t->blocks.size(); ++i) {   // every entry checked before anything is done
+      const int d = desired[i];
+      if (d == 0) continue;
+      const BlockState& b = t->blocks[i];
+      if (!b.registered) return fail(PW_EINVAL, "pw_plan_apply: block %zu is not registered", i);
+      if (d < b.b_min || d > b.n_bits)
+        return fail(PW_EINVAL, "pw_plan_apply: block %zu: q %d outside [%d, %d]", i, d, b.b_min, b.n_bits);
+      if (d == b.q) continue;
+      if (d <= b.resident) {
+        now.push_back({i, d});
+        continue;
+      }
+      if (b.pending) return fail(PW_EINVAL, "pw_plan_apply: block %zu has a reload pending", i);
+      for (int p = 0; p < d; ++p)
+        if (!b.pages[p]) return fail(PW_EINVAL, "pw_plan_apply: block %zu has no page for plane %d", i, p);
+      const int kind = static_cast<int>(i % 2), expert = static_cast<int>((i / 2) % t->E),
+                layer = static_cast<int>(i / (2 * static_cast<size_t>(t->E)));
+      moves.push_back({layer, expert, kind, d});
+    }
+    if (!moves.empty()) {
+      std::lock_guard<std::mutex> mk(t->mover_mu);
+      if (!t->mover.joinable())
+        return fail(PW_EINVAL, "pw_plan_apply: %zu blocks need a reload and the mover is not running",
+                    moves.size());
+    }
+    if (!now.empty()) {
+      const int rc = commit_descs(t, now, reinterpret_cast<cudaStream_t>(compute));
+      if (rc != PW_OK) return rc;
+    }
+  }
+  if (!moves.empty()) {
+    {
+      std::lock_guard<std::mutex> mk(t->mover_mu);
+      for (const MoveReq& r : moves) t->requests.push_back(r);
+    }
+    t->mover_cv.notify_all();
+  }
+  if (n_now) *n_now = static_cast<int>(now.size());
+  if (n_moved) *n_moved = static_cast<int>(moves.size());
+  return PW_OK;
+}
+
 int pw_commit_arrived(pw_table* t, pw_stream_t compute, int* n_committed, int* n_outstanding) {
   if (n_committed) *n_committed = 0;
   if (n_outstanding) *n_outstanding = 0;

@@ -268,6 +268,49 @@ int pw_commit_arrived(pw_table* t, pw_stream_t compute, int* n_committed, int* n
  */
 int pw_stats_attach(pw_table* t, float* d_stats, float alpha);
 
+/* ------------------------------------------------------------------ planner (host) */
+
+/*
+ * pw_plan_bits -- the quality-aware bitwidth planner ("Quality-Aware Runtime
+ * Planner": offline Hessian-weighted sensitivity, online routing mass with
+ * higher floors and damage multipliers for hot experts, a prompt residual
+ * correcting the sensitivity; greedy lowest damage per byte saved until a
+ * memory target is met).  Host only, no CUDA call.
+ *
+ * Per block i (host arrays of n_blocks): R[i] x K[i] weights, sens[i] the
+ * offline sensitivity, resid[i] the prompt residual (resid may be null: 0),
+ * mass[i] the routing mass of the block's expert.  The pages give no formulas;
+ * this reading is used:
+ *   s' = max(0, sens + resid), m = 1 + n_experts * mass,
+ *   floor = hot_floor if mass >= hot_mass else b_min,
+ *   damage of b -> b-1 bits = m * s' * R * K * (4^-(b-1) - 4^-b),
+ *   bytes saved = R*K/8 + R * 2^b * 2 (one plane and the b-bit table).
+ * Starting from n_bits everywhere, reductions are taken in increasing damage /
+ * bytes saved (ties: lower block index) while the resident bytes exceed
+ * target_bytes and some block is above its floor.  bits_out[i] receives the
+ * planned bitwidth; *resident_out (if not null) the resident bytes of the plan
+ * (above target_bytes when the floors stop it).
+ * Errors: PW_EINVAL (null array, bad sizes, not 1 <= b_min <= hot_floor <= n_bits <= 8).
+ */
+int pw_plan_bits(int n_blocks, const int* R, const int* K, const double* sens, const double* resid,
+                 const double* mass, int n_experts, double hot_mass, int hot_floor, int b_min,
+                 int n_bits, double target_bytes, int* bits_out, int64_t* resident_out);
+
+/*
+ * pw_plan_apply -- carries out a plan on a table.  desired[] holds one
+ * bitwidth per block in descriptor order ((layer * n_experts + expert) * 2 +
+ * kind), 0 for "leave alone".  Blocks to lower, and blocks to raise whose
+ * planes are already resident, are committed at once on the compute stream
+ * (one batched commit); blocks to raise above their resident planes are
+ * submitted to the mover (pw_mover_start must have been called) and commit
+ * at a later pw_commit_arrived.  Every entry is checked before anything is
+ * done.  *n_now / *n_moved (either may be null): blocks committed now / handed
+ * to the mover.  Errors: PW_EINVAL (unregistered block with desired > 0, q out
+ * of range, no page for a plane, mover not running while a reload is needed),
+ * PW_ECUDA.
+ */
+int pw_plan_apply(pw_table* t, const int* desired, pw_stream_t compute, int* n_now, int* n_moved);
+
 /* Host view of one block: committed q, resident planes, pending reload target (0 if none). */
 int pw_block_state(pw_table* t, int layer, int expert, int kind, int* q, int* resident,
                    int* reload_target);

@@ -341,3 +341,57 @@ def test_mover_commits_landed_reloads_at_step_boundaries():
         assert not np.array_equal(got, before[l])
     with pytest.raises(pw.PWError):
         m.pw_mover_start(copy)                    # already running
+
+
+def test_planner_plan_applied_to_a_stack():
+    """pw_plan_bits on the table's blocks, then pw_plan_apply: lowering (and raising
+    within resident planes) commits at once, raising above them goes through the
+    mover; each layer then matches the oracle at the planned bits."""
+    import torch
+    import any_precision_weight_gb300 as pw
+    from oracle import planner as oplan
+    cfg = synth.CONFIGS["tiny"]
+    L_ = 3
+    start = {l: np.full((cfg.E, 2), 4, dtype=np.int32) for l in range(L_)}
+    m = gpu_layer(cfg, n_layers=L_, bits=start, alloc_planes=lambda e, k: 8)
+    nb = L_ * cfg.E * 2
+    R = np.array([cfg.rows(i % 2) for i in range(nb)])
+    K = np.array([cfg.cols(i % 2) for i in range(nb)])
+    rng = np.random.default_rng(3)
+    sens = rng.lognormal(0.0, 1.0, nb)
+    mass = np.repeat(rng.dirichlet(np.ones(cfg.E), size=L_).reshape(-1), 2)
+    full = sum(oplan.resident_bytes(int(r), int(k), 8, 3) for r, k in zip(R, K))
+    x = torch.from_numpy(synth.tokens(cfg)).cuda()
+    Ls = [torch.from_numpy(synth.logits(cfg, l)).cuda() for l in range(L_)]
+    copy = torch.cuda.Stream()
+    m.pw_mover_start(copy)
+
+    def run_plan(frac):
+        bits, _ = pw.pw_plan_bits(R, K, sens, mass, cfg.E, 1.0 / cfg.E, 6, frac * full)
+        want, _ = oplan.plan_bits(list(R), list(K), list(sens), list(mass), cfg.E, 1.0 / cfg.E, 6, 3, 8,
+                                  frac * full)
+        assert np.array_equal(bits, want)
+        now, moved = m.pw_plan_apply(bits.reshape(L_, cfg.E, 2))
+        left = moved
+        for _ in range(100000):
+            if left == 0:
+                break
+            _, left = m.pw_commit_arrived()
+        assert left == 0
+        torch.cuda.synchronize()
+        b3 = bits.reshape(L_, cfg.E, 2)
+        for l in range(L_):
+            for e in range(cfg.E):
+                for k in range(2):
+                    assert m.pw_block_state(l, e, k)[0] == b3[l, e, k]
+            got = to_np(m.pw_moe_forward(l, x, Ls[l], cfg.top_k, cfg.renorm))
+            ref = omoe.layer(to_np(x), to_np(Ls[l]), cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, l), b3[l]))
+            assert_close(got, ref["out"])
+        return now, moved
+
+    now, moved = run_plan(0.7)      # from 4 bits everywhere: most blocks go up through the mover
+    assert moved > 0
+    now, moved = run_plan(0.45)     # lowering only: everything commits at once
+    assert moved == 0 and now > 0
+    now, moved = run_plan(0.7)      # back up: the planes are still resident, no copy needed
+    assert moved == 0 and now > 0
