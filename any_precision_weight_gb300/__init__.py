@@ -31,6 +31,7 @@ PW_EDEVICE = -7
 PW_STATUS_NAN_LOGIT = 1
 PW_STATUS_TIMEOUT = 2
 PW_STATUS_BAD_DESC = 4
+PW_PLANE_HOST, PW_PLANE_HOST_PAGED, PW_PLANE_MOVING, PW_PLANE_DEVICE = 0, 1, 2, 3
 KIND_GATE_UP = 0
 KIND_DOWN = 1
 MAX_BITS = 8
@@ -72,6 +73,9 @@ _SIGS = {
     "pw_plan_bits": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _i, ctypes.c_double, _i, _i, _i, ctypes.c_double,
                           _vp, ctypes.POINTER(ctypes.c_int64)]),
     "pw_plan_apply": (_i, [_vp, _vp, _vp, _pi, _pi]),
+    "pw_block_release": (_i, [_vp, _i, _i, _i, _i, ctypes.POINTER(_vp)]),
+    "pw_block_attach_pages": (_i, [_vp, _i, _i, _i, ctypes.POINTER(_vp)]),
+    "pw_plane_states": (_i, [_vp, _i, _i, _i, _pi]),
 }
 
 
@@ -210,16 +214,24 @@ class PagedMoE:
         return (2 * self.I, self.H) if kind == KIND_GATE_UP else (self.H, self.I)
 
     def register(self, layer: int, expert: int, kind: int, planes_host, luts_host, q_init: int,
-                 n_bits: int = 8, b_min: int = 3, alloc_planes: int | None = None, stream=None):
+                 n_bits: int = 8, b_min: int = 3, alloc_planes: int | None = None, stream=None,
+                 per_plane: bool = False):
         """planes_host / luts_host: pinned torch CPU tensors (or numpy arrays) in
-        pw_pack layout; kept alive by this object."""
+        pw_pack layout; kept alive by this object.  per_plane: one device
+        tensor per plane (so released planes free their memory) instead of one
+        tensor for all of the block's pages."""
         import torch
         R, K = self.rows_cols(kind)
         pb = pw_plane_bytes(R, K)
         na = n_bits if alloc_planes is None else max(q_init, min(alloc_planes, n_bits))
-        pages = torch.empty(na * pb, dtype=torch.uint8, device=self.device)
         luts = torch.empty(pw_lut_bytes(R, b_min, n_bits), dtype=torch.uint8, device=self.device)
-        ptrs = (_vp * n_bits)(*[pages.data_ptr() + p * pb if p < na else None for p in range(n_bits)])
+        if per_plane:
+            pages = [torch.empty(pb, dtype=torch.uint8, device=self.device) if p < na else None
+                     for p in range(n_bits)]
+            ptrs = (_vp * n_bits)(*[pg.data_ptr() if pg is not None else None for pg in pages])
+        else:
+            pages = torch.empty(na * pb, dtype=torch.uint8, device=self.device)
+            ptrs = (_vp * n_bits)(*[pages.data_ptr() + p * pb if p < na else None for p in range(n_bits)])
         _check(lib().pw_block_register(self._t, layer, expert, kind, n_bits, b_min, _ptr(planes_host),
                                        _ptr(luts_host), ptrs, luts.data_ptr(), q_init, _stream(stream)),
                "pw_block_register")
@@ -230,7 +242,49 @@ class PagedMoE:
         return self._keep[(layer, expert, kind)][:2]
 
     def device_bytes(self) -> int:
-        return sum(v[0].numel() + v[1].numel() for v in self._keep.values())
+        def nb(pages):
+            if isinstance(pages, list):
+                return sum(p.numel() for p in pages if p is not None)
+            return pages.numel()
+        return sum(nb(v[0]) + v[1].numel() for v in self._keep.values())
+
+    def pw_block_release(self, layer, expert, kind, keep, stream=None):
+        """Offloads planes [keep, n) of a block.  Per-plane blocks drop their
+        page tensors once the stream has passed every earlier forward.
+        Returns the released device addresses (None where none)."""
+        import torch
+        out = (_vp * MAX_BITS)()
+        _check(lib().pw_block_release(self._t, layer, expert, kind, keep, out), "pw_block_release")
+        rel = [out[p] for p in range(MAX_BITS)]
+        pages = self._keep[(layer, expert, kind)][0]
+        if isinstance(pages, list) and any(rel):
+            (stream or torch.cuda.current_stream()).synchronize()
+            for p in range(MAX_BITS):
+                if rel[p] and p < len(pages):
+                    pages[p] = None
+        return rel
+
+    def pw_block_attach_pages(self, layer, expert, kind):
+        """Gives a per-plane block fresh device pages for every plane without one."""
+        import torch
+        pages = self._keep[(layer, expert, kind)][0]
+        assert isinstance(pages, list), "attach_pages needs a block registered with per_plane=True"
+        R, K = self.rows_cols(kind)
+        pb = pw_plane_bytes(R, K)
+        new = [None] * MAX_BITS
+        for p in range(len(pages)):
+            if pages[p] is None:
+                new[p] = torch.empty(pb, dtype=torch.uint8, device=self.device)
+        ptrs = (_vp * MAX_BITS)(*[t.data_ptr() if t is not None else None for t in new])
+        _check(lib().pw_block_attach_pages(self._t, layer, expert, kind, ptrs), "pw_block_attach_pages")
+        for p in range(len(pages)):
+            if new[p] is not None:
+                pages[p] = new[p]
+
+    def pw_plane_states(self, layer, expert, kind):
+        st = (_i * MAX_BITS)()
+        _check(lib().pw_plane_states(self._t, layer, expert, kind, st), "pw_plane_states")
+        return [st[p] for p in range(MAX_BITS)]
 
     def pw_set_commit(self, layer, expert, kind, q, stream=None):
         return _check(lib().pw_set_commit(self._t, layer, expert, kind, q, _stream(stream)),

@@ -834,6 +834,59 @@ int pw_commit_arrived(pw_table* t, pw_stream_t compute, int* n_committed, int* n
   return rc;
 }
 
+int pw_block_release(pw_table* t, int layer, int expert, int kind, int keep, void** released) {
+  if (!t) return fail(PW_EINVAL, "pw_block_release: null table");
+  std::lock_guard<std::mutex> lk(t->mu);
+  BlockState* b = block_of(t, layer, expert, kind);
+  if (!b || !b->registered) return fail(PW_EINVAL, "pw_block_release: block not registered");
+  if (keep < b->q || keep > b->n_bits)
+    return fail(PW_EINVAL, "pw_block_release: keep %d outside [committed q %d, %d]", keep, b->q, b->n_bits);
+  if (b->pending) return fail(PW_EINVAL, "pw_block_release: a reload of this block is pending");
+  for (int p = 0; p < PW_MAX_BITS; ++p) {
+    void* page = nullptr;
+    if (p >= keep && p < b->n_bits) {
+      page = b->pages[p];
+      b->pages[p] = nullptr;
+    }
+    if (released) released[p] = page;
+  }
+  if (b->resident > keep) b->resident = keep;
+  return PW_OK;
+}
+
+int pw_block_attach_pages(pw_table* t, int layer, int expert, int kind, void* const* pages) {
+  if (!t || !pages) return fail(PW_EINVAL, "pw_block_attach_pages: null table or pages");
+  std::lock_guard<std::mutex> lk(t->mu);
+  BlockState* b = block_of(t, layer, expert, kind);
+  if (!b || !b->registered) return fail(PW_EINVAL, "pw_block_attach_pages: block not registered");
+  if (b->pending) return fail(PW_EINVAL, "pw_block_attach_pages: a reload of this block is pending");
+  for (int p = 0; p < b->n_bits; ++p) {   // all checked first
+    if (!pages[p]) continue;
+    if (p < b->resident && pages[p] != b->pages[p])
+      return fail(PW_EINVAL, "pw_block_attach_pages: plane %d is resident on another page", p);
+    if (!aligned16(pages[p])) return fail(PW_EINVAL, "pw_block_attach_pages: page %d not 16-byte aligned", p);
+  }
+  for (int p = b->resident; p < b->n_bits; ++p)
+    if (pages[p]) b->pages[p] = pages[p];
+  return PW_OK;
+}
+
+int pw_plane_states(pw_table* t, int layer, int expert, int kind, int* states) {
+  if (!t || !states) return fail(PW_EINVAL, "pw_plane_states: null table or output");
+  std::lock_guard<std::mutex> lk(t->mu);
+  BlockState* b = block_of(t, layer, expert, kind);
+  if (!b || !b->registered) return fail(PW_EINVAL, "pw_plane_states: block not registered");
+  for (int p = 0; p < PW_MAX_BITS; ++p) {
+    int st = PW_PLANE_HOST;
+    if (p >= b->n_bits) st = PW_PLANE_HOST;
+    else if (p < b->resident) st = PW_PLANE_DEVICE;
+    else if (b->pending && !b->failed && p < b->pending) st = PW_PLANE_MOVING;
+    else if (b->pages[p]) st = PW_PLANE_HOST_PAGED;
+    states[p] = st;
+  }
+  return PW_OK;
+}
+
 int pw_block_state(pw_table* t, int layer, int expert, int kind, int* q, int* resident,
                    int* reload_target) {
   if (!t) return fail(PW_EINVAL, "pw_block_state: null table");

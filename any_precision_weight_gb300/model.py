@@ -62,7 +62,8 @@ def pack_pinned(P: np.ndarray, parent_lut: np.ndarray, n_bits: int = 8, b_min: i
 
 
 def load_expert_layer(moe: PagedMoE, layer: int, blocks, bits, n_bits: int = 8, b_min: int = 3,
-                      alloc_planes=None, stream=None, store: HostStore | None = None):
+                      alloc_planes=None, stream=None, store: HostStore | None = None,
+                      per_plane: bool = False):
     """Registers every block of one layer.
 
     blocks(e, kind) -> (P uint8 [R][K], parent_lut fp16 [R][2^n]);
@@ -76,4 +77,4 @@ def load_expert_layer(moe: PagedMoE, layer: int, blocks, bits, n_bits: int = 8, 
             planes, luts = pack_pinned(P, par, n_bits, b_min, store=store)
             na = None if alloc_planes is None else alloc_planes(e, kind)
             moe.register(layer, e, kind, planes, luts, int(bits[e][kind]), n_bits=n_bits,
-                         b_min=b_min, alloc_planes=na, stream=stream)
+                         b_min=b_min, alloc_planes=na, stream=stream, per_plane=per_plane)

@@ -311,6 +311,47 @@ int pw_plan_bits(int n_blocks, const int* R, const int* K, const double* sens, c
  */
 int pw_plan_apply(pw_table* t, const int* desired, pw_stream_t compute, int* n_now, int* n_moved);
 
+/* ------------------------------------------------------------------ offload */
+
+/*
+ * Page states of a plane ("Weight Page Table": pages are GPU-resident,
+ * CPU-resident or in transfer).  The host backing store given to
+ * pw_block_register holds every plane of the block for the table's lifetime
+ * (weights never change), so a plane leaves the GPU by releasing its device
+ * page; no device-to-host copy is needed.
+ */
+#define PW_PLANE_HOST 0        /* host copy only, no device page */
+#define PW_PLANE_HOST_PAGED 1  /* host copy; a device page is attached but not filled */
+#define PW_PLANE_MOVING 2      /* a reload into the device page is in flight */
+#define PW_PLANE_DEVICE 3      /* resident on the device */
+
+/*
+ * pw_block_release -- offloads planes [keep, n_bits) of one block: they stop
+ * being resident and their device pages are detached from the table and
+ * returned in released[0..7] (null where no page was detached), for the
+ * caller to free or reuse.  keep must be >= the committed q, so no forward
+ * enqueued after this call reads them; forwards enqueued earlier at a higher
+ * committed q may still be running, so reuse a released page only after the
+ * compute stream has passed the commit that lowered q (for example after a
+ * stream synchronisation or an event recorded after that commit).  Errors:
+ * PW_EINVAL (keep outside [q, n_bits], a reload pending).
+ */
+int pw_block_release(pw_table* t, int layer, int expert, int kind, int keep, void** released);
+
+/*
+ * pw_block_attach_pages -- gives a block device pages for its non-resident
+ * planes (pages[p] for p >= resident; null entries leave a plane as it is), so
+ * that a later reload can fill them (page-pool reuse).  Each page holds
+ * pw_plane_bytes(R, K) bytes, 16-byte aligned.  Errors: PW_EINVAL (a page for a
+ * resident plane that differs from the current one, misaligned page, a reload
+ * pending).
+ */
+int pw_block_attach_pages(pw_table* t, int layer, int expert, int kind, void* const* pages);
+
+/* pw_plane_states -- the PW_PLANE_* state of planes 0..7 of one block (planes
+ * at or above n_bits read PW_PLANE_HOST). */
+int pw_plane_states(pw_table* t, int layer, int expert, int kind, int* states);
+
 /* Host view of one block: committed q, resident planes, pending reload target (0 if none). */
 int pw_block_state(pw_table* t, int layer, int expert, int kind, int* q, int* resident,
                    int* reload_target);

@@ -23,7 +23,7 @@ class SynthBlocks:
                 synth.parent_lut(self.cfg, self.layer, e, kind))
 
 
-def gpu_layer(cfg, n_layers=1, bits=None, blocks=None, alloc_planes=None, layers=None):
+def gpu_layer(cfg, n_layers=1, bits=None, blocks=None, alloc_planes=None, layers=None, per_plane=False):
     """A PagedMoE with the given layers registered.  bits[l] -> [E][2]."""
     import any_precision_weight_gb300 as pw
     from any_precision_weight_gb300.model import load_expert_layer
@@ -31,7 +31,7 @@ def gpu_layer(cfg, n_layers=1, bits=None, blocks=None, alloc_planes=None, layers
     for l in (range(n_layers) if layers is None else layers):
         b = synth.block_bits(cfg, l) if bits is None else bits[l]
         src = SynthBlocks(cfg, l) if blocks is None else blocks[l]
-        load_expert_layer(m, l, src, b, alloc_planes=alloc_planes)
+        load_expert_layer(m, l, src, b, alloc_planes=alloc_planes, per_plane=per_plane)
     return m
 
 

@@ -395,3 +395,47 @@ def test_planner_plan_applied_to_a_stack():
     assert moved == 0 and now > 0
     now, moved = run_plan(0.7)      # back up: the planes are still resident, no copy needed
     assert moved == 0 and now > 0
+
+
+def test_offload_release_and_reattach_round_trip():
+    """Planes above the committed q leave the GPU (their pages are released and
+    freed), the layer keeps matching the oracle at q; fresh pages are attached,
+    the planes are reloaded from the host store and committed again."""
+    import torch
+    import any_precision_weight_gb300 as pw
+    cfg = synth.CONFIGS["tiny"]
+    bits = np.full((cfg.E, 2), 6, dtype=np.int32)
+    m = gpu_layer(cfg, bits={0: bits}, per_plane=True)
+    x = torch.from_numpy(synth.tokens(cfg)).cuda()
+    L = torch.from_numpy(synth.logits(cfg)).cuda()
+    D, HP, HO, MV = pw.PW_PLANE_DEVICE, pw.PW_PLANE_HOST_PAGED, pw.PW_PLANE_HOST, pw.PW_PLANE_MOVING
+    assert m.pw_plane_states(0, 3, 0) == [D] * 6 + [HP] * 2
+    with pytest.raises(pw.PWError):
+        m.pw_block_release(0, 3, 0, 5)                  # below the committed q
+    before = m.device_bytes()
+    for e in range(cfg.E):
+        rel = m.pw_block_release(0, e, 0, 6)
+        assert all(r for r in rel[6:]) and not any(rel[:6])
+    assert m.device_bytes() == before - cfg.E * 2 * cfg.rows(0) * cfg.cols(0) // 8
+    assert m.pw_plane_states(0, 3, 0) == [D] * 6 + [HO] * 2
+    with pytest.raises(pw.PWError) as err:
+        m.pw_reload_async(0, 3, 0, 8)                   # no page for plane 6
+    assert err.value.code == pw.PW_EINVAL
+    ref6 = omoe.layer(to_np(x), to_np(L), cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), bits))
+    assert_close(_fwd(m, cfg, x, L), ref6["out"])
+    # back: fresh pages, reload, commit
+    copy = torch.cuda.Stream()
+    for e in range(cfg.E):
+        m.pw_block_attach_pages(0, e, 0)
+        assert m.pw_plane_states(0, e, 0) == [D] * 6 + [HP] * 2
+        m.pw_reload_async(0, e, 0, 8, stream=copy)
+        st = m.pw_plane_states(0, e, 0)
+        assert st[:6] == [D] * 6 and all(s in (MV, D) for s in st[6:])
+        with pytest.raises(pw.PWError):
+            m.pw_block_release(0, e, 0, 6)              # a reload is pending
+        m.pw_set_commit(0, e, 0, 8)
+    hi = bits.copy()
+    hi[:, 0] = 8
+    ref8 = omoe.layer(to_np(x), to_np(L), cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), hi))
+    assert_close(_fwd(m, cfg, x, L), ref8["out"])
+    assert m.pw_plane_states(0, 3, 0) == [D] * 8
