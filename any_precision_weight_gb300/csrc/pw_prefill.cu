@@ -37,7 +37,8 @@
 namespace pw {
 namespace {
 
-constexpr int kPThreads = 256;
+constexpr int kDqThreads = 256;                // dequantising warps 0..7
+constexpr int kPThreads = kDqThreads + 32;     // + one TMA / MMA issue warp
 constexpr int kBM = 128;                       // tokens per tile (MMA M)
 constexpr int kBN = 128;                       // weight rows per tile (MMA N)
 constexpr int kBK = 64;                        // K per stage: one 128-byte swizzle row of fp16
@@ -68,8 +69,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-// Bounded wait for the phase of the given parity; false when the limit runs out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Bounded wait for the phase of the given parity; false when the limit runs
+// out or when another thread has raised the abort flag.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
   for (long long i = 0; i < kWaitLimit; ++i) {
     uint32_t done;
     asm volatile(
@@ -80,8 +82,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
         : "r"(bar), "r"(parity)
         : "memory");
     if (done) return true;
+    if (*abort) return false;
   }
   return false;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Barrier of the dequantising warps only (the issue warp keeps running).
+__device__ __forceinline__ void named_sync_dq() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kDqThreads) : "memory");
 }
 
 // ---------------------------------------------------------------- TMA / tcgen05
@@ -200,8 +210,9 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = saddr(smem);
   const uint32_t bar_full = sbase + kOffBar;          // [2] TMA of A arrived
-  const uint32_t bar_mma = sbase + kOffBar + 16;      // [2] MMAs of the stage done
-  int* s_misc = reinterpret_cast<int*>(smem + kOffBar + 64);   // [0] tmem addr, [1] abort, [2..] tiles
+  const uint32_t bar_mma = sbase + kOffBar + 16;      // [2] MMAs of the step done (B and A stage free)
+  const uint32_t bar_b = sbase + kOffBar + 32;        // [2] B tile of the step dequantised
+  int* s_misc = reinterpret_cast<int*>(smem + kOffBar + 64);   // [0] tmem addr, [1] abort, [4..] item starts
   __half* lut_s = reinterpret_cast<__half*>(smem + kOffLut);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -220,6 +231,7 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
     for (int s = 0; s < kPStages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_mma + 8 * s, 1);
+      mbar_init(bar_b + 8 * s, kDqThreads);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_misc[1] = 0;
@@ -239,13 +251,14 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
   tc_fence_after();
   const uint32_t tmem = static_cast<uint32_t>(s_misc[0]);
   const int total = s_start[E];
+  const bool mma_warp = warp == kDqThreads / 32;
 
   // dequant role: tile row and which 32-k half of the K step
-  const int row = tid & 127, half = tid >> 7;
+  const int row = tid & 127, half = (tid >> 7) & 1;
   const uint32_t rowoff = static_cast<uint32_t>(row) * 2u;     // byte offset of the row in a table line
-  uint32_t g = 0;                                              // K steps issued so far (stage ring)
+  uint32_t g = 0;                                              // K steps so far (stage ring), same in every warp
 
-  for (int item = blockIdx.x; item < total && !s_misc[1]; item += gridDim.x) {
+  for (int item = blockIdx.x; item < total; item += gridDim.x) {
     int e = 0;
     while (s_start[e + 1] <= item) ++e;
     const int local = item - s_start[e];
@@ -260,8 +273,59 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
       if (tid == 0) atomicOr(p.status, PW_STATUS_BAD_DESC);
       continue;
     }
-    const int grow = wrow<KIND>(p, nt, row);
+    const uint32_t g0 = g;
 
+    if (mma_warp) {
+      // ---- TMA and MMA issue (one lane): A of step k goes to stage (g0+k)&1 once the
+      // MMAs of step k-2 are done; the MMAs of step k wait for A and for B
+      if (lane == 0 && !s_misc[1]) {
+        auto wait_or_abort = [&](uint32_t bar, uint32_t parity) {
+          if (mbar_wait(bar, parity, s_misc + 1)) return true;
+          atomicOr(p.status, PW_STATUS_TIMEOUT);
+          s_misc[1] = 1;
+          return false;
+        };
+        auto load_a = [&](uint32_t gk, int k) {
+          const uint32_t sa = gk & 1;
+          mbar_expect_tx(bar_full + 8 * sa, nm * kTileBytes);
+          for (int m = 0; m < nm; ++m)
+            tma_load_2d(sbase + kOffA + (sa * kMT + m) * kTileBytes, &tmA, k * kBK, row0 + m * kBM,
+                        bar_full + 8 * sa);
+        };
+        bool ok = true;
+        // step 0's stage was last used by step g0-2: wait for its MMAs
+        if (g0 >= 2) ok = wait_or_abort(bar_mma + 8 * (g0 & 1), ((g0 - 2) >> 1) & 1);
+        if (ok) load_a(g0, 0);
+        for (int ks = 0; ks < nksteps && ok; ++ks) {
+          const uint32_t gk = g0 + ks, s = gk & 1;
+          ok = wait_or_abort(bar_full + 8 * s, (gk >> 1) & 1) && wait_or_abort(bar_b + 8 * s, (gk >> 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t b0 = sbase + kOffB + s * kTileBytes;
+          for (int m = 0; m < nm; ++m) {
+            const uint32_t a0 = sbase + kOffA + (s * kMT + m) * kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_f16(tmem + m * kBN, smem_desc(a0 + kk * 32), smem_desc(b0 + kk * 32), (ks | kk) != 0);
+          }
+          mma_commit(bar_mma + 8 * s);
+          // step ks+1's tokens go to the stage of step ks-1 once its MMAs are done
+          // (step ks's MMAs are queued behind them meanwhile)
+          if (ks + 1 < nksteps) {
+            if (gk >= 1) ok = wait_or_abort(bar_mma + 8 * (s ^ 1), ((gk - 1) >> 1) & 1);
+            if (ok) load_a(gk + 1, ks + 1);
+          }
+        }
+      }
+      __syncwarp();
+      g = g0 + nksteps;
+      continue;
+    }
+
+    // ---- dequantisation (warps 0..7): LUT, plane chunks, one B tile per K step
+    const int grow = wrow<KIND>(p, nt, row);
+    // the previous item's dequant steps and epilogue are done by every dequant thread
+    named_sync_dq();
     // the tile's table: LUT_q[row][v] fp16 -> lut_s[v][row]
     for (int vc = half; vc * 8 < V; vc += 2) {
       uint4 raw = make_uint4(0, 0, 0, 0);
@@ -270,11 +334,9 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) reinterpret_cast<uint16_t*>(lut_s)[(vc * 8 + j) * kBN + row] = hv[j];
     }
-    __syncthreads();
-
     // plane chunks: 16 bytes (4 words = K steps 2j, 2j+1) per row and plane;
     // thread (row, group) copies planes 4*group .. 4*group+3 of its row
-    const int cgrp = tid >> 7;
+    const int cgrp = half;
     auto fetch_chunk = [&](int j) {
       if (grow >= 0 && 2 * j < nksteps) {
         unsigned char* dst = smem + kOffPl + (j & 1) * kPlaneChunkBytes + row * 16;
@@ -291,22 +353,23 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
       }
       asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    const uint32_t g0 = g;
-    if (tid == 0) {   // token tiles of K step 0 (stage g0: free, the previous item's MMAs are done)
-      const int s0 = g0 & 1;
-      mbar_expect_tx(bar_full + 8 * s0, nm * kTileBytes);
-      for (int m = 0; m < nm; ++m)
-        tma_load_2d(sbase + kOffA + (s0 * kMT + m) * kTileBytes, &tmA, 0, row0 + m * kBM, bar_full + 8 * s0);
-    }
     fetch_chunk(0);
     fetch_chunk(1);
     asm volatile("cp.async.wait_group 1;" ::: "memory");
-    __syncthreads();
+    named_sync_dq();          // table and chunk 0 visible to every dequant thread
 
-    for (int ks = 0; ks < nksteps; ++ks, ++g) {
-      const int s = g & 1;
-      const uint32_t use = g >> 1;
-      // dequantise 32 weights of this row into the swizzled B tile
+    const unsigned char* lutb = reinterpret_cast<const unsigned char*>(lut_s);
+    for (int ks = 0; ks < nksteps; ++ks) {
+      const uint32_t gk = g0 + ks, s = gk & 1;
+      // B stage s was last read by the MMAs of step gk-2
+      if (gk >= 2) {
+        if (lane == 0 && !mbar_wait(bar_mma + 8 * s, ((gk - 2) >> 1) & 1, s_misc + 1)) {
+          atomicOr(p.status, PW_STATUS_TIMEOUT);
+          s_misc[1] = 1;
+        }
+        __syncwarp();
+        tc_fence_after();
+      }
       {
         // the row's plane words of this K step and half: word (ks & 1) * 2 + half of
         // the staged 16-byte chunk, plane q-1-r into o[r]
@@ -316,7 +379,6 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
 #pragma unroll
         for (int r = 0; r < 8; ++r) o[r] = (r < Q) ? src[(Q - 1 - r) * (kBM * 4)] : 0u;
         transpose8(o);
-        const unsigned char* lutb = reinterpret_cast<const unsigned char*>(lut_s);
         unsigned char* tileB = smem + kOffB + s * kTileBytes + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
         for (int bb = 0; bb < 4; ++bb) {
@@ -336,93 +398,70 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
         }
       }
       proxy_fence_smem();   // generic-proxy writes of B visible to the tensor core
-      tc_fence_before();
-      __syncthreads();      // B(ks) complete; every thread is done reading the current chunk
-      if (s_misc[1]) break; // a bounded wait gave up: stop issuing work
-      if (ks & 1) fetch_chunk((ks >> 1) + 2);   // both K steps of the chunk done: refill its buffer
-      if (tid == 0) {
-        if (!mbar_wait(bar_full + 8 * s, use & 1)) {
-          atomicOr(p.status, PW_STATUS_TIMEOUT);
-          s_misc[1] = 1;
-        } else {
-          tc_fence_after();
-          const uint32_t b0 = sbase + kOffB + s * kTileBytes;
-          for (int m = 0; m < nm; ++m) {
-            const uint32_t a0 = sbase + kOffA + (s * kMT + m) * kTileBytes;
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-              mma_f16(tmem + m * kBN, smem_desc(a0 + kk * 32), smem_desc(b0 + kk * 32), (ks | kk) != 0);
-          }
-          mma_commit(bar_mma + 8 * s);
-          // stage s^1 frees once the MMAs of step ks-1 finish: then fetch step ks+1's tokens
-          if (ks + 1 < nksteps) {
-            if (g > g0 && !mbar_wait(bar_mma + 8 * (s ^ 1), ((g - 1) >> 1) & 1)) {
-              atomicOr(p.status, PW_STATUS_TIMEOUT);
-              s_misc[1] = 1;
-            } else {
-              mbar_expect_tx(bar_full + 8 * (s ^ 1), nm * kTileBytes);
-              for (int m = 0; m < nm; ++m)
-                tma_load_2d(sbase + kOffA + ((s ^ 1) * kMT + m) * kTileBytes, &tmA, (ks + 1) * kBK,
-                            row0 + m * kBM, bar_full + 8 * (s ^ 1));
-            }
-          }
-        }
+      mbar_arrive(bar_b + 8 * s);
+      if (ks & 1) {
+        // both K steps of chunk ks/2 are read by every thread: refill its buffer with
+        // chunk ks/2 + 2 after chunk ks/2 + 1 has landed and is visible
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        named_sync_dq();
+        fetch_chunk((ks >> 1) + 2);
       }
-      if (ks & 1) asm volatile("cp.async.wait_group 1;" ::: "memory");   // next chunk landed
-      tc_fence_before();
-      __syncthreads();      // B(ks+1)'s buffer is free (step ks-1's MMAs done), next chunk visible
-      tc_fence_after();
     }
+    g = g0 + nksteps;
 
     // ---- epilogue: wait for the tile's last MMAs, then TMEM -> registers -> global
     {
       const uint32_t gl = g - 1;
-      if (tid == 0 && !mbar_wait(bar_mma + 8 * (gl & 1), (gl >> 1) & 1)) {
+      if (lane == 0 && !mbar_wait(bar_mma + 8 * (gl & 1), (gl >> 1) & 1, s_misc + 1)) {
         atomicOr(p.status, PW_STATUS_TIMEOUT);
         s_misc[1] = 1;
       }
-      tc_fence_before();
-      __syncthreads();
+      __syncwarp();
       tc_fence_after();
-      const int lg = warp & 3, ch = warp >> 2;
-      for (int m = 0; m < nm; ++m) {
-        const int tok = m * kBM + lg * 32 + lane;              // TMEM lane = token row of the tile
-        const uint32_t lane_addr = tmem + m * kBN + (static_cast<uint32_t>(lg * 32) << 16);
-        if (KIND == PW_KIND_GATE_UP) {
-          float gv[32], uv[32];
-          tmem_ld32(lane_addr + ch * 32, gv);
-          tmem_ld32(lane_addr + 64 + ch * 32, uv);
-          if (tok < nvalid) {
-            __half* dst = p.hh + static_cast<size_t>(row0 + tok) * p.I + nt * 64 + ch * 32;
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              __half2 h2[4];
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const float a = gv[j + 2 * u], b = gv[j + 2 * u + 1];
-                const float ha = a / (1.f + expf(-a)) * uv[j + 2 * u];
-                const float hb = b / (1.f + expf(-b)) * uv[j + 2 * u + 1];
-                h2[u] = __floats2half2_rn(ha, hb);
-              }
-              *reinterpret_cast<uint4*>(dst + j) = *reinterpret_cast<const uint4*>(h2);
-            }
-          }
-        } else {
-          float yv[32];
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            tmem_ld32(lane_addr + ch * 64 + c * 32, yv);
+      // after an abort (a bounded wait gave up) every wait returns at once and the
+      // accumulators are not read; the status word reports the failure
+      if (!__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(s_misc + 1), 0)) {
+        const int lg = warp & 3, ch = warp >> 2;
+        for (int m = 0; m < nm; ++m) {
+          const int tok = m * kBM + lg * 32 + lane;              // TMEM lane = token row of the tile
+          const uint32_t lane_addr = tmem + m * kBN + (static_cast<uint32_t>(lg * 32) << 16);
+          if (KIND == PW_KIND_GATE_UP) {
+            float gv[32], uv[32];
+            tmem_ld32(lane_addr + ch * 32, gv);
+            tmem_ld32(lane_addr + 64 + ch * 32, uv);
             if (tok < nvalid) {
-              float* dst = p.y + static_cast<size_t>(row0 + tok) * p.H + nt * kBN + ch * 64 + c * 32;
+              __half* dst = p.hh + static_cast<size_t>(row0 + tok) * p.I + nt * 64 + ch * 32;
 #pragma unroll
-              for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(dst + j) = make_float4(yv[j], yv[j + 1], yv[j + 2], yv[j + 3]);
+              for (int j = 0; j < 32; j += 8) {
+                __half2 h2[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const float a = gv[j + 2 * u], b = gv[j + 2 * u + 1];
+                  const float ha = a / (1.f + expf(-a)) * uv[j + 2 * u];
+                  const float hb = b / (1.f + expf(-b)) * uv[j + 2 * u + 1];
+                  h2[u] = __floats2half2_rn(ha, hb);
+                }
+                *reinterpret_cast<uint4*>(dst + j) = *reinterpret_cast<const uint4*>(h2);
+              }
+            }
+          } else {
+            float yv[32];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              tmem_ld32(lane_addr + ch * 64 + c * 32, yv);
+              if (tok < nvalid) {
+                float* dst = p.y + static_cast<size_t>(row0 + tok) * p.H + nt * kBN + ch * 64 + c * 32;
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                  *reinterpret_cast<float4*>(dst + j) = make_float4(yv[j], yv[j + 1], yv[j + 2], yv[j + 3]);
+              }
             }
           }
         }
       }
+      // TMEM reads complete before this thread's next B arrival lets the MMA warp
+      // overwrite the accumulators with the next tile's first MMAs
       tc_fence_before();
-      __syncthreads();   // TMEM reads done before the next tile's first MMA overwrites D
     }
   }
 
