@@ -206,8 +206,9 @@ template <int KIND>
 __global__ void __launch_bounds__(kPThreads, 1)
 k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1 KB-aligned base for the swizzled tiles, derived from the shared array
+  // itself so the compiler keeps every access below in the shared window
+  unsigned char* smem = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = saddr(smem);
   const uint32_t bar_full = sbase + kOffBar;          // [2] TMA of A arrived
   const uint32_t bar_mma = sbase + kOffBar + 16;      // [2] MMAs of the step done (B and A stage free)
@@ -327,12 +328,24 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
     // the previous item's dequant steps and epilogue are done by every dequant thread
     named_sync_dq();
     // the tile's table: LUT_q[row][v] fp16 -> lut_s[v][row]
-    for (int vc = half; vc * 8 < V; vc += 2) {
-      uint4 raw = make_uint4(0, 0, 0, 0);
-      if (grow >= 0) raw = __ldg(reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(grow) * V + vc * 8));
-      const uint16_t* hv = reinterpret_cast<const uint16_t*>(&raw);
+    // four 16-byte loads in flight per thread before their values are stored
+    for (int vc0 = half; vc0 * 8 < V; vc0 += 8) {
+      uint4 raw[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) reinterpret_cast<uint16_t*>(lut_s)[(vc * 8 + j) * kBN + row] = hv[j];
+      for (int u = 0; u < 4; ++u) {
+        const int vc = vc0 + 2 * u;
+        raw[u] = make_uint4(0, 0, 0, 0);
+        if (grow >= 0 && vc * 8 < V)
+          raw[u] = __ldg(reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(grow) * V + vc * 8));
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int vc = vc0 + 2 * u;
+        if (vc * 8 >= V) break;
+        const uint16_t* hv = reinterpret_cast<const uint16_t*>(&raw[u]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) reinterpret_cast<uint16_t*>(lut_s)[(vc * 8 + j) * kBN + row] = hv[j];
+      }
     }
     // plane chunks: 16 bytes (4 words = K steps 2j, 2j+1) per row and plane;
     // thread (row, group) copies planes 4*group .. 4*group+3 of its row
