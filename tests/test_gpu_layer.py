@@ -287,3 +287,56 @@ def test_stats_attach_rejects_bad_alpha():
         with pytest.raises(pw.PWError) as e:
             m.pw_stats_attach(s, a)
         assert e.value.code == pw.PW_EINVAL
+
+
+# ----------------------------------------------------------------------------- edge cases
+
+def test_empty_batch_is_a_no_op():
+    import torch
+    cfg = synth.CONFIGS["tiny"]
+    m = gpu_layer(cfg)
+    x = torch.empty((0, cfg.H), dtype=torch.float16, device="cuda")
+    L = torch.empty((0, cfg.E), dtype=torch.float32, device="cuda")
+    out = m.pw_moe_forward(0, x, L, cfg.top_k, cfg.renorm)
+    torch.cuda.synchronize()
+    assert out.shape == (0, cfg.H)
+    oh = torch.empty((0, cfg.H), dtype=torch.float16).pin_memory()
+    m.pw_moe_forward_host(0, x.cpu().pin_memory(), L.cpu().pin_memory(), cfg.top_k, cfg.renorm, oh)
+
+
+@pytest.mark.parametrize("T", [64, 65])     # the largest fused batch and the first unfused one
+def test_fused_path_boundary(T):
+    cfg = synth.CONFIGS["tiny"].with_(T=T)
+    m = gpu_layer(cfg)
+    x, L = synth.tokens(cfg), synth.logits(cfg)
+    out, ri, rw, ro, rp = _run(m, cfg, x, L)
+    ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg)))
+    _check_routing(ref, ri, rw, ro, rp)
+    assert_close(out, ref["out"])
+
+
+def test_largest_expert_count_and_pair_count():
+    # E = 256 experts (the routing's limit) and T * k = 256 pairs (the fused kernel's limit)
+    cfg = synth.CONFIGS["tiny"].with_(E=256, T=32, top_k=8, H=128, I=128)
+    m = gpu_layer(cfg)
+    x, L = synth.tokens(cfg), synth.logits(cfg)
+    out, ri, rw, ro, rp = _run(m, cfg, x, L)
+    ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg)))
+    _check_routing(ref, ri, rw, ro, rp)
+    assert_close(out, ref["out"])
+
+
+@pytest.mark.parametrize("T", [16, 300])
+def test_every_token_routed_to_one_expert(T):
+    # one expert far above the others takes every token (the hottest-expert extreme):
+    # its tiles carry all T tokens, the others none
+    cfg = synth.CONFIGS["tiny"].with_(T=T)
+    m = gpu_layer(cfg)
+    x = synth.tokens(cfg)
+    L = synth.logits(cfg).copy()
+    L[:, 5] += 40.0
+    out, ri, rw, ro, rp = _run(m, cfg, x, L)
+    ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg)))
+    assert (ref["idx"][:, 0] == 5).all()
+    _check_routing(ref, ri, rw, ro, rp)
+    assert_close(out, ref["out"])
