@@ -421,7 +421,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
     } else if (threadIdx.x == 0) {
       atomicOr(p.status, PW_STATUS_BAD_DESC);
     }
-    __threadfence();   // this thread's h / y writes before the counters below
+    // the h / y writers (threads below kTok * kRows) order their writes before the
+    // counters below; the other threads wrote nothing other CTAs read
+    if (threadIdx.x < kTok * kRows) __threadfence();
     __syncthreads();
     if (gu) {
       if (threadIdx.x == 0) atomicAdd(&expert_done[it.expert], 1);
