@@ -335,7 +335,7 @@ __device__ bool wait_eq(const int* ptr, int want) {
   return false;
 }
 
-// One persistent cooperative launch for the whole decode layer.
+// One persistent launch (the co-resident grid) for the whole decode layer.
 // CTA 0 clears the work-queue counters and publishes a ready epoch at once;
 // every CTA routes the batch itself into shared memory (a few hundred logits,
 // so no CTA waits for another's routing), then takes items from one queue:
@@ -364,15 +364,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
   int* expert_done = p.sync + 2;
   int* tile_done = p.sync + 2 + p.E;
 
+  // The launch lets the next forward on the stream start on SMs this grid frees
+  // (programmatic dependent launch): that forward routes its own batch while
+  // this one finishes, and waits for it before touching the workspace.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) s_int[3] = 0;   // NaN logit seen
+  __syncthreads();
+  route_local(p, r, &s_int[3], kTok);   // reads only logits and descriptors
+  // the previous kernel on the stream (possibly the previous forward, using the
+  // same workspace) has finished and its writes are visible after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (blockIdx.x == 0) {
-    if (threadIdx.x == 0) p.status[0] = 0u;
+    if (threadIdx.x == 0) p.status[0] = s_int[3] ? PW_STATUS_NAN_LOGIT : 0u;
     for (int i = threadIdx.x; i < 1 + p.E + tiles_dn; i += blockDim.x) queue[i] = 0;
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) st_release(p.sync, static_cast<int>(p.epoch));
-  }
-  route_local(p, r, blockIdx.x == 0, kTok);
-  if (blockIdx.x == 0) {   // the routing outputs the caller asked for
+    // the routing outputs the caller asked for
     const int P = p.T * p.k;
     for (int i = threadIdx.x; i < P; i += blockDim.x) {
       if (p.user_idx) p.user_idx[i] = r.idx[i];
@@ -444,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
 }
 
 constexpr int kMaxDevices = 64;
-int g_fused[kMaxDevices] = {};   // cooperative grid of the fused layer per device
+int g_fused[kMaxDevices] = {};   // co-resident grid of the fused layer per device
 
 }  // namespace
 
@@ -463,10 +471,22 @@ cudaError_t launch_layer_fused(const Fwd& p, cudaStream_t s) {
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     g_fused[dev] = per_sm * sms;
   }
-  Fwd arg = p;
-  void* args[] = {&arg};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<void*>(k_layer), dim3(g_fused[dev]),
-                                     dim3(kThreads), args, kSmemBytes, s);
+  // An ordinary launch of exactly the co-resident grid (every wait in the kernel
+  // is on work that a running CTA has already claimed, or on CTA 0, which is
+  // scheduled first), allowed to start while the previous kernel on the stream
+  // finishes (programmatic stream serialisation; the kernel waits for it with
+  // griddepcontrol.wait before it touches the workspace or the token rows).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(g_fused[dev]);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_layer, p);
 }
 
 }  // namespace pw

@@ -165,12 +165,12 @@ __host__ __device__ constexpr int route_smem_bytes() {
 
 // Every CTA of the fused layer computes the same routing on its own (it is a
 // few hundred logits), so no CTA waits for another's results.  Same order of
-// results as route_permute_block.  `report` selects the one CTA that raises the
-// NaN status bit.  Needs T*k <= kRouteSmemMaxPairs and a block of >= 32 threads.
+// results as route_permute_block.  A NaN logit sets *nan_flag (shared memory);
+// the caller raises the status bit.  Needs T*k <= kRouteSmemMaxPairs and a block of >= 32 threads.
 // Top-k and softmax weights of the tokens t = warp, warp + nwarp, ... with
 // NPER logits per lane (E <= 32 * NPER); results into r.idx / r.w.
 template <int NPER>
-__device__ __forceinline__ void route_tokens(const Fwd& p, const RouteSmem& r, bool report) {
+__device__ __forceinline__ void route_tokens(const Fwd& p, const RouteSmem& r, int* nan_flag) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
   const int E = p.E, k = p.k, T = p.T;
   for (int t = warp; t < T; t += nwarp) {
@@ -188,7 +188,7 @@ __device__ __forceinline__ void route_tokens(const Fwd& p, const RouteSmem& r, b
       v[i] = z;
       taken[i] = (e >= E);
     }
-    if (__any_sync(0xffffffffu, nan_seen) && lane == 0 && report) atomicOr(p.status, PW_STATUS_NAN_LOGIT);
+    if (__any_sync(0xffffffffu, nan_seen) && lane == 0) atomicOr(nan_flag, 1);
     float m = -INFINITY;
 #pragma unroll
     for (int i = 0; i < NPER; ++i) m = fmaxf(m, v[i]);
@@ -229,7 +229,7 @@ __device__ __forceinline__ void route_tokens(const Fwd& p, const RouteSmem& r, b
   }
 }
 
-__device__ __forceinline__ void route_local(const Fwd& p, const RouteSmem& r, bool report,
+__device__ __forceinline__ void route_local(const Fwd& p, const RouteSmem& r, int* nan_flag,
                                             int tok_cost) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
   const int E = p.E, k = p.k, T = p.T;
@@ -237,10 +237,10 @@ __device__ __forceinline__ void route_local(const Fwd& p, const RouteSmem& r, bo
     r.qgu[e] = p.desc[desc_index(p.layer, e, PW_KIND_GATE_UP, E)].q;
     r.cnt[e] = 0;
   }
-  if (E <= 32) route_tokens<1>(p, r, report);
-  else if (E <= 64) route_tokens<2>(p, r, report);
-  else if (E <= 128) route_tokens<4>(p, r, report);
-  else route_tokens<8>(p, r, report);
+  if (E <= 32) route_tokens<1>(p, r, nan_flag);
+  else if (E <= 64) route_tokens<2>(p, r, nan_flag);
+  else if (E <= 128) route_tokens<4>(p, r, nan_flag);
+  else route_tokens<8>(p, r, nan_flag);
   __syncthreads();
   for (int i = threadIdx.x; i < T * k; i += blockDim.x) atomicAdd(&r.cnt[r.idx[i]], 1);
   __syncthreads();
