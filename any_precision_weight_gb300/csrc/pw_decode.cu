@@ -137,9 +137,14 @@ __device__ __forceinline__ float* piece(unsigned char* smem, int n) {
   return reinterpret_cast<float*>(smem + n * 256 + 128);
 }
 
+// mode: kTileWhole runs the tile; kTilePrologue only loads the tile's tables and
+// its first stage of plane words (nothing that another kernel writes) and
+// returns; kTileResume runs a tile whose prologue has been done.
+constexpr int kTileWhole = 0, kTilePrologue = 1, kTileResume = 2;
+
 template <int KIND>
 __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsigned char* smem,
-                         const int* perm) {
+                         const int* perm, int mode = kTileWhole) {
   float* lut_s = reinterpret_cast<float*>(smem);
   uint32_t* pl_s = reinterpret_cast<uint32_t*>(smem + kLutBytes);
   __half* x_s = reinterpret_cast<__half*>(smem + kLutBytes + 2 * kPlaneStageBytes);
@@ -166,9 +171,9 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
     const int xt = tid >> 6, xc = tid & 63;         // token staging: thread -> (token, 16 B)
     const __half* trow = (xt < nt) ? token_row<KIND>(p, perm, it.off + t0 + xt, K) : nullptr;
 
-    auto fill = [&](int c, int s) {
+    auto fill = [&](int c, int s, bool planes = true, bool tokens = true) {
       const int wsrc = c * kStageWords + fc * 4;
-      if (fgr >= 0 && wsrc < W) {
+      if (planes && fgr >= 0 && wsrc < W) {
         uint32_t* dst = pl_s + s * (kPlaneStageBytes / 4) + fdst;
 #pragma unroll
         for (int j = 0; j < PW_MAX_BITS / 2; ++j) {   // static indices keep the descriptor in registers
@@ -178,12 +183,13 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
         }
       }
       const int kk = c * kStageK + xc * 8;
-      if (trow && kk < K) cp_async16(x_s + s * (kXStageBytes / 2) + xt * kStageK + xc * 8, trow + kk);
+      if (tokens && trow && kk < K) cp_async16(x_s + s * (kXStageBytes / 2) + xt * kStageK + xc * 8, trow + kk);
       cp_commit();
     };
 
-    fill(0, 0);
-    if (t0 == 0) {
+    const bool first = t0 == 0;
+    fill(0, 0, !(first && mode == kTileResume), !(first && mode == kTilePrologue));
+    if (first && mode != kTileResume) {
       // this tile's tables: LUT_q[row][v] fp16 -> lut_s[v][row] fp32 (overlaps stage 0)
       const int i = tid & 31;
       const int gr = global_row<KIND>(p, it.tile, i);
@@ -206,6 +212,7 @@ __device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsig
         for (int e = 0; e < 8; ++e) lut_s[(vc * 8 + e) * 64 + i] = f[e];
       }
     }
+    if (mode == kTilePrologue) return;
 
     // four independent packed (two-wide fp32) accumulators per token keep the
     // FMA chains short
@@ -371,6 +378,32 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
   if (threadIdx.x == 0) s_int[3] = 0;   // NaN logit seen
   __syncthreads();
   route_local(p, r, &s_int[3], kTok);   // reads only logits and descriptors
+  const int nact = r.lpt[0];
+  const int n_gu = nact * tiles_gu, total = n_gu + nact * tiles_dn;
+  // Every CTA's first item is item blockIdx.x (later ones come from the queue).
+  // A gate_up first item needs only weights, so its tables and first stage of
+  // planes load before the wait below, overlapping the previous kernel's tail.
+  auto make_item = [&](int item, int& kind) {
+    const bool gu = item < n_gu;
+    const int rank = gu ? item / tiles_gu : (item - n_gu) / tiles_dn;
+    Item it;
+    it.expert = r.lpt[1 + rank];
+    it.tile = gu ? item % tiles_gu : (item - n_gu) % tiles_dn;
+    it.n = r.cnt[it.expert];
+    it.off = r.off[it.expert];
+    kind = gu ? PW_KIND_GATE_UP : PW_KIND_DOWN;
+    return it;
+  };
+  int pre_item = -1;
+  if (static_cast<int>(blockIdx.x) < n_gu) {
+    int kind0;
+    const Item it0 = make_item(blockIdx.x, kind0);
+    const BlockDesc d0 = *block_desc(p, it0.expert, kind0);
+    if (d0.q >= 1 && d0.q <= PW_MAX_BITS && d0.K == p.H) {
+      run_tile<PW_KIND_GATE_UP>(p, d0, it0, smem, r.perm, kTilePrologue);
+      pre_item = blockIdx.x;
+    }
+  }
   // the previous kernel on the stream (possibly the previous forward, using the
   // same workspace) has finished and its writes are visible after this
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -397,25 +430,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
       s_int[2] = ok;
     }
     __syncthreads();
-    if (!s_int[2]) return;
+    if (!s_int[2]) {
+      cp_wait<0>();   // no copy of a pre-started tile outlives the CTA
+      return;
+    }
   }
 
-  const int nact = r.lpt[0];
-  const int n_gu = nact * tiles_gu, total = n_gu + nact * tiles_dn;
-  if (threadIdx.x == 0) s_int[0] = atomicAdd(queue, 1);
+  if (threadIdx.x == 0) s_int[0] = blockIdx.x;
   __syncthreads();
   for (int slot = 0;; slot ^= 1) {
     const int item = s_int[slot];
     if (item >= total) break;
-    if (threadIdx.x == 0) s_int[slot ^ 1] = atomicAdd(queue, 1);   // claim the next one now
-    const bool gu = item < n_gu;
-    const int rank = gu ? item / tiles_gu : (item - n_gu) / tiles_dn;
-    Item it;
-    it.expert = r.lpt[1 + rank];
-    it.tile = gu ? item % tiles_gu : (item - n_gu) % tiles_dn;
-    it.n = r.cnt[it.expert];
-    it.off = r.off[it.expert];
-    const int kind = gu ? PW_KIND_GATE_UP : PW_KIND_DOWN;
+    if (threadIdx.x == 0) s_int[slot ^ 1] = atomicAdd(queue, 1) + gridDim.x;   // claim the next one now
+    int kind;
+    const Item it = make_item(item, kind);
+    const bool gu = kind == PW_KIND_GATE_UP;
     const BlockDesc d = *block_desc(p, it.expert, kind);
     const bool ok = d.q >= 1 && d.q <= PW_MAX_BITS && d.K == (gu ? p.H : p.I);
     if (!gu) {
@@ -424,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
       __syncthreads();
     }
     if (ok) {
-      if (gu) run_tile<PW_KIND_GATE_UP>(p, d, it, smem, r.perm);
+      if (gu) run_tile<PW_KIND_GATE_UP>(p, d, it, smem, r.perm, item == pre_item ? kTileResume : kTileWhole);
       else run_tile<PW_KIND_DOWN>(p, d, it, smem, r.perm);
     } else if (threadIdx.x == 0) {
       atomicOr(p.status, PW_STATUS_BAD_DESC);
