@@ -49,6 +49,7 @@ _SIGS = {
     "pw_lut_bytes": (_sz, [_i, _i, _i]),
     "pw_lut_offset": (_sz, [_i, _i, _i]),
     "pw_pack": (_i, [_vp, _i, _i, _i, _vp, _i, _vp, _vp]),
+    "pw_tile_planes": (_i, [_vp, _i, _i, _i, _vp]),
     "pw_desc_bytes": (_sz, [_i, _i]),
     "pw_table_create": (_i, [ctypes.POINTER(_vp), _i, _i, _i, _i, _vp, _sz, _vp]),
     "pw_block_register": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, ctypes.POINTER(_vp), _vp, _i, _vp]),
@@ -158,6 +159,17 @@ def pw_pack(idx: np.ndarray, parent_lut: np.ndarray, n_bits: int = 8, b_min: int
     _check(lib().pw_pack(_ptr(idx), R, K, n_bits, _ptr(par), b_min, _ptr(planes_out),
                          _ptr(luts_out)), "pw_pack")
     return planes_out, luts_out
+
+
+def pw_tile_planes(planes: np.ndarray, out=None):
+    """Reorders pw_pack planes uint32 [n][R][K/32] into the device page layout
+    (returned as a flat uint32 array of the same size, or written into ``out``)."""
+    planes = np.ascontiguousarray(planes, dtype=np.uint32)
+    n, R, W = planes.shape
+    if out is None:
+        out = np.empty(planes.size, dtype=np.uint32)
+    _check(lib().pw_tile_planes(_ptr(planes), n, R, W * 32, _ptr(out)), "pw_tile_planes")
+    return out
 
 
 def pw_profile_attach(events):

@@ -1,31 +1,42 @@
-// Decode-sized dequantised GEMV of the fused APL MoE layer (sm_103a, CUDA cores).
+// Decode-sized fused APL MoE layer (sm_103a): one persistent launch per layer.
 //
 // Source: PagedWeight technical summary, core components section 3 ("Fused
 // Mixed-Precision Kernel": reads APL bit-planes and lookup tables directly,
 // a different committed bitwidth per linear block within one fused operation).
 //
-// Decode batches give each active expert a handful of tokens, so these
-// kernels stream each active block's q bit-planes and q-bit table from HBM
-// exactly once and keep the tokens on chip.  Design:
+// A decode batch gives each active expert a handful of tokens, so the layer
+// streams every active block's q bit-planes and q-bit table from HBM once and
+// keeps the tokens on chip.  What limits such a kernel is the instruction
+// stream that turns plane bits into weights, so the design spends as few
+// instructions per weight as it can:
 //
-//  * persistent CTAs (two per SM) pull (active expert, 32-row tile) items from
-//    a device work queue, so the committed q of each block is read from the
-//    page table on the device and the grid never depends on the routing;
-//  * a tile is 32 rows x all of K; lane l of each of the 8 warps owns row l,
-//    the warps split K; the 32 rows' tables sit in shared memory as fp32
-//    [v][row], so the 32 lanes of a warp always hit 32 different banks,
-//    whatever their indices (conflict-free lookups at every q);
-//  * bit-planes are staged global->shared with cp.async in 16-word (512-k)
-//    chunks, double buffered, with the 16-byte chunks XOR-swizzled by row;
-//    tokens are staged the same way (fp32), two tokens per pass;
-//  * per 32-bit plane word a lane turns the q plane words into 32 q-bit
-//    indices with an 8x8 bit-matrix transpose done four bytes at a time (delta
-//    swaps), then one byte permute per element forms the table address
-//    (index * 256 + row * 4);
-//  * products accumulate in fp32 with packed two-wide FMAs; the eight K-warps'
-//    partial sums are added in a fixed order (deterministic results).
-// gate_up tiles hold 16 gate rows and the 16 matching up rows and finish with
-// h = silu(gate) * up rounded to fp16; down tiles hold 32 rows of y (fp32).
+//  * work items are 64-row tiles of one block (gate_up: 32 gate rows and the
+//    32 matching up rows; down: 64 rows) for one pass of up to four of the
+//    expert's tokens, laid out in a fixed order (largest gate_up cost first,
+//    then all down tiles) and dealt round-robin to the CTAs, so every CTA knows
+//    its next items and loads their descriptors and tables ahead of time;
+//  * lane l of every warp owns two rows of the tile (gate row l and up row l,
+//    or rows l and 32 + l); the eight warps split K.  The two rows' q-bit
+//    tables sit in shared memory as one 32-bit slot per (index, lane) holding
+//    both rows' fp16 entries, so a warp's 32 lookups hit 32 different banks
+//    whatever the indices;
+//  * each warp streams its own plane words through a private three-stage
+//    cp.async ring that runs on into the warp's share of the next item, so
+//    the HBM stream does not stop at item boundaries;
+//  * per 32-bit plane word, a lane turns q plane words into 32 indices with an
+//    8x8 bit transpose (delta swaps), one byte permute per weight forms the
+//    table address, and the looked-up fp16 weights go straight from registers
+//    into the A operand of a warp-level tensor-core MMA (m16n8k16, fp32
+//    accumulate).  The MMA's 16 k-slots are split between the four lanes of a
+//    row group, and the token operand is zero outside each lane's own column
+//    pair, so every lane accumulates the dot products of its own two rows with
+//    two tokens (a second MMA adds tokens 2 and 3).  The MMA does the
+//    multiply-adds that would otherwise cost two fp32 instructions per weight
+//    and token;
+//  * the eight K-warps' partial sums are added in a fixed order (bitwise
+//    deterministic); gate_up items finish with h = silu(gate) * up (fp16),
+//    down items with fp32 y rows; the last down item of a 64-row output tile
+//    combines it.
 
 #include <cuda_fp16.h>
 #include <cstdint>
@@ -36,46 +47,48 @@ namespace pw {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kCtasPerSm = 2;        // two CTAs per SM overlap each other's item start-up
-constexpr int kRows = 32;            // rows per tile: lane l of every warp owns row l
-constexpr int kKW = 8;               // K-warps: each warp takes 2 of a stage's 16 words per row
-constexpr int kStageWords = 16;      // plane words per row per stage
-constexpr int kStageK = kStageWords * 32;
-constexpr int kTok = 2;              // tokens per pass over a tile
-// Shared memory.  The tables take [v][64 slots] fp32 so that one byte permute
-// forms index*256 + row*4; rows use slots 0..31, and the other 128 bytes of
-// every 256-byte line ("pieces") hold the per-warp token scratch and the
-// K-warp partial sums.
-constexpr int kLutBytes = 256 * 64 * 4;
-constexpr int kPlaneStageBytes = PW_MAX_BITS * kRows * kStageWords * 4;
-constexpr int kXStageBytes = kTok * kStageK * 2;            // fp16 tokens
-constexpr int kPieceRed = 0;                                // kKW * kTok pieces
-constexpr int kPieceXw = kPieceRed + kKW * kTok;            // 2 per (warp, token)
-constexpr int kSmemBytes = kLutBytes + 2 * kPlaneStageBytes + 2 * kXStageBytes + route_smem_bytes() + 64;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnitWords = 2;      // plane words per row per ring stage
+constexpr int kStages = 3;         // ring stages per warp
+constexpr int kTokPass = 4;        // tokens per pass over a tile (two MMA column sets)
+constexpr int kGateUpTileRows = 32;   // gate rows per gate_up tile (plus as many up rows)
+constexpr int kDownTileRows = 64;
 
-// The kernel's dynamic shared memory.  Table reads index this symbol directly,
-// so its (link-time constant) shared address folds into the load's immediate
-// offset instead of costing an add per looked-up weight.
+// Shared memory.  Table line v (256 bytes) holds the 32 lanes' slots for index
+// v in its first half; the second halves ("pieces", 128 bytes each) hold the
+// split-K partial sums and the descriptors of the items in flight.
+constexpr int kLine = 256;
+constexpr int kTableBytes = 256 * kLine;
+constexpr int kStageBytes = PW_MAX_BITS * 2 * 32 * 8;   // [plane][row half][lane] x 2 words
+constexpr int kRingOff = kTableBytes;
+constexpr int kRingBytes = kWarps * kStages * kStageBytes;
+constexpr int kRouteOff = kRingOff + kRingBytes;
+constexpr int kCumOff = kRouteOff + route_smem_bytes();
+constexpr int kItemOff = kCumOff + 2 * (kMaxE + 1) * 4;
+constexpr int kSlots = 3;          // items in flight: current, next, the one after
+constexpr int kSmemBytes = kItemOff + 256;
+constexpr int kPieceRed = 0;       // 8 warps x 8 (row half, token) x 32 lanes fp32
+constexpr int kPieceDesc = 64;     // one BlockDesc per item slot
+
 extern __shared__ __align__(128) unsigned char g_smem[];
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst)), "l"(src));
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
-
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void cp_wait_n(int n) {   // n = groups allowed to stay in flight
+  if (n <= 0) cp_wait<0>();
+  else if (n == 1) cp_wait<1>();
+  else cp_wait<2>();
+}
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
   return d;
 }
-
 // (a & ~m) | (b & m) in one three-input logic op.
 __device__ __forceinline__ uint32_t bitsel(uint32_t a, uint32_t b, uint32_t m) {
   uint32_t d;
@@ -90,7 +103,6 @@ __device__ __forceinline__ void delta_swap(uint32_t& lo, uint32_t& hi, int s, ui
   lo = nlo;
   hi = nhi;
 }
-
 // 8x8 bit transposes, four byte lanes at once.  Row r of the input holds plane
 // (q-1-r) (zero for r >= q); after the three rounds, byte bb of o[r] is the
 // q-bit index (plane 0 most significant) of element 8*bb + r.
@@ -106,218 +118,250 @@ __device__ __forceinline__ void planes_to_indices(uint32_t (&o)[8]) {
   for (int r = 0; r < 8; r += 2) delta_swap(o[r], o[r + 1], 1, 0x55555555u);
 }
 
-struct Item {
-  int expert, tile, n, off;
+// Table slot at byte address a (index * 256 + lane * 4).  Indexing the dynamic
+// shared-memory symbol lets its address fold into the load's immediate offset.
+__device__ __forceinline__ uint32_t lut_slot(uint32_t a) {
+  return *reinterpret_cast<const uint32_t*>(g_smem + a);
+}
+
+// D += A * B, m16n8k16, fp16 operands, fp32 accumulators.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 ld_nc16(const void* p) {   // read-only for the kernel's lifetime
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// 128-byte piece n (second half of table line n).
+__device__ __forceinline__ unsigned char* piece(int n) { return g_smem + n * kLine + 128; }
+
+// ------------------------------------------------------------------ work items
+
+struct ItemInfo {
+  int valid, kind, expert, tile;
+  int n;      // tokens of this pass (1..4)
+  int off;    // permuted position of the pass's first token
+  int need;   // down: gate_up items of the expert that must be done first
+  int pad;
 };
 
-// Global row of tile row i: gate_up tiles are 16 gate rows + the 16 matching
-// up rows; down tiles are 32 consecutive rows.  Returns -1 past the block.
-template <int KIND>
-__device__ __forceinline__ int global_row(const Fwd& p, int tile, int i) {
-  if (KIND == PW_KIND_GATE_UP) {
-    const int r = tile * 16 + (i & 15);
-    if (r >= p.I) return -1;
-    return (i < 16) ? r : p.I + r;
+struct Plan {
+  int nact, tiles_gu, tiles_dn, total_gu, total, down_per_tile;
+  const int* cum_gu;   // [nact+1] first gate_up item of each cost rank
+  const int* cum_dn;
+};
+
+// Item g of the layer's fixed order: gate_up items (experts by cost rank; per
+// expert pass-major, then tile), then down items in the same expert order.
+__device__ ItemInfo item_of(int g, const Plan& pl, const RouteSmem& r) {
+  ItemInfo it{};
+  if (g < 0 || g >= pl.total) return it;
+  const bool gu = g < pl.total_gu;
+  const int* cum = gu ? pl.cum_gu : pl.cum_dn;
+  const int gg = gu ? g : g - pl.total_gu;
+  int lo = 0, hi = pl.nact - 1;   // last rank whose first item is <= gg
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cum[mid] <= gg) lo = mid;
+    else hi = mid - 1;
+  }
+  const int tiles = gu ? pl.tiles_gu : pl.tiles_dn;
+  const int rem = gg - cum[lo];
+  const int e = r.lpt[1 + lo];
+  const int pass = rem / tiles;
+  const int cnt = r.cnt[e];
+  it.valid = 1;
+  it.kind = gu ? PW_KIND_GATE_UP : PW_KIND_DOWN;
+  it.expert = e;
+  it.tile = rem % tiles;
+  it.n = min(kTokPass, cnt - pass * kTokPass);
+  it.off = r.off[e] + pass * kTokPass;
+  it.need = pl.tiles_gu * ((cnt + kTokPass - 1) / kTokPass);
+  return it;
+}
+
+// Rows of lane l in a tile: rho (first half) and rho2 (second half).
+__device__ __forceinline__ void lane_rows(const Fwd& p, const ItemInfo& it, int lane, int& rho, int& rho2) {
+  if (it.kind == PW_KIND_GATE_UP) {
+    rho = it.tile * kGateUpTileRows + lane;
+    rho2 = p.I + rho;
   } else {
-    const int r = tile * kRows + i;
-    return (r < p.H) ? r : -1;
+    rho = it.tile * kDownTileRows + lane;
+    rho2 = rho + 32;
   }
 }
 
-// fp16 input row of permuted position pos: the token's x for gate_up, the
-// pair's h for down.  perm may live in global or shared memory.
-template <int KIND>
-__device__ __forceinline__ const __half* token_row(const Fwd& p, const int* perm, int pos, int K) {
-  if (KIND == PW_KIND_GATE_UP) return p.x + static_cast<size_t>(perm[pos] / p.k) * K;
-  return p.hh + static_cast<size_t>(pos) * K;
+// A descriptor is usable when its bitwidth and shape match the layer.
+__device__ __forceinline__ bool desc_ok(const Fwd& p, const BlockDesc& d, int kind) {
+  const bool gu = kind == PW_KIND_GATE_UP;
+  return d.q >= 1 && d.q <= PW_MAX_BITS && d.K == (gu ? p.H : p.I) && d.R == (gu ? 2 * p.I : p.H);
 }
 
-// 128-byte piece n of the tables' unused half.
-__device__ __forceinline__ float* piece(unsigned char* smem, int n) {
-  return reinterpret_cast<float*>(smem + n * 256 + 128);
+// This warp's plane-word units (2 words each) of an item: [u0, u1).
+__device__ __forceinline__ void warp_units(const BlockDesc& d, bool ok, int warp, int& u0, int& u1) {
+  const int U = ok ? (d.K >> 6) : 0;
+  u0 = U * warp / kWarps;
+  u1 = U * (warp + 1) / kWarps;
 }
 
-// mode: kTileWhole runs the tile; kTilePrologue only loads the tile's tables and
-// its first stage of plane words (nothing that another kernel writes) and
-// returns; kTileResume runs a tile whose prologue has been done.
-constexpr int kTileWhole = 0, kTilePrologue = 1, kTileResume = 2;
+// ------------------------------------------------------------------ tables
 
-template <int KIND>
-__device__ void run_tile(const Fwd& p, const BlockDesc& d, const Item& it, unsigned char* smem,
-                         const int* perm, int mode = kTileWhole) {
-  float* lut_s = reinterpret_cast<float*>(smem);
-  uint32_t* pl_s = reinterpret_cast<uint32_t*>(smem + kLutBytes);
-  __half* x_s = reinterpret_cast<__half*>(smem + kLutBytes + 2 * kPlaneStageBytes);
+// The next item's two table rows per lane, held in registers while the
+// current item runs: thread (lane, wv) owns 8-entry chunks wv, wv+8, ...
+struct LutRegs {
+  uint4 a[4], b[4];
+};
 
-  const int tid = threadIdx.x, lane = tid & 31, kw = tid >> 5;
-  const int K = d.K, W = K >> 5;
-  const int Q = d.q, V = 1 << Q;
-  const int nchunk = (W + kStageWords - 1) / kStageWords;
-
-  // plane staging: threads 0..127 and 128..255 each cover the 32 rows x four
-  // 16-byte chunks, taking even and odd planes; chunks are XOR-swizzled by row
-  const int fr = (tid & 127) >> 2, fc = tid & 3, fpl = tid >> 7;
-  const int fgr = global_row<KIND>(p, it.tile, fr);
-  const int fdst = fr * kStageWords + ((fc ^ ((fr >> 1) & 3)) * 4);
-  const size_t fsrc = (fgr >= 0 ? static_cast<size_t>(fgr) * W : 0) + fc * 4;
-
-  const int row = lane;
-  const uint32_t laneoff = static_cast<uint32_t>(row) * 4u;
-  const int rsw = (((kw >> 1) ^ ((row >> 1) & 3)) * 4) + (kw & 1) * 2;
-  const unsigned char* lut_bytes = g_smem;   // lut_s == g_smem
-
-  for (int t0 = 0; t0 < it.n; t0 += kTok) {
-    const int nt = min(kTok, it.n - t0);
-    const int xt = tid >> 6, xc = tid & 63;         // token staging: thread -> (token, 16 B)
-    const __half* trow = (xt < nt) ? token_row<KIND>(p, perm, it.off + t0 + xt, K) : nullptr;
-
-    auto fill = [&](int c, int s, bool planes = true, bool tokens = true) {
-      const int wsrc = c * kStageWords + fc * 4;
-      if (planes && fgr >= 0 && wsrc < W) {
-        uint32_t* dst = pl_s + s * (kPlaneStageBytes / 4) + fdst;
+__device__ __forceinline__ void lut_load(LutRegs& f, const BlockDesc& d, int rho, int rho2, int wv) {
+  const int q = d.q, V = 1 << q;
+  if (V >= 8) {
+    const uint4* ra = reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(rho) * V);
+    const uint4* rb = reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(rho2) * V);
 #pragma unroll
-        for (int j = 0; j < PW_MAX_BITS / 2; ++j) {   // static indices keep the descriptor in registers
-          const int pl = 2 * j + fpl;
-          const uint32_t* src = fpl ? d.planes[2 * j + 1] : d.planes[2 * j];
-          if (pl < Q) cp_async16(dst + pl * kRows * kStageWords, src + fsrc + c * kStageWords);
-        }
-      }
-      const int kk = c * kStageK + xc * 8;
-      if (tokens && trow && kk < K) cp_async16(x_s + s * (kXStageBytes / 2) + xt * kStageK + xc * 8, trow + kk);
-      cp_commit();
-    };
-
-    const bool first = t0 == 0;
-    fill(0, 0, !(first && mode == kTileResume), !(first && mode == kTilePrologue));
-    if (first && mode != kTileResume) {
-      // this tile's tables: LUT_q[row][v] fp16 -> lut_s[v][row] fp32 (overlaps stage 0)
-      const int i = tid & 31;
-      const int gr = global_row<KIND>(p, it.tile, i);
-      for (int vc = tid >> 5; vc * 8 < V; vc += kThreads / 32) {
-        float f[8];
-        if (gr >= 0) {
-          const uint4 raw = __ldg(reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(gr) * V + vc * 8));
-          const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 ff = __half22float2(h2[e]);
-            f[2 * e] = ff.x;
-            f[2 * e + 1] = ff.y;
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] = 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) lut_s[(vc * 8 + e) * 64 + i] = f[e];
+    for (int j = 0; j < 4; ++j) {
+      const int vc = wv + 8 * j;
+      if (vc * 8 < V) {
+        f.a[j] = ld_nc16(ra + vc);
+        f.b[j] = ld_nc16(rb + vc);
       }
     }
-    if (mode == kTilePrologue) return;
+  } else if (wv == 0) {   // 2 or 4 entries per row
+    uint32_t wa[2] = {0u, 0u}, wb[2] = {0u, 0u};
+    const uint32_t* ra = reinterpret_cast<const uint32_t*>(d.lut + static_cast<size_t>(rho) * V);
+    const uint32_t* rb = reinterpret_cast<const uint32_t*>(d.lut + static_cast<size_t>(rho2) * V);
+    for (int w = 0; w < V / 2; ++w) {
+      wa[w] = __ldg(ra + w);
+      wb[w] = __ldg(rb + w);
+    }
+    f.a[0] = make_uint4(wa[0], wa[1], 0u, 0u);
+    f.b[0] = make_uint4(wb[0], wb[1], 0u, 0u);
+  }
+}
 
-    // four independent packed (two-wide fp32) accumulators per token keep the
-    // FMA chains short
-    float2 acc[kTok][4];
+// Slot (v, lane) = (row rho entry v) | (row rho2 entry v) << 16.
+__device__ __forceinline__ void lut_store(const LutRegs& f, int q, int lane, int wv) {
+  const int V = 1 << q;
 #pragma unroll
-    for (int t = 0; t < kTok; ++t)
+  for (int j = 0; j < 4; ++j) {
+    const int vc = wv + 8 * j;
+    if (vc * 8 < V || (j == 0 && vc == 0)) {
+      const uint32_t aw[4] = {f.a[j].x, f.a[j].y, f.a[j].z, f.a[j].w};
+      const uint32_t bw[4] = {f.b[j].x, f.b[j].y, f.b[j].z, f.b[j].w};
 #pragma unroll
-      for (int m = 0; m < 4; ++m) acc[t][m] = make_float2(0.f, 0.f);
-
-    // one barrier per stage: it publishes stage c and proves every warp is done
-    // with stage c-1, whose buffer the fill for stage c+1 then reuses
-    for (int c = 0; c < nchunk; ++c) {
-      const int s = c & 1;
-      cp_wait<0>();
-      __syncthreads();
-      if (c + 1 < nchunk) fill(c + 1, s ^ 1);
-
-      const int wbase = c * kStageWords + kw * 2;
-      const int nw = min(2, W - wbase);
-      if (nw > 0) {
-        // this warp's 64 token values of the stage, fp16 -> fp32 scratch
-        __syncwarp();
-#pragma unroll
-        for (int t = 0; t < kTok; ++t) {
-          if (t < nt) {
-            const __half2 h2 = reinterpret_cast<const __half2*>(x_s + s * (kXStageBytes / 2) + t * kStageK + kw * 64)[lane];
-            *reinterpret_cast<float2*>(piece(smem, kPieceXw + 2 * (kw * kTok + t) + (lane >> 4)) + ((2 * lane) & 31)) =
-                __half22float2(h2);
-          }
-        }
-        __syncwarp();
-        const uint32_t* ps = pl_s + s * (kPlaneStageBytes / 4) + row * kStageWords + rsw;
-        uint2 pv[PW_MAX_BITS];
-#pragma unroll
-        for (int pl = 0; pl < PW_MAX_BITS; ++pl)   // pv[r] = plane (q-1-r)
-          pv[pl] = (pl < Q) ? *reinterpret_cast<const uint2*>(ps + (Q - 1 - pl) * kRows * kStageWords)
-                            : make_uint2(0u, 0u);
-#pragma unroll
-        for (int wi = 0; wi < 2; ++wi) {
-          if (wi < nw) {
-            uint32_t o[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) o[r] = wi == 0 ? pv[r].x : pv[r].y;
-            planes_to_indices(o);
-            // eight weights at a time (byte lane bb of the transposed words),
-            // each multiplied into every token of the pass before the next eight
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb) {
-              float w8[8];
-#pragma unroll
-              for (int r = 0; r < 8; ++r) {
-                const uint32_t a = prmt(o[r], laneoff, 0x5504u | (static_cast<uint32_t>(bb) << 4));
-                w8[r] = *reinterpret_cast<const float*>(lut_bytes + a);
-              }
-#pragma unroll
-              for (int t = 0; t < kTok; ++t) {
-                if (t < nt) {
-                  const float4* xr = reinterpret_cast<const float4*>(piece(smem, kPieceXw + 2 * (kw * kTok + t) + wi));
-                  const float4 x0 = xr[2 * bb], x1 = xr[2 * bb + 1];
-                  acc[t][0] = __ffma2_rn(make_float2(w8[0], w8[1]), make_float2(x0.x, x0.y), acc[t][0]);
-                  acc[t][1] = __ffma2_rn(make_float2(w8[2], w8[3]), make_float2(x0.z, x0.w), acc[t][1]);
-                  acc[t][2] = __ffma2_rn(make_float2(w8[4], w8[5]), make_float2(x1.x, x1.y), acc[t][2]);
-                  acc[t][3] = __ffma2_rn(make_float2(w8[6], w8[7]), make_float2(x1.z, x1.w), acc[t][3]);
-                }
-              }
-            }
-          }
+      for (int e = 0; e < 4; ++e) {
+        const int v = vc * 8 + 2 * e;
+        if (v < V) {
+          *reinterpret_cast<uint32_t*>(g_smem + v * kLine + lane * 4) = prmt(aw[e], bw[e], 0x5410u);
+          *reinterpret_cast<uint32_t*>(g_smem + (v + 1) * kLine + lane * 4) = prmt(aw[e], bw[e], 0x7632u);
         }
       }
     }
+  }
+}
 
-    // ---- partial sums of the eight K-warps, added in a fixed order
+// ------------------------------------------------------------------ inner loop
+
+// 16 bytes of a token row into x when pred is set (x keeps its value otherwise).
+__device__ __forceinline__ void ld_x16(uint4& x, const void* ptr, bool pred) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " @p ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%5];\n}"
+      : "+r"(x.x), "+r"(x.y), "+r"(x.z), "+r"(x.w)
+      : "r"(static_cast<int>(pred)), "l"(ptr));
+}
+
+// One plane word (32 k) of the lane's two rows into the accumulators.
+// o0 / o1: transposed indices of rho / rho2 (byte bb of o[r] = element 8bb + r);
+// X0 / X1: token operand of the word for column sets 0 / 1, refilled with the
+// next word's (x0n / x1n + 16 bytes per bb, when `more`) as each part is used.
+__device__ __forceinline__ void word_mma(const uint32_t (&o0)[8], const uint32_t (&o1)[8], uint32_t laneoff,
+                                         uint4 (&X0)[4], uint4 (&X1)[4], const uint4* x0n, const uint4* x1n,
+                                         bool p0, bool p1, float (&acc)[2][2][4]) {
 #pragma unroll
-    for (int t = 0; t < kTok; ++t)
-      if (t < nt)
-        piece(smem, kPieceRed + kw * kTok + t)[row] =
-            ((acc[t][0].x + acc[t][0].y) + (acc[t][1].x + acc[t][1].y)) +
-            ((acc[t][2].x + acc[t][2].y) + (acc[t][3].x + acc[t][3].y));
-    __syncthreads();
-    if (KIND == PW_KIND_GATE_UP) {
-      if (tid < nt * 16) {
-        const int t = tid >> 4, i = tid & 15;
-        const int r = it.tile * 16 + i;
-        float g = 0.f, u = 0.f;
+  for (int bb = 0; bb < 4; ++bb) {
+    const uint32_t sel = 0x5504u | (static_cast<uint32_t>(bb) << 4);
+    uint32_t s[8], t[8];
 #pragma unroll
-        for (int w8 = 0; w8 < kKW; ++w8) {
-          g += piece(smem, kPieceRed + w8 * kTok + t)[i];
-          u += piece(smem, kPieceRed + w8 * kTok + t)[16 + i];
-        }
-        if (r < p.I) {
-          const float hv = g / (1.f + expf(-g)) * u;
-          p.hh[static_cast<size_t>(it.off + t0 + t) * p.I + r] = __float2half_rn(hv);
-        }
-      }
-    } else {
-      if (tid < nt * kRows) {
-        const int t = tid >> 5, i = tid & 31;
-        const int r = it.tile * kRows + i;
-        float yv = 0.f;
+    for (int r = 0; r < 8; ++r) {
+      s[r] = lut_slot(prmt(o0[r], laneoff, sel));
+      t[r] = lut_slot(prmt(o1[r], laneoff, sel));
+    }
 #pragma unroll
-        for (int w8 = 0; w8 < kKW; ++w8) yv += piece(smem, kPieceRed + w8 * kTok + t)[i];
-        if (r < p.H) p.y[static_cast<size_t>(it.off + t0 + t) * p.H + r] = yv;
+    for (int hh = 0; hh < 2; ++hh) {
+      // k-slots (2c, 2c+1) <- elements 8bb+4hh+{0,1}; (2c+8, 2c+9) <- +{2,3}
+      uint32_t a[4];
+      a[0] = prmt(s[4 * hh + 0], s[4 * hh + 1], 0x5410u);   // row rho
+      a[1] = prmt(t[4 * hh + 0], t[4 * hh + 1], 0x7632u);   // row rho2
+      a[2] = prmt(s[4 * hh + 2], s[4 * hh + 3], 0x5410u);
+      a[3] = prmt(t[4 * hh + 2], t[4 * hh + 3], 0x7632u);
+      mma16816(acc[0][hh], a, hh ? X0[bb].z : X0[bb].x, hh ? X0[bb].w : X0[bb].y);
+      mma16816(acc[1][hh], a, hh ? X1[bb].z : X1[bb].x, hh ? X1[bb].w : X1[bb].y);
+    }
+    ld_x16(X0[bb], x0n + bb, p0);
+    ld_x16(X1[bb], x1n + bb, p1);
+  }
+}
+
+// Where the warp's ring fetch stands: item (this CTA's local index), unit,
+// end of the warp's units in that item, and what issuing a unit needs.  A unit
+// is one word pair (64 k) of the tile's two 32-row groups; in the page layout
+// each (plane, group, word pair) is 256 contiguous bytes, so lane l copies 16
+// bytes: rows 2(l%16), 2(l%16)+1 of group l/16.
+struct Fetch {
+  int item, u, end, q;
+  size_t off;        // page word offset of this lane's 16 bytes at unit 0
+  uint32_t desc;     // shared address of the item's descriptor
+};
+
+__device__ __forceinline__ void fetch_enter(Fetch& f, const Fwd& p, int item, int warp, int lane) {
+  const int sl = item % kSlots;
+  const ItemInfo& it = reinterpret_cast<const ItemInfo*>(g_smem + kItemOff)[sl];
+  const BlockDesc& d = *reinterpret_cast<const BlockDesc*>(piece(kPieceDesc + sl));
+  f.item = item;
+  f.desc = smem_addr(&d);
+  const bool ok = it.valid && desc_ok(p, d, it.kind);
+  warp_units(d, ok, warp, f.u, f.end);
+  const int h = lane >> 4;
+  int grp;   // 32-row group of row half h
+  if (it.kind == PW_KIND_GATE_UP) grp = h ? p.I / 32 + it.tile : it.tile;
+  else grp = 2 * it.tile + h;
+  f.q = d.q;
+  f.off = static_cast<size_t>(grp) * static_cast<size_t>(d.K >> 6) * 64 + (lane & 15) * 4;
+}
+
+// Issues ring stages until kStages units are in flight or the next unit
+// belongs to an item whose descriptor is not in shared memory yet
+// (items up to `known`).  `issued` counts units issued by this warp.  The
+// caller has synchronised the warp after the last read of the stage that the
+// next issue overwrites.
+__device__ __forceinline__ void fetch_fill(Fetch& f, const Fwd& p, int n_items, int known, int consumed,
+                                           int& issued, int warp, int lane, uint32_t ring) {
+  while (issued < consumed + kStages) {
+    while (f.u == f.end) {   // the warp has no more units in this item
+      if (f.item + 1 > known || f.item + 1 >= n_items) return;
+      fetch_enter(f, p, f.item + 1, warp, lane);
+    }
+    const uint32_t dst = ring + (issued % kStages) * kStageBytes + (lane >> 4) * 256 + (lane & 15) * 16;
+    const size_t w = f.off + static_cast<size_t>(f.u) * 64;
+#pragma unroll
+    for (int pl = 0; pl < PW_MAX_BITS; ++pl) {
+      if (pl < f.q) {
+        uint64_t base;
+        asm volatile("ld.shared.u64 %0, [%1];" : "=l"(base) : "r"(f.desc + pl * 8));
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(base) + w;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + pl * 512), "l"(src) : "memory");
       }
     }
-    __syncthreads();
+    cp_commit();
+    ++issued;
+    ++f.u;
   }
 }
 
@@ -333,7 +377,8 @@ __device__ __forceinline__ int ld_acquire(const int* ptr) {
 __device__ __forceinline__ void st_release(int* ptr, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
-// Bounded wait (one thread): true once *ptr == want, false when the limit runs out.
+// Bounded waits (one thread): true once *ptr == want (resp. >= want), false
+// when the limit runs out.
 __device__ bool wait_eq(const int* ptr, int want) {
   for (int i = 0; i < kSpinLimit; ++i) {
     if (ld_acquire(ptr) == want) return true;
@@ -341,20 +386,25 @@ __device__ bool wait_eq(const int* ptr, int want) {
   }
   return false;
 }
+__device__ bool wait_ge(const int* ptr, int want) {
+  for (int i = 0; i < kSpinLimit; ++i) {
+    if (ld_acquire(ptr) >= want) return true;
+    __nanosleep(64);
+  }
+  return false;
+}
 
-// One persistent launch (the co-resident grid) for the whole decode layer.
-// CTA 0 clears the work-queue counters and publishes a ready epoch at once;
-// every CTA routes the batch itself into shared memory (a few hundred logits,
-// so no CTA waits for another's routing), then takes items from one queue:
-// first all (expert, gate_up tile) items, largest gate_up cost first, then all
-// (expert, down tile) items in the same expert order.  A down item first waits
-// until its expert's gate_up tiles are all done; the last down item of a
-// 32-row tile of H (over all active experts) combines that tile's output rows.
-// Every wait is bounded and reports PW_STATUS_TIMEOUT instead of hanging.
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
-  unsigned char* smem = g_smem;
-  int* s_int = reinterpret_cast<int*>(smem + kSmemBytes - 64);
-  int* rs = reinterpret_cast<int*>(smem + kLutBytes + 2 * kPlaneStageBytes + 2 * kXStageBytes);
+// One persistent launch (one CTA per SM, the co-resident grid) for the whole
+// decode layer.  Every CTA routes the batch itself into shared memory (a few
+// hundred logits, so no CTA waits for another's routing) and derives the
+// layer's item order from it; CTA b takes items b, b + G, b + 2G, ...  Down
+// items wait until their expert's gate_up items are done (all gate_up items
+// precede all down items, and no CTA waits while it still holds a gate_up
+// item, so the waits end); the last down item of a 64-row output tile combines
+// it.  Every wait is bounded and reports PW_STATUS_TIMEOUT instead of hanging.
+__global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int* rs = reinterpret_cast<int*>(g_smem + kRouteOff);
   RouteSmem r;
   r.idx = rs;
   r.w = reinterpret_cast<float*>(rs + kRouteSmemMaxPairs);
@@ -365,9 +415,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
   r.act = r.off + (kMaxE + 1);
   r.lpt = r.act + (kMaxE + 1);
   r.qgu = r.lpt + (kMaxE + 1);
+  int* cum_gu = reinterpret_cast<int*>(g_smem + kCumOff);
+  int* cum_dn = cum_gu + (kMaxE + 1);
+  ItemInfo* s_item = reinterpret_cast<ItemInfo*>(g_smem + kItemOff);
+  int* s_int = reinterpret_cast<int*>(s_item + kSlots);
 
-  const int tiles_gu = p.I / 16, tiles_dn = (p.H + kRows - 1) / kRows;
-  int* queue = p.sync + 1;
+  Plan pl;
+  pl.tiles_gu = p.I / kGateUpTileRows;
+  pl.tiles_dn = p.H / kDownTileRows;
   int* expert_done = p.sync + 2;
   int* tile_done = p.sync + 2 + p.E;
 
@@ -375,109 +430,256 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_layer(Fwd p) {
   // (programmatic dependent launch): that forward routes its own batch while
   // this one finishes, and waits for it before touching the workspace.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) s_int[3] = 0;   // NaN logit seen
+  if (tid == 0) s_int[0] = 0;   // NaN logit seen
   __syncthreads();
-  route_local(p, r, &s_int[3], kTok);   // reads only logits and descriptors
-  const int nact = r.lpt[0];
-  const int n_gu = nact * tiles_gu, total = n_gu + nact * tiles_dn;
-  // Every CTA's first item is item blockIdx.x (later ones come from the queue).
-  // A gate_up first item needs only weights, so its tables and first stage of
-  // planes load before the wait below, overlapping the previous kernel's tail.
-  auto make_item = [&](int item, int& kind) {
-    const bool gu = item < n_gu;
-    const int rank = gu ? item / tiles_gu : (item - n_gu) / tiles_dn;
-    Item it;
-    it.expert = r.lpt[1 + rank];
-    it.tile = gu ? item % tiles_gu : (item - n_gu) % tiles_dn;
-    it.n = r.cnt[it.expert];
-    it.off = r.off[it.expert];
-    kind = gu ? PW_KIND_GATE_UP : PW_KIND_DOWN;
-    return it;
-  };
-  int pre_item = -1;
-  if (static_cast<int>(blockIdx.x) < n_gu) {
-    int kind0;
-    const Item it0 = make_item(blockIdx.x, kind0);
-    const BlockDesc d0 = *block_desc(p, it0.expert, kind0);
-    if (d0.q >= 1 && d0.q <= PW_MAX_BITS && d0.K == p.H) {
-      run_tile<PW_KIND_GATE_UP>(p, d0, it0, smem, r.perm, kTilePrologue);
-      pre_item = blockIdx.x;
+  route_local(p, r, &s_int[0], kTokPass);   // reads only logits and descriptors
+  pl.nact = r.lpt[0];
+  if (warp == 0) {   // items per cost rank: tiles x passes; exclusive scan
+    int run = 0;
+    for (int a0 = 0; a0 <= pl.nact; a0 += 32) {
+      const int a = a0 + lane;
+      const int np = a < pl.nact ? (r.cnt[r.lpt[1 + a]] + kTokPass - 1) / kTokPass : 0;
+      int incl = np;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (a <= pl.nact) {
+        cum_gu[a] = (run + incl - np) * pl.tiles_gu;
+        cum_dn[a] = (run + incl - np) * pl.tiles_dn;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
+  __syncthreads();
+  pl.cum_gu = cum_gu;
+  pl.cum_dn = cum_dn;
+  pl.total_gu = cum_gu[pl.nact];
+  pl.total = pl.total_gu + cum_dn[pl.nact];
+  pl.down_per_tile = pl.tiles_dn > 0 ? cum_dn[pl.nact] / pl.tiles_dn : 0;
+  const int G = gridDim.x, b = blockIdx.x;
+  const int n_items = b < pl.total ? (pl.total - 1 - b) / G + 1 : 0;
+
+  // Items 0 and 1 of this CTA and their descriptors; item 0's tables and the
+  // first ring stages load before the dependency wait (weights only).
+  if (tid < 2) s_item[tid] = item_of(b + tid * G, pl, r);
+  __syncthreads();
+  if (warp == 0 && lane < 16) {
+    const int sl = lane >> 3, part = lane & 7;
+    if (s_item[sl].valid) {
+      const uint4* src = reinterpret_cast<const uint4*>(block_desc(p, s_item[sl].expert, s_item[sl].kind));
+      reinterpret_cast<uint4*>(piece(kPieceDesc + sl))[part] = ld_nc16(src + part);
+    }
+  }
+  __syncthreads();
+  const uint32_t ring = smem_addr(g_smem + kRingOff) + warp * (kStages * kStageBytes);
+  const uint32_t laneoff = static_cast<uint32_t>(lane) * 4u;
+  Fetch f;
+  int issued = 0, consumed = 0;
+  LutRegs lr;
+  if (n_items > 0) {
+    const BlockDesc& d0 = *reinterpret_cast<const BlockDesc*>(piece(kPieceDesc));
+    int rho, rho2;
+    lane_rows(p, s_item[0], lane, rho, rho2);
+    if (desc_ok(p, d0, s_item[0].kind)) {
+      lut_load(lr, d0, rho, rho2, warp);
+      lut_store(lr, d0.q, lane, warp);
+    }
+    fetch_enter(f, p, 0, warp, lane);
+    fetch_fill(f, p, n_items, 1, consumed, issued, warp, lane, ring);
+  }
+
   // the previous kernel on the stream (possibly the previous forward, using the
   // same workspace) has finished and its writes are visible after this
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (blockIdx.x == 0) {
-    if (threadIdx.x == 0) p.status[0] = s_int[3] ? PW_STATUS_NAN_LOGIT : 0u;
-    for (int i = threadIdx.x; i < 1 + p.E + tiles_dn; i += blockDim.x) queue[i] = 0;
+  if (b == 0) {
+    if (tid == 0) p.status[0] = s_int[0] ? PW_STATUS_NAN_LOGIT : 0u;
+    for (int i = tid; i < 1 + p.E + pl.tiles_dn; i += blockDim.x) p.sync[1 + i] = 0;
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) st_release(p.sync, static_cast<int>(p.epoch));
+    if (tid == 0) st_release(p.sync, static_cast<int>(p.epoch));
     // the routing outputs the caller asked for
     const int P = p.T * p.k;
-    for (int i = threadIdx.x; i < P; i += blockDim.x) {
+    for (int i = tid; i < P; i += blockDim.x) {
       if (p.user_idx) p.user_idx[i] = r.idx[i];
       if (p.user_w) p.user_w[i] = r.w[i];
       if (p.user_perm) p.user_perm[i] = r.perm[i];
     }
     if (p.user_offsets)
-      for (int e = threadIdx.x; e <= p.E; e += blockDim.x) p.user_offsets[e] = r.off[e];
+      for (int e = tid; e <= p.E; e += blockDim.x) p.user_offsets[e] = r.off[e];
     update_route_stats(p, r.perm, r.w, r.off);
   } else {
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
       const bool ok = wait_eq(p.sync, static_cast<int>(p.epoch));
       if (!ok) atomicOr(p.status, PW_STATUS_TIMEOUT);
       s_int[2] = ok;
     }
     __syncthreads();
     if (!s_int[2]) {
-      cp_wait<0>();   // no copy of a pre-started tile outlives the CTA
+      cp_wait<0>();   // no copy outlives the CTA
       return;
     }
   }
+  __syncthreads();   // the prologue's tables are complete
 
-  if (threadIdx.x == 0) s_int[0] = blockIdx.x;
-  __syncthreads();
-  for (int slot = 0;; slot ^= 1) {
-    const int item = s_int[slot];
-    if (item >= total) break;
-    if (threadIdx.x == 0) s_int[slot ^ 1] = atomicAdd(queue, 1) + gridDim.x;   // claim the next one now
-    int kind;
-    const Item it = make_item(item, kind);
-    const bool gu = kind == PW_KIND_GATE_UP;
-    const BlockDesc d = *block_desc(p, it.expert, kind);
-    const bool ok = d.q >= 1 && d.q <= PW_MAX_BITS && d.K == (gu ? p.H : p.I);
-    if (!gu) {
-      if (threadIdx.x == 0 && !wait_eq(&expert_done[it.expert], tiles_gu))
-        atomicOr(p.status, PW_STATUS_TIMEOUT);
-      __syncthreads();
+  for (int i = 0; i < n_items; ++i) {
+    const int sl = i % kSlots;
+    const ItemInfo it = s_item[sl];
+    const BlockDesc& d = *reinterpret_cast<const BlockDesc*>(piece(kPieceDesc + sl));
+    const bool gu = it.kind == PW_KIND_GATE_UP;
+    const bool ok = desc_ok(p, d, it.kind);
+    if (!ok && tid == 0) atomicOr(p.status, PW_STATUS_BAD_DESC);
+
+    // item i+2: where it is and its descriptor (stored at the end of this item)
+    uint4 dnext = make_uint4(0u, 0u, 0u, 0u);
+    const int sl2 = (i + 2) % kSlots;
+    if (warp == 0) {
+      if (lane == 0) s_item[sl2] = item_of(b + (i + 2) * G, pl, r);
+      __syncwarp();
+      if (lane < 8 && s_item[sl2].valid)
+        dnext = ld_nc16(reinterpret_cast<const uint4*>(block_desc(p, s_item[sl2].expert, s_item[sl2].kind)) + lane);
     }
-    if (ok) {
-      if (gu) run_tile<PW_KIND_GATE_UP>(p, d, it, smem, r.perm, item == pre_item ? kTileResume : kTileWhole);
-      else run_tile<PW_KIND_DOWN>(p, d, it, smem, r.perm);
-    } else if (threadIdx.x == 0) {
-      atomicOr(p.status, PW_STATUS_BAD_DESC);
+    // item i+1's tables, into registers until this item's lookups are done
+    const int sl1 = (i + 1) % kSlots;
+    const ItemInfo it1 = s_item[sl1];
+    const BlockDesc& d1 = *reinterpret_cast<const BlockDesc*>(piece(kPieceDesc + sl1));
+    const bool ok1 = i + 1 < n_items && it1.valid && desc_ok(p, d1, it1.kind);
+    if (ok1) {
+      int rho, rho2;
+      lane_rows(p, it1, lane, rho, rho2);
+      lut_load(lr, d1, rho, rho2, warp);
     }
-    // the h / y writers (threads below kTok * kRows) order their writes before the
-    // counters below; the other threads wrote nothing other CTAs read
-    if (threadIdx.x < kTok * kRows) __threadfence();
-    __syncthreads();
+
+    int u0, u1;
+    warp_units(d, ok, warp, u0, u1);
+    float acc[2][2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[j][hh][c] = 0.f;
+    if (u0 < u1) {
+      // this lane's token rows (lanes 9c + 4t carry token t of each column set)
+      const int tl = (lane >> 2) - 2 * (lane & 3);
+      const uint4* xr[2] = {nullptr, nullptr};
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int tok = 2 * j + tl;
+        if (tl >= 0 && tl <= 1 && tok < it.n) {
+          const int pos = it.off + tok;
+          xr[j] = reinterpret_cast<const uint4*>(gu ? p.x + static_cast<size_t>(r.perm[pos] / p.k) * p.H
+                                                    : p.hh + static_cast<size_t>(pos) * p.I);
+        }
+      }
+      if (!gu) {   // h of this expert comes from its gate_up items
+        if (lane == 0 && !wait_ge(&expert_done[it.expert], it.need)) atomicOr(p.status, PW_STATUS_TIMEOUT);
+        __syncwarp();
+      }
+      uint4 X0[4], X1[4];
+      const int w0 = u0 * kUnitWords, w1 = u1 * kUnitWords;
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        X0[k4] = make_uint4(0u, 0u, 0u, 0u);
+        X1[k4] = make_uint4(0u, 0u, 0u, 0u);
+        ld_x16(X0[k4], xr[0] + w0 * 4 + k4, xr[0] != nullptr);
+        ld_x16(X1[k4], xr[1] + w0 * 4 + k4, xr[1] != nullptr);
+      }
+      const int Q = d.q;
+      for (int u = u0; u < u1; ++u) {
+        cp_wait_n(issued - consumed - 1);
+        __syncwarp();   // every lane's copies of this stage visible; the previous stage is read
+        fetch_fill(f, p, n_items, i + 1, consumed, issued, warp, lane, ring);
+        const uint32_t st = ring + (consumed % kStages) * kStageBytes + lane * 8;
+        ++consumed;
+#pragma unroll 1
+        for (int wi = 0; wi < kUnitWords; ++wi) {
+          const int gw = u * kUnitWords + wi;
+          uint32_t o0[8], o1[8];
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr) {   // o[rr] = plane (Q-1-rr) of the row
+            o0[rr] = 0u;
+            o1[rr] = 0u;
+            if (rr < Q) {
+              const uint32_t a = st + wi * 4 + (Q - 1 - rr) * 512;
+              asm volatile("ld.shared.u32 %0, [%1];" : "=r"(o0[rr]) : "r"(a));
+              asm volatile("ld.shared.u32 %0, [%1];" : "=r"(o1[rr]) : "r"(a + 256));
+            }
+          }
+          planes_to_indices(o0);
+          planes_to_indices(o1);
+          const bool more = gw + 1 < w1;
+          word_mma(o0, o1, laneoff, X0, X1, xr[0] + (gw + 1) * 4, xr[1] + (gw + 1) * 4,
+                   more && xr[0] != nullptr, more && xr[1] != nullptr, acc);
+        }
+      }
+    }
+    // keep the ring running into the next item while this one finishes
+    __syncwarp();
+    fetch_fill(f, p, n_items, i + 1, consumed, issued, warp, lane, ring);
+
+    // ---- partial sums: piece(warp * 8 + half * 4 + token)[lane]
+    {
+      float* red = reinterpret_cast<float*>(piece(kPieceRed + warp * 8));
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {   // column set j: tokens 2j, 2j+1 of the rows rho / rho2
+        v[2 * j] = acc[j][0][0] + acc[j][1][0];
+        v[2 * j + 1] = acc[j][0][1] + acc[j][1][1];
+        v[4 + 2 * j] = acc[j][0][2] + acc[j][1][2];
+        v[4 + 2 * j + 1] = acc[j][0][3] + acc[j][1][3];
+      }
+#pragma unroll
+      for (int k8 = 0; k8 < 8; ++k8) red[k8 * (kLine / 4) + lane] = v[k8];
+    }
+    __syncthreads();   // every lookup of this item is done; partials visible
+
+    if (ok1) lut_store(lr, d1.q, lane, warp);
+    if (warp == 0 && lane < 8) reinterpret_cast<uint4*>(piece(kPieceDesc + sl2))[lane] = dnext;
+    auto red_at = [&](int w, int k8, int l) {
+      return reinterpret_cast<const float*>(piece(kPieceRed + w * 8 + k8))[l];
+    };
     if (gu) {
-      if (threadIdx.x == 0) atomicAdd(&expert_done[it.expert], 1);
+      if (tid < 32 * it.n) {
+        const int l = tid & 31, t = tid >> 5;
+        float g = 0.f, u = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          g += red_at(w, t, l);
+          u += red_at(w, 4 + t, l);
+        }
+        const float hv = g / (1.f + expf(-g)) * u;
+        p.hh[static_cast<size_t>(it.off + t) * p.I + it.tile * kGateUpTileRows + l] = __float2half_rn(hv);
+        __threadfence();
+      }
     } else {
-      if (threadIdx.x == 0) {
-        s_int[2] = (atomicAdd(&tile_done[it.tile], 1) == nact - 1);
+      if (tid < 64 * it.n) {
+        const int l = tid & 31, hf = (tid >> 5) & 1, t = tid >> 6;
+        float yv = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) yv += red_at(w, hf * 4 + t, l);
+        p.y[static_cast<size_t>(it.off + t) * p.H + it.tile * kDownTileRows + hf * 32 + l] = yv;
+        __threadfence();
+      }
+    }
+    __syncthreads();   // outputs fenced; next item's tables and descriptor in place
+    if (gu) {
+      if (tid == 0) atomicAdd(&expert_done[it.expert], 1);
+    } else {
+      if (tid == 0) {
+        s_int[1] = (atomicAdd(&tile_done[it.tile], 1) == pl.down_per_tile - 1);
         __threadfence();
       }
       __syncthreads();
-      if (s_int[2]) {
+      if (s_int[1]) {
         __threadfence();
-        const int r0 = it.tile * kRows;
-        combine_rows(p, r.w, r.inv, r0, min(r0 + kRows, p.H), 0, p.T, threadIdx.x, blockDim.x);
+        const int r0 = it.tile * kDownTileRows;
+        combine_rows(p, r.w, r.inv, r0, min(r0 + kDownTileRows, p.H), 0, p.T, tid, blockDim.x);
       }
     }
-    __syncthreads();
   }
+  cp_wait<0>();
 }
 
 constexpr int kMaxDevices = 64;
@@ -490,6 +692,7 @@ cudaError_t launch_layer_fused(const Fwd& p, cudaStream_t s) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (p.H % kDownTileRows != 0 || p.I % kGateUpTileRows != 0) return cudaErrorInvalidValue;
   if (g_fused[dev] == 0) {   // once per device: shared-memory opt-in and co-resident grid size
     e = cudaFuncSetAttribute(k_layer, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     int per_sm = 0, sms = 0;
@@ -501,7 +704,7 @@ cudaError_t launch_layer_fused(const Fwd& p, cudaStream_t s) {
     g_fused[dev] = per_sm * sms;
   }
   // An ordinary launch of exactly the co-resident grid (every wait in the kernel
-  // is on work that a running CTA has already claimed, or on CTA 0, which is
+  // is on work that a running CTA has already been dealt, or on CTA 0, which is
   // scheduled first), allowed to start while the previous kernel on the stream
   // finishes (programmatic stream serialisation; the kernel waits for it with
   // griddepcontrol.wait before it touches the workspace or the token rows).

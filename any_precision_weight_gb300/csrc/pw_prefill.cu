@@ -348,8 +348,11 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
       }
     }
     // plane chunks: 16 bytes (4 words = K steps 2j, 2j+1) per row and plane;
-    // thread (row, group) copies planes 4*group .. 4*group+3 of its row
+    // thread (row, group) copies planes 4*group .. 4*group+3 of its row.  In
+    // the page layout a row's word pairs are 64 words apart, so each chunk is
+    // two 8-byte copies (32 consecutive rows' copies are contiguous)
     const int cgrp = half;
+    const size_t prow = grow >= 0 ? (static_cast<size_t>(grow >> 5) * (W >> 1)) * 64 + (grow & 31) * 2 : 0;
     auto fetch_chunk = [&](int j) {
       if (grow >= 0 && 2 * j < nksteps) {
         unsigned char* dst = smem + kOffPl + (j & 1) * kPlaneChunkBytes + row * 16;
@@ -358,9 +361,11 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
           const int pl = cgrp * 4 + u;
           const uint32_t* src = cgrp ? d.planes[4 + u] : d.planes[u];
           if (pl < Q) {
-            const uint32_t* gsrc = src + static_cast<size_t>(grow) * W + 4 * j;
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr(dst + pl * kBM * 16)),
+            const uint32_t* gsrc = src + prow + static_cast<size_t>(2 * j) * 64;
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(saddr(dst + pl * kBM * 16)),
                          "l"(gsrc));
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(saddr(dst + pl * kBM * 16 + 8)),
+                         "l"(gsrc + 64));
           }
         }
       }

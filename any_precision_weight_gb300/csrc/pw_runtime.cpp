@@ -518,6 +518,47 @@ int pw_pack(const uint8_t* idx, int R, int K, int n_bits, const uint16_t* parent
   return PW_OK;
 }
 
+int pw_tile_planes(const uint32_t* planes, int n_bits, int R, int K, uint32_t* tiled_out) {
+  if (!planes || !tiled_out) return fail(PW_EINVAL, "pw_tile_planes: null pointer");
+  if (n_bits < 1 || n_bits > PW_MAX_BITS || R < 32 || R % 32 || K < 64 || K % 64)
+    return fail(PW_EINVAL, "pw_tile_planes: need 1 <= n_bits <= 8, R %% 32 == 0, K %% 64 == 0");
+  const size_t W = static_cast<size_t>(K) / 32, plane_words = static_cast<size_t>(R) * W;
+  const uint32_t* lo = planes;
+  const uint32_t* hi = planes + plane_words * n_bits;
+  if (tiled_out < hi && lo < tiled_out + plane_words * n_bits)
+    return fail(PW_EINVAL, "pw_tile_planes: input and output overlap");
+  // word (p, r, w) -> p*R*W + ((r/32)*(W/2) + w/2)*64 + (r%32)*2 + w%2; one
+  // task per (plane, group of 32 rows), spread over CPU threads
+  const int groups = R / 32, tasks = n_bits * groups;
+  auto work = [&](int t0, int step) {
+    for (int t = t0; t < tasks; t += step) {
+      const int p = t / groups, g = t % groups;
+      const uint32_t* src = planes + p * plane_words + static_cast<size_t>(g) * 32 * W;
+      uint32_t* dst = tiled_out + p * plane_words + static_cast<size_t>(g) * 32 * W;
+      for (int rr = 0; rr < 32; ++rr) {
+        const uint32_t* row = src + static_cast<size_t>(rr) * W;
+        uint32_t* d = dst + rr * 2;
+        for (size_t w = 0; w < W; w += 2) {
+          d[w * 32] = row[w];
+          d[w * 32 + 1] = row[w + 1];
+        }
+      }
+    }
+  };
+  unsigned nthr = std::thread::hardware_concurrency();
+  if (nthr == 0) nthr = 1;
+  if (plane_words * n_bits < (1u << 20)) nthr = 1;
+  if (nthr > 32) nthr = 32;
+  if (nthr == 1) {
+    work(0, 1);
+  } else {
+    std::vector<std::thread> th;
+    for (unsigned i = 0; i < nthr; ++i) th.emplace_back(work, static_cast<int>(i), static_cast<int>(nthr));
+    for (auto& x : th) x.join();
+  }
+  return PW_OK;
+}
+
 size_t pw_desc_bytes(int n_layers, int n_experts) {
   if (n_layers <= 0 || n_experts <= 0) return 0;
   return static_cast<size_t>(n_layers) * n_experts * 2 * sizeof(pw::BlockDesc);

@@ -8,7 +8,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import KIND_DOWN, KIND_GATE_UP, PagedMoE, pw_lut_bytes, pw_pack
+from . import KIND_DOWN, KIND_GATE_UP, PagedMoE, pw_lut_bytes, pw_pack, pw_tile_planes
 
 
 class HostStore:
@@ -44,8 +44,9 @@ class HostStore:
 
 def pack_pinned(P: np.ndarray, parent_lut: np.ndarray, n_bits: int = 8, b_min: int = 3,
                 store: HostStore | None = None):
-    """pw_pack into pinned torch CPU tensors (planes as int32, tables as int16),
-    from ``store`` if given, else one pinned allocation each."""
+    """pw_pack into pinned torch CPU tensors (planes as int32 in the device page
+    layout of pw_tile_planes, tables as int16), from ``store`` if given, else one
+    pinned allocation each."""
     import torch
     R, K = P.shape
     pb = n_bits * R * (K // 32) * 4
@@ -56,8 +57,8 @@ def pack_pinned(P: np.ndarray, parent_lut: np.ndarray, n_bits: int = 8, b_min: i
     else:
         planes = store.alloc(pb).view(torch.int32).view(n_bits, R, K // 32)
         luts = store.alloc(lb).view(torch.int16)
-    pw_pack(P, parent_lut, n_bits, b_min, planes_out=planes.numpy().view(np.uint32),
-            luts_out=luts.numpy().view(np.uint16))
+    flat, _ = pw_pack(P, parent_lut, n_bits, b_min, luts_out=luts.numpy().view(np.uint16))
+    pw_tile_planes(flat, out=planes.numpy().view(np.uint32).reshape(-1))
     return planes, luts
 
 

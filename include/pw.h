@@ -22,6 +22,8 @@
  *   top b planes (index P >> (n-b)) and the row's own 2^b-entry fp16 table LUT_b.
  *   Each plane of a block is one page of R*K/8 bytes, so the planes below the
  *   committed bitwidth form a tail that can live on the CPU and be reloaded.
+ *   Inside a device page the words are interleaved across groups of 32 rows
+ *   (pw_tile_planes), so that a warp's reads of 32 rows are contiguous.
  *
  * Block shapes: gate_up has R = 2I rows (rows [0, I) gate, [I, 2I) up) and
  * K = H columns; down has R = H rows and K = I columns.  H, I multiples of 128.
@@ -100,6 +102,24 @@ size_t pw_lut_offset(int R, int b_min, int b);
 int pw_pack(const uint8_t* idx, int R, int K, int n_bits, const uint16_t* parent_lut,
             int b_min, uint32_t* planes_out, uint16_t* luts_out);
 
+/*
+ * pw_tile_planes -- the device page layout of a block's planes (host, CPU).
+ * Source: "Paged Weight Representation" (each plane one page); the order of
+ * the words inside a page is this library's choice.
+ * Reorders pw_pack's planes [n_bits][R][K/32] into the layout the kernels and
+ * pw_block_register use: within each plane, rows are taken in groups of 32
+ * and every pair of consecutive words along K is stored for the group's 32
+ * rows side by side, [n_bits][R/32][K/64][32][2]; word w of row r of plane p
+ * lands at p*R*(K/32) + ((r/32)*(K/64) + w/2)*64 + (r%32)*2 + w%2.  A warp
+ * reading two words of 32 consecutive rows then reads 256 contiguous bytes.
+ * Each plane is still one contiguous page of R*K/8 bytes.
+ *   planes     host [n_bits][R][K/32] uint32 (pw_pack output), read only
+ *   tiled_out  host, same size, must not overlap planes
+ * Requirements: 1 <= n_bits <= 8, R % 32 == 0, K % 64 == 0.
+ * Errors: PW_EINVAL (shape, null pointer, overlapping buffers).
+ */
+int pw_tile_planes(const uint32_t* planes, int n_bits, int R, int K, uint32_t* tiled_out);
+
 /* ------------------------------------------------------------------ page table */
 
 /* Bytes of the device descriptor array for n_layers x n_experts x 2 blocks. */
@@ -121,8 +141,9 @@ int pw_table_create(pw_table** out, int n_layers, int n_experts, int H, int I,
 
 /*
  * pw_block_register -- attach one linear block (layer, expert, kind).
- *   host_planes  host [n_bits][R][K/32] uint32 (pw_pack output), the backing store
- *                of every plane; pinned memory makes later reloads asynchronous.
+ *   host_planes  host planes in the page layout of pw_tile_planes (pw_pack output
+ *                reordered by it), the backing store of every plane; pinned
+ *                memory makes later reloads asynchronous.
  *                Must stay valid until pw_table_destroy.
  *   host_luts    host tables as written by pw_pack; same lifetime rule.
  *   d_plane_pages n_bits device pointers, page p holding plane p (R*K/8 bytes,

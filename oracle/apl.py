@@ -62,6 +62,21 @@ def unpack(planes: np.ndarray, b: int, n: int) -> np.ndarray:
     return idx
 
 
+def tile_planes(planes: np.ndarray) -> np.ndarray:
+    """Planes [n][R][W] -> the device page order, flat uint32.
+
+    Each plane is cut into groups of 32 rows and pairs of words along K; a
+    page lists, for each group (in row order) and each word pair (in K order),
+    the 32 rows' two words side by side: [n][R/32][W/2][32][2].  A pure
+    reordering of the words; R must be a multiple of 32 and W even.
+    """
+    planes = np.asarray(planes, dtype=np.uint32)
+    n, R, W = planes.shape
+    if R % 32 or W % 2:
+        raise ValueError("R must be a multiple of 32 and W even")
+    return planes.reshape(n, R // 32, 32, W // 2, 2).transpose(0, 1, 3, 2, 4).reshape(-1).copy()
+
+
 def child_lut(parent_lut: np.ndarray, b: int, n: int) -> np.ndarray:
     """LUT_b [R][2^b] fp16 from the parent table [R][2^n] fp16 (see module doc)."""
     par = np.asarray(parent_lut, dtype=np.float16).astype(np.float64)

@@ -90,3 +90,17 @@ def test_workspace_bytes_cover_sections():
     nb = pw.lib().pw_workspace_bytes(4, 60, 4, 2048, 1408)
     assert nb >= 16 * 1408 * 2 + 16 * 2048 * 4      # h (fp16) and y (fp32) of every pair
     assert pw.lib().pw_workspace_bytes(-1, 60, 4, 2048, 1408) == 0
+
+
+@pytest.mark.parametrize("R,K,n", [(32, 64, 1), (64, 256, 8), (256, 1408, 6)])
+def test_tile_planes_matches_oracle_bit_exact(R, K, n):
+    rng = np.random.default_rng(R + K + n)
+    planes = rng.integers(0, 1 << 32, size=(n, R, K // 32), dtype=np.uint64).astype(np.uint32)
+    assert np.array_equal(pw.pw_tile_planes(planes), apl.tile_planes(planes))
+
+
+def test_tile_planes_rejects_bad_shapes():
+    with pytest.raises(pw.PWError):
+        pw.pw_tile_planes(np.zeros((1, 48, 2), dtype=np.uint32))      # R % 32
+    with pytest.raises(pw.PWError):
+        pw.pw_tile_planes(np.zeros((1, 32, 3), dtype=np.uint32))      # K % 64

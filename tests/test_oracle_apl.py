@@ -105,3 +105,26 @@ def test_dequant_brute_force():
             for k in range(32):
                 v = int(P[r, k]) // (2 ** (8 - b))
                 assert W[r, k] == float(lut[r, v])
+
+
+def test_tile_planes_places_every_word_at_its_closed_form_index():
+    """The page order of the planes: word w of row r of plane p sits at
+    p*R*W + ((r/32)*(W/2) + w/2)*64 + (r%32)*2 + w%2, checked word by word
+    against an explicit loop over that formula (tags make each word unique)."""
+    n, R, W = 3, 64, 6
+    planes = ((np.arange(n * R * W, dtype=np.uint64) * 2654435761) % (1 << 32)).astype(np.uint32)
+    planes = planes.reshape(n, R, W)
+    got = apl.tile_planes(planes)
+    want = np.zeros(n * R * W, dtype=np.uint32)
+    for p in range(n):
+        for r in range(R):
+            for w in range(W):
+                want[p * R * W + ((r // 32) * (W // 2) + w // 2) * 64 + (r % 32) * 2 + w % 2] = planes[p, r, w]
+    assert np.array_equal(got, want)
+    assert sorted(got.tolist()) == sorted(planes.reshape(-1).tolist())     # a permutation
+    # a warp reading word pair u of 32 consecutive rows reads 64 contiguous words
+    u, g = 1, 1
+    block = got[(g * (W // 2) + u) * 64:(g * (W // 2) + u + 1) * 64].reshape(32, 2)
+    assert np.array_equal(block, planes[0, 32 * g:32 * g + 32, 2 * u:2 * u + 2])
+    with pytest.raises(ValueError):
+        apl.tile_planes(np.zeros((1, 48, 4), dtype=np.uint32))
