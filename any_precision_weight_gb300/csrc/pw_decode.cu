@@ -56,17 +56,23 @@ constexpr int kDownTileRows = 64;
 
 // Shared memory.  Table line v (256 bytes) holds the 32 lanes' slots for index
 // v in its first half; the second halves ("pieces", 128 bytes each) hold the
-// split-K partial sums and the descriptors of the items in flight.
+// split-K partial sums and the descriptors of the items in flight.  The table
+// starts at a 64 KB-aligned shared address, so that one byte permute forms a
+// lookup's complete address (index in byte 1, lane * 4 in byte 0, the table's
+// 64 KB window in bytes 2-3).  The warps' rings fill the space before it and
+// continue after it, followed by the routing results ("rest").
 constexpr int kLine = 256;
 constexpr int kTableBytes = 256 * kLine;
 constexpr int kStageBytes = PW_MAX_BITS * 2 * 32 * 8;   // [plane][row half][lane] x 2 words
-constexpr int kRingOff = kTableBytes;
-constexpr int kRingBytes = kWarps * kStages * kStageBytes;
-constexpr int kRouteOff = kRingOff + kRingBytes;
+constexpr int kRingWarpBytes = kStages * kStageBytes;
+constexpr int kSlots = 3;          // items in flight: current, next, the one after
+constexpr int kRouteOff = 0;       // offsets within the rest area
 constexpr int kCumOff = kRouteOff + route_smem_bytes();
 constexpr int kItemOff = kCumOff + 2 * (kMaxE + 1) * 4;
-constexpr int kSlots = 3;          // items in flight: current, next, the one after
-constexpr int kSmemBytes = kItemOff + 256;
+constexpr int kRestBytes = kItemOff + 256;
+// whatever the dynamic window's start, everything fits in: at most one ring's
+// worth of bytes before the table is left unused
+constexpr int kSmemBytes = (kWarps + 1) * kRingWarpBytes + kTableBytes + kRestBytes;
 constexpr int kPieceRed = 0;       // 8 warps x 8 (row half, token) x 32 lanes fp32
 constexpr int kPieceDesc = 64;     // one BlockDesc per item slot
 
@@ -118,10 +124,36 @@ __device__ __forceinline__ void planes_to_indices(uint32_t (&o)[8]) {
   for (int r = 0; r < 8; r += 2) delta_swap(o[r], o[r + 1], 1, 0x55555555u);
 }
 
-// Table slot at byte address a (index * 256 + lane * 4).  Indexing the dynamic
-// shared-memory symbol lets its address fold into the load's immediate offset.
+// Table slot at shared address a.
 __device__ __forceinline__ uint32_t lut_slot(uint32_t a) {
-  return *reinterpret_cast<const uint32_t*>(g_smem + a);
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+
+// Where the table, the rings and the rest area sit in this CTA's dynamic
+// shared memory (computed once from the window address of g_smem).
+struct Smem {
+  unsigned char* table;   // 64 KB-aligned shared address
+  unsigned char* rest;
+  uint32_t table_hi;      // shared address of the table (bytes 2-3 only)
+  int nb;                 // warps whose rings sit before the table
+  uint32_t toff;
+};
+__device__ __forceinline__ Smem smem_layout() {
+  Smem m;
+  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(g_smem));
+  m.toff = (0x10000u - (base & 0xFFFFu)) & 0xFFFFu;
+  m.nb = min(kWarps, static_cast<int>(m.toff / kRingWarpBytes));
+  m.table = g_smem + m.toff;
+  m.table_hi = base + m.toff;
+  m.rest = m.table + kTableBytes + (kWarps - m.nb) * kRingWarpBytes;
+  return m;
+}
+__device__ __forceinline__ uint32_t ring_of(const Smem& m, int warp) {
+  const uint32_t off = warp < m.nb ? warp * kRingWarpBytes
+                                   : m.toff + kTableBytes + (warp - m.nb) * kRingWarpBytes;
+  return static_cast<uint32_t>(__cvta_generic_to_shared(g_smem)) + off;
 }
 
 // D += A * B, m16n8k16, fp16 operands, fp32 accumulators.
@@ -140,7 +172,7 @@ __device__ __forceinline__ uint4 ld_nc16(const void* p) {   // read-only for the
 }
 
 // 128-byte piece n (second half of table line n).
-__device__ __forceinline__ unsigned char* piece(int n) { return g_smem + n * kLine + 128; }
+__device__ __forceinline__ unsigned char* piece(unsigned char* table, int n) { return table + n * kLine + 128; }
 
 // ------------------------------------------------------------------ work items
 
@@ -246,7 +278,7 @@ __device__ __forceinline__ void lut_load(LutRegs& f, const BlockDesc& d, int rho
 }
 
 // Slot (v, lane) = (row rho entry v) | (row rho2 entry v) << 16.
-__device__ __forceinline__ void lut_store(const LutRegs& f, int q, int lane, int wv) {
+__device__ __forceinline__ void lut_store(unsigned char* table, const LutRegs& f, int q, int lane, int wv) {
   const int V = 1 << q;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -258,8 +290,8 @@ __device__ __forceinline__ void lut_store(const LutRegs& f, int q, int lane, int
       for (int e = 0; e < 4; ++e) {
         const int v = vc * 8 + 2 * e;
         if (v < V) {
-          *reinterpret_cast<uint32_t*>(g_smem + v * kLine + lane * 4) = prmt(aw[e], bw[e], 0x5410u);
-          *reinterpret_cast<uint32_t*>(g_smem + (v + 1) * kLine + lane * 4) = prmt(aw[e], bw[e], 0x7632u);
+          *reinterpret_cast<uint32_t*>(table + v * kLine + lane * 4) = prmt(aw[e], bw[e], 0x5410u);
+          *reinterpret_cast<uint32_t*>(table + (v + 1) * kLine + lane * 4) = prmt(aw[e], bw[e], 0x7632u);
         }
       }
     }
@@ -286,7 +318,7 @@ __device__ __forceinline__ void word_mma(const uint32_t (&o0)[8], const uint32_t
                                          bool p0, bool p1, float (&acc)[2][2][4]) {
 #pragma unroll
   for (int bb = 0; bb < 4; ++bb) {
-    const uint32_t sel = 0x5504u | (static_cast<uint32_t>(bb) << 4);
+    const uint32_t sel = 0x7604u | (static_cast<uint32_t>(bb) << 4);
     uint32_t s[8], t[8];
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
@@ -320,10 +352,11 @@ struct Fetch {
   uint32_t desc;     // shared address of the item's descriptor
 };
 
-__device__ __forceinline__ void fetch_enter(Fetch& f, const Fwd& p, int item, int warp, int lane) {
+__device__ __forceinline__ void fetch_enter(Fetch& f, const Fwd& p, const Smem& sm, int item, int warp,
+                                            int lane) {
   const int sl = item % kSlots;
-  const ItemInfo& it = reinterpret_cast<const ItemInfo*>(g_smem + kItemOff)[sl];
-  const BlockDesc& d = *reinterpret_cast<const BlockDesc*>(piece(kPieceDesc + sl));
+  const ItemInfo& it = reinterpret_cast<const ItemInfo*>(sm.rest + kItemOff)[sl];
+  const BlockDesc& d = *reinterpret_cast<const BlockDesc*>(piece(sm.table, kPieceDesc + sl));
   f.item = item;
   f.desc = smem_addr(&d);
   const bool ok = it.valid && desc_ok(p, d, it.kind);
@@ -341,22 +374,27 @@ __device__ __forceinline__ void fetch_enter(Fetch& f, const Fwd& p, int item, in
 // (items up to `known`).  `issued` counts units issued by this warp.  The
 // caller has synchronised the warp after the last read of the stage that the
 // next issue overwrites.
-__device__ __forceinline__ void fetch_fill(Fetch& f, const Fwd& p, int n_items, int known, int consumed,
-                                           int& issued, int warp, int lane, uint32_t ring) {
+__device__ __forceinline__ void fetch_fill(Fetch& f, const Fwd& p, const Smem& sm, int n_items, int known,
+                                           int consumed, int& issued, int warp, int lane, uint32_t ring) {
   while (issued < consumed + kStages) {
     while (f.u == f.end) {   // the warp has no more units in this item
       if (f.item + 1 > known || f.item + 1 >= n_items) return;
-      fetch_enter(f, p, f.item + 1, warp, lane);
+      fetch_enter(f, p, sm, f.item + 1, warp, lane);
     }
+    // plane p of a q-plane item goes to stage slot 8 - q + p, so that plane
+    // q-1-r is always slot 7-r; the slots below 8 - q are zeroed
     const uint32_t dst = ring + (issued % kStages) * kStageBytes + (lane >> 4) * 256 + (lane & 15) * 16;
     const size_t w = f.off + static_cast<size_t>(f.u) * 64;
+    const int lo = PW_MAX_BITS - f.q;
 #pragma unroll
-    for (int pl = 0; pl < PW_MAX_BITS; ++pl) {
-      if (pl < f.q) {
+    for (int sl = 0; sl < PW_MAX_BITS; ++sl) {
+      if (sl >= lo) {
         uint64_t base;
-        asm volatile("ld.shared.u64 %0, [%1];" : "=l"(base) : "r"(f.desc + pl * 8));
+        asm volatile("ld.shared.u64 %0, [%1];" : "=l"(base) : "r"(f.desc + (sl - lo) * 8));
         const uint32_t* src = reinterpret_cast<const uint32_t*>(base) + w;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + pl * 512), "l"(src) : "memory");
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + sl * 512), "l"(src) : "memory");
+      } else {
+        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst + sl * 512), "r"(0u) : "memory");
       }
     }
     cp_commit();
@@ -373,6 +411,14 @@ __device__ __forceinline__ int ld_acquire(const int* ptr) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
   return v;
+}
+__device__ __forceinline__ void red_release_add(int* ptr, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+__device__ __forceinline__ int atom_acq_rel_add(int* ptr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+  return old;
 }
 __device__ __forceinline__ void st_release(int* ptr, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
@@ -404,7 +450,8 @@ __device__ bool wait_ge(const int* ptr, int want) {
 // it.  Every wait is bounded and reports PW_STATUS_TIMEOUT instead of hanging.
 __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int* rs = reinterpret_cast<int*>(g_smem + kRouteOff);
+  const Smem sm = smem_layout();
+  int* rs = reinterpret_cast<int*>(sm.rest + kRouteOff);
   RouteSmem r;
   r.idx = rs;
   r.w = reinterpret_cast<float*>(rs + kRouteSmemMaxPairs);
@@ -415,9 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   r.act = r.off + (kMaxE + 1);
   r.lpt = r.act + (kMaxE + 1);
   r.qgu = r.lpt + (kMaxE + 1);
-  int* cum_gu = reinterpret_cast<int*>(g_smem + kCumOff);
+  int* cum_gu = reinterpret_cast<int*>(sm.rest + kCumOff);
   int* cum_dn = cum_gu + (kMaxE + 1);
-  ItemInfo* s_item = reinterpret_cast<ItemInfo*>(g_smem + kItemOff);
+  ItemInfo* s_item = reinterpret_cast<ItemInfo*>(sm.rest + kItemOff);
   int* s_int = reinterpret_cast<int*>(s_item + kSlots);
 
   Plan pl;
@@ -469,25 +516,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     const int sl = lane >> 3, part = lane & 7;
     if (s_item[sl].valid) {
       const uint4* src = reinterpret_cast<const uint4*>(block_desc(p, s_item[sl].expert, s_item[sl].kind));
-      reinterpret_cast<uint4*>(piece(kPieceDesc + sl))[part] = ld_nc16(src + part);
+      reinterpret_cast<uint4*>(piece(sm.table, kPieceDesc + sl))[part] = ld_nc16(src + part);
     }
   }
   __syncthreads();
-  const uint32_t ring = smem_addr(g_smem + kRingOff) + warp * (kStages * kStageBytes);
-  const uint32_t laneoff = static_cast<uint32_t>(lane) * 4u;
+  const uint32_t ring = ring_of(sm, warp);
+  const uint32_t laneoff = sm.table_hi | (static_cast<uint32_t>(lane) * 4u);
   Fetch f;
   int issued = 0, consumed = 0;
   LutRegs lr;
   if (n_items > 0) {
-    const BlockDesc& d0 = *reinterpret_cast<const BlockDesc*>(piece(kPieceDesc));
+    const BlockDesc& d0 = *reinterpret_cast<const BlockDesc*>(piece(sm.table, kPieceDesc));
     int rho, rho2;
     lane_rows(p, s_item[0], lane, rho, rho2);
     if (desc_ok(p, d0, s_item[0].kind)) {
       lut_load(lr, d0, rho, rho2, warp);
-      lut_store(lr, d0.q, lane, warp);
+      lut_store(sm.table, lr, d0.q, lane, warp);
     }
-    fetch_enter(f, p, 0, warp, lane);
-    fetch_fill(f, p, n_items, 1, consumed, issued, warp, lane, ring);
+    fetch_enter(f, p, sm, 0, warp, lane);
+    fetch_fill(f, p, sm, n_items, 1, consumed, issued, warp, lane, ring);
   }
 
   // the previous kernel on the stream (possibly the previous forward, using the
@@ -523,10 +570,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   }
   __syncthreads();   // the prologue's tables are complete
 
+  // thread 0: the last down item's tile and the count its update returned,
+  // looked at only at the next item boundary
+  int pending_tile = -1, pending_old = -1;
   for (int i = 0; i < n_items; ++i) {
     const int sl = i % kSlots;
     const ItemInfo it = s_item[sl];
-    const BlockDesc& d = *reinterpret_cast<const BlockDesc*>(piece(kPieceDesc + sl));
+    const BlockDesc& d = *reinterpret_cast<const BlockDesc*>(piece(sm.table, kPieceDesc + sl));
     const bool gu = it.kind == PW_KIND_GATE_UP;
     const bool ok = desc_ok(p, d, it.kind);
     if (!ok && tid == 0) atomicOr(p.status, PW_STATUS_BAD_DESC);
@@ -543,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     // item i+1's tables, into registers until this item's lookups are done
     const int sl1 = (i + 1) % kSlots;
     const ItemInfo it1 = s_item[sl1];
-    const BlockDesc& d1 = *reinterpret_cast<const BlockDesc*>(piece(kPieceDesc + sl1));
+    const BlockDesc& d1 = *reinterpret_cast<const BlockDesc*>(piece(sm.table, kPieceDesc + sl1));
     const bool ok1 = i + 1 < n_items && it1.valid && desc_ok(p, d1, it1.kind);
     if (ok1) {
       int rho, rho2;
@@ -586,26 +636,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
         ld_x16(X0[k4], xr[0] + w0 * 4 + k4, xr[0] != nullptr);
         ld_x16(X1[k4], xr[1] + w0 * 4 + k4, xr[1] != nullptr);
       }
-      const int Q = d.q;
       for (int u = u0; u < u1; ++u) {
         cp_wait_n(issued - consumed - 1);
         __syncwarp();   // every lane's copies of this stage visible; the previous stage is read
-        fetch_fill(f, p, n_items, i + 1, consumed, issued, warp, lane, ring);
+        fetch_fill(f, p, sm, n_items, i + 1, consumed, issued, warp, lane, ring);
         const uint32_t st = ring + (consumed % kStages) * kStageBytes + lane * 8;
         ++consumed;
 #pragma unroll 1
         for (int wi = 0; wi < kUnitWords; ++wi) {
           const int gw = u * kUnitWords + wi;
           uint32_t o0[8], o1[8];
+          const uint32_t sw = st + wi * 4;
 #pragma unroll
-          for (int rr = 0; rr < 8; ++rr) {   // o[rr] = plane (Q-1-rr) of the row
-            o0[rr] = 0u;
-            o1[rr] = 0u;
-            if (rr < Q) {
-              const uint32_t a = st + wi * 4 + (Q - 1 - rr) * 512;
-              asm volatile("ld.shared.u32 %0, [%1];" : "=r"(o0[rr]) : "r"(a));
-              asm volatile("ld.shared.u32 %0, [%1];" : "=r"(o1[rr]) : "r"(a + 256));
-            }
+          for (int rr = 0; rr < 8; ++rr) {   // o[rr] = plane (Q-1-rr) of the row (zero for rr >= Q)
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(o0[rr]) : "r"(sw + (7 - rr) * 512));
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(o1[rr]) : "r"(sw + (7 - rr) * 512 + 256));
           }
           planes_to_indices(o0);
           planes_to_indices(o1);
@@ -617,11 +662,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     }
     // keep the ring running into the next item while this one finishes
     __syncwarp();
-    fetch_fill(f, p, n_items, i + 1, consumed, issued, warp, lane, ring);
+    fetch_fill(f, p, sm, n_items, i + 1, consumed, issued, warp, lane, ring);
 
     // ---- partial sums: piece(warp * 8 + half * 4 + token)[lane]
     {
-      float* red = reinterpret_cast<float*>(piece(kPieceRed + warp * 8));
+      float* red = reinterpret_cast<float*>(piece(sm.table, kPieceRed + warp * 8));
       float v[8];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {   // column set j: tokens 2j, 2j+1 of the rows rho / rho2
@@ -633,12 +678,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
 #pragma unroll
       for (int k8 = 0; k8 < 8; ++k8) red[k8 * (kLine / 4) + lane] = v[k8];
     }
+    // a down tile whose last item completed with the previous item: combine it now
+    if (tid == 0) s_int[1] = pending_old == pl.down_per_tile - 1 ? pending_tile : -1;
     __syncthreads();   // every lookup of this item is done; partials visible
+    if (s_int[1] >= 0) {
+      const int r0 = s_int[1] * kDownTileRows;
+      combine_rows(p, r.w, r.inv, r0, min(r0 + kDownTileRows, p.H), 0, p.T, tid, blockDim.x);
+    }
+    pending_tile = -1;
+    pending_old = -1;
 
-    if (ok1) lut_store(lr, d1.q, lane, warp);
-    if (warp == 0 && lane < 8) reinterpret_cast<uint4*>(piece(kPieceDesc + sl2))[lane] = dnext;
+    if (ok1) lut_store(sm.table, lr, d1.q, lane, warp);
+    if (warp == 0 && lane < 8) reinterpret_cast<uint4*>(piece(sm.table, kPieceDesc + sl2))[lane] = dnext;
     auto red_at = [&](int w, int k8, int l) {
-      return reinterpret_cast<const float*>(piece(kPieceRed + w * 8 + k8))[l];
+      return reinterpret_cast<const float*>(piece(sm.table, kPieceRed + w * 8 + k8))[l];
     };
     if (gu) {
       if (tid < 32 * it.n) {
@@ -651,7 +704,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
         }
         const float hv = g / (1.f + expf(-g)) * u;
         p.hh[static_cast<size_t>(it.off + t) * p.I + it.tile * kGateUpTileRows + l] = __float2half_rn(hv);
-        __threadfence();
       }
     } else {
       if (tid < 64 * it.n) {
@@ -660,24 +712,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) yv += red_at(w, hf * 4 + t, l);
         p.y[static_cast<size_t>(it.off + t) * p.H + it.tile * kDownTileRows + hf * 32 + l] = yv;
-        __threadfence();
       }
     }
-    __syncthreads();   // outputs fenced; next item's tables and descriptor in place
-    if (gu) {
-      if (tid == 0) atomicAdd(&expert_done[it.expert], 1);
-    } else {
-      if (tid == 0) {
-        s_int[1] = (atomicAdd(&tile_done[it.tile], 1) == pl.down_per_tile - 1);
-        __threadfence();
-      }
-      __syncthreads();
-      if (s_int[1]) {
-        __threadfence();
-        const int r0 = it.tile * kDownTileRows;
-        combine_rows(p, r.w, r.inv, r0, min(r0 + kDownTileRows, p.H), 0, p.T, tid, blockDim.x);
+    // Outputs written; next item's tables and descriptor in place.  After the
+    // barrier, thread 0's release-ordered counter update publishes every
+    // thread's h / y writes (ordered before it by the barrier).  A gate_up
+    // update is fire and forget; a down update returns the tile's count, which
+    // thread 0 looks at only at the next item boundary (the atomic's round trip
+    // overlaps the next item), where the CTA that completed the tile combines it.
+    __syncthreads();
+    if (tid == 0) {
+      if (gu) {
+        red_release_add(&expert_done[it.expert], 1);
+      } else {
+        pending_old = atom_acq_rel_add(&tile_done[it.tile], 1);
+        pending_tile = it.tile;
       }
     }
+  }
+  if (tid == 0) s_int[1] = pending_old == pl.down_per_tile - 1 ? pending_tile : -1;
+  __syncthreads();
+  if (s_int[1] >= 0) {
+    const int r0 = s_int[1] * kDownTileRows;
+    combine_rows(p, r.w, r.inv, r0, min(r0 + kDownTileRows, p.H), 0, p.T, tid, blockDim.x);
   }
   cp_wait<0>();
 }
