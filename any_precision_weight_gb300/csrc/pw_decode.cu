@@ -46,10 +46,10 @@
 namespace pw {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnitWords = 2;      // plane words per row per ring stage
-constexpr int kStages = 3;         // ring stages per warp
+constexpr int kStages = 2;         // ring stages per warp
 constexpr int kTokPass = 4;        // tokens per pass over a tile (two MMA column sets)
 constexpr int kGateUpTileRows = 32;   // gate rows per gate_up tile (plus as many up rows)
 constexpr int kDownTileRows = 64;
@@ -73,8 +73,10 @@ constexpr int kRestBytes = kItemOff + 256;
 // whatever the dynamic window's start, everything fits in: at most one ring's
 // worth of bytes before the table is left unused
 constexpr int kSmemBytes = (kWarps + 1) * kRingWarpBytes + kTableBytes + kRestBytes;
-constexpr int kPieceRed = 0;       // 8 warps x 8 (row half, token) x 32 lanes fp32
-constexpr int kPieceDesc = 64;     // one BlockDesc per item slot
+constexpr int kPieceRed = 0;       // warps x 8 (row half, token) x 32 lanes fp32
+constexpr int kPieceDesc = kWarps * 8;   // one BlockDesc per item slot
+constexpr int kPieceCache = kPieceDesc + kSlots;   // descriptors of every block of the layer
+constexpr int kCacheBlocks = 256 - kPieceCache;    // (when 2 E fits)
 
 extern __shared__ __align__(128) unsigned char g_smem[];
 
@@ -88,6 +90,10 @@ __device__ __forceinline__ void cp_wait_n(int n) {   // n = groups allowed to st
   if (n <= 0) cp_wait<0>();
   else if (n == 1) cp_wait<1>();
   else cp_wait<2>();
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -246,9 +252,10 @@ __device__ __forceinline__ void warp_units(const BlockDesc& d, bool ok, int warp
 // ------------------------------------------------------------------ tables
 
 // The next item's two table rows per lane, held in registers while the
-// current item runs: thread (lane, wv) owns 8-entry chunks wv, wv+8, ...
+// current item runs: thread (lane, wv) owns 8-entry chunks wv, wv + kWarps, ...
+constexpr int kLutChunks = (32 + kWarps - 1) / kWarps;   // 8-entry chunks per thread at q = 8
 struct LutRegs {
-  uint4 a[4], b[4];
+  uint4 a[kLutChunks], b[kLutChunks];
 };
 
 __device__ __forceinline__ void lut_load(LutRegs& f, const BlockDesc& d, int rho, int rho2, int wv) {
@@ -257,8 +264,8 @@ __device__ __forceinline__ void lut_load(LutRegs& f, const BlockDesc& d, int rho
     const uint4* ra = reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(rho) * V);
     const uint4* rb = reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(rho2) * V);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int vc = wv + 8 * j;
+    for (int j = 0; j < kLutChunks; ++j) {
+      const int vc = wv + kWarps * j;
       if (vc * 8 < V) {
         f.a[j] = ld_nc16(ra + vc);
         f.b[j] = ld_nc16(rb + vc);
@@ -281,8 +288,8 @@ __device__ __forceinline__ void lut_load(LutRegs& f, const BlockDesc& d, int rho
 __device__ __forceinline__ void lut_store(unsigned char* table, const LutRegs& f, int q, int lane, int wv) {
   const int V = 1 << q;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int vc = wv + 8 * j;
+  for (int j = 0; j < kLutChunks; ++j) {
+    const int vc = wv + kWarps * j;
     if (vc * 8 < V || (j == 0 && vc == 0)) {
       const uint32_t aw[4] = {f.a[j].x, f.a[j].y, f.a[j].z, f.a[j].w};
       const uint32_t bw[4] = {f.b[j].x, f.b[j].y, f.b[j].z, f.b[j].w};
@@ -403,6 +410,12 @@ __device__ __forceinline__ void fetch_fill(Fetch& f, const Fwd& p, const Smem& s
   }
 }
 
+// 16-byte part of a block's descriptor: from the shared cache or global memory.
+__device__ __forceinline__ uint4 desc_part(const Fwd& p, const Smem& sm, bool cached, int e, int kind, int part) {
+  if (cached) return reinterpret_cast<const uint4*>(piece(sm.table, kPieceCache + 2 * e + kind))[part];
+  return ld_nc16(reinterpret_cast<const uint4*>(block_desc(p, e, kind)) + part);
+}
+
 // ------------------------------------------------------------------ fused layer
 
 constexpr int kSpinLimit = 1 << 22;   // ~0.3 s of polling before a wait gives up
@@ -478,6 +491,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   // this one finishes, and waits for it before touching the workspace.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) s_int[0] = 0;   // NaN logit seen
+  // every block descriptor of the layer into shared memory (when they fit),
+  // in flight while the batch is routed
+  const bool cached = 2 * p.E <= kCacheBlocks;
+  if (cached)
+    for (int i = tid; i < 2 * p.E * 8; i += kThreads)
+      cp_async16(piece(sm.table, kPieceCache + (i >> 3)) + (i & 7) * 16,
+                 reinterpret_cast<const uint4*>(p.desc + desc_index(p.layer, i >> 4, (i >> 3) & 1, p.E)) + (i & 7));
+  cp_commit();
   __syncthreads();
   route_local(p, r, &s_int[0], kTokPass);   // reads only logits and descriptors
   pl.nact = r.lpt[0];
@@ -499,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
+  cp_wait<0>();   // the descriptor cache
   __syncthreads();
   pl.cum_gu = cum_gu;
   pl.cum_dn = cum_dn;
@@ -514,10 +536,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   __syncthreads();
   if (warp == 0 && lane < 16) {
     const int sl = lane >> 3, part = lane & 7;
-    if (s_item[sl].valid) {
-      const uint4* src = reinterpret_cast<const uint4*>(block_desc(p, s_item[sl].expert, s_item[sl].kind));
-      reinterpret_cast<uint4*>(piece(sm.table, kPieceDesc + sl))[part] = ld_nc16(src + part);
-    }
+    if (s_item[sl].valid)
+      reinterpret_cast<uint4*>(piece(sm.table, kPieceDesc + sl))[part] =
+          desc_part(p, sm, cached, s_item[sl].expert, s_item[sl].kind, part);
   }
   __syncthreads();
   const uint32_t ring = ring_of(sm, warp);
@@ -529,12 +550,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     const BlockDesc& d0 = *reinterpret_cast<const BlockDesc*>(piece(sm.table, kPieceDesc));
     int rho, rho2;
     lane_rows(p, s_item[0], lane, rho, rho2);
-    if (desc_ok(p, d0, s_item[0].kind)) {
-      lut_load(lr, d0, rho, rho2, warp);
-      lut_store(sm.table, lr, d0.q, lane, warp);
-    }
+    const bool ok0 = desc_ok(p, d0, s_item[0].kind);
+    if (ok0) lut_load(lr, d0, rho, rho2, warp);
     fetch_enter(f, p, sm, 0, warp, lane);
     fetch_fill(f, p, sm, n_items, 1, consumed, issued, warp, lane, ring);
+    if (ok0) lut_store(sm.table, lr, d0.q, lane, warp);
   }
 
   // the previous kernel on the stream (possibly the previous forward, using the
@@ -588,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
       if (lane == 0) s_item[sl2] = item_of(b + (i + 2) * G, pl, r);
       __syncwarp();
       if (lane < 8 && s_item[sl2].valid)
-        dnext = ld_nc16(reinterpret_cast<const uint4*>(block_desc(p, s_item[sl2].expert, s_item[sl2].kind)) + lane);
+        dnext = desc_part(p, sm, cached, s_item[sl2].expert, s_item[sl2].kind, lane);
     }
     // item i+1's tables, into registers until this item's lookups are done
     const int sl1 = (i + 1) % kSlots;

@@ -270,21 +270,35 @@ __device__ __forceinline__ void route_local(const Fwd& p, const RouteSmem& r, in
     }
   }
   __syncthreads();
-  for (int e = warp; e < E; e += nwarp) {
-    int run = 0;
-    for (int base = 0; base < T; base += 32) {
-      const int t = base + lane;
-      int jsel = -1;
-      if (t < T)
-        for (int j = 0; j < k; ++j)
-          if (r.idx[t * k + j] == e) jsel = j;
-      const unsigned mask = __ballot_sync(0xffffffffu, jsel >= 0);
-      if (jsel >= 0) {
-        const int pos = r.off[e] + run + __popc(mask & ((1u << lane) - 1u));
-        r.perm[pos] = t * k + jsel;
-        r.inv[t * k + jsel] = pos;
+  if (T <= 16) {
+    // small batches: one thread per pair; its place among the expert's pairs is
+    // the number of earlier tokens routed to the same expert (a token's top-k
+    // experts are distinct)
+    for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+      const int t = i / k, e = r.idx[i];
+      int rank = 0;
+      for (int i2 = 0; i2 < t * k; ++i2) rank += (r.idx[i2] == e);
+      const int pos = r.off[e] + rank;
+      r.perm[pos] = i;
+      r.inv[i] = pos;
+    }
+  } else {
+    for (int e = warp; e < E; e += nwarp) {
+      int run = 0;
+      for (int base = 0; base < T; base += 32) {
+        const int t = base + lane;
+        int jsel = -1;
+        if (t < T)
+          for (int j = 0; j < k; ++j)
+            if (r.idx[t * k + j] == e) jsel = j;
+        const unsigned mask = __ballot_sync(0xffffffffu, jsel >= 0);
+        if (jsel >= 0) {
+          const int pos = r.off[e] + run + __popc(mask & ((1u << lane) - 1u));
+          r.perm[pos] = t * k + jsel;
+          r.inv[t * k + jsel] = pos;
+        }
+        run += __popc(mask);
       }
-      run += __popc(mask);
     }
   }
   // active experts by gate_up cost, largest first (ties keep expert order)
