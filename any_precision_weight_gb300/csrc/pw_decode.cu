@@ -662,15 +662,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
         fetch_fill(f, p, sm, n_items, i + 1, consumed, issued, warp, lane, ring);
         const uint32_t st = ring + (consumed % kStages) * kStageBytes + lane * 8;
         ++consumed;
-#pragma unroll 1
+        uint2 pv0[8], pv1[8];
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+          asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(pv0[rr].x), "=r"(pv0[rr].y) : "r"(st + (7 - rr) * 512));
+          asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(pv1[rr].x), "=r"(pv1[rr].y) : "r"(st + (7 - rr) * 512 + 256));
+        }
+#pragma unroll
         for (int wi = 0; wi < kUnitWords; ++wi) {
           const int gw = u * kUnitWords + wi;
           uint32_t o0[8], o1[8];
-          const uint32_t sw = st + wi * 4;
 #pragma unroll
-          for (int rr = 0; rr < 8; ++rr) {   // o[rr] = plane (Q-1-rr) of the row (zero for rr >= Q)
-            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(o0[rr]) : "r"(sw + (7 - rr) * 512));
-            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(o1[rr]) : "r"(sw + (7 - rr) * 512 + 256));
+          for (int rr = 0; rr < 8; ++rr) {
+            o0[rr] = wi ? pv0[rr].y : pv0[rr].x;
+            o1[rr] = wi ? pv1[rr].y : pv1[rr].x;
           }
           planes_to_indices(o0);
           planes_to_indices(o1);
