@@ -16,13 +16,15 @@
 //    then all down tiles) and dealt round-robin to the CTAs, so every CTA knows
 //    its next items and loads their descriptors and tables ahead of time;
 //  * lane l of every warp owns two rows of the tile (gate row l and up row l,
-//    or rows l and 32 + l); the eight warps split K.  The two rows' q-bit
+//    or rows l and 32 + l); the twelve warps split K.  The two rows' q-bit
 //    tables sit in shared memory as one 32-bit slot per (index, lane) holding
 //    both rows' fp16 entries, so a warp's 32 lookups hit 32 different banks
 //    whatever the indices;
-//  * each warp streams its own plane words through a private three-stage
-//    cp.async ring that runs on into the warp's share of the next item, so
-//    the HBM stream does not stop at item boundaries;
+//  * each warp streams its own plane words through a private two-stage
+//    cp.async ring (one coalesced 16-byte copy per lane and plane, the pages
+//    being interleaved across 32-row groups) that runs on into the warp's
+//    share of the next item, so the HBM stream does not stop at item
+//    boundaries;
 //  * per 32-bit plane word, a lane turns q plane words into 32 indices with an
 //    8x8 bit transpose (delta swaps), one byte permute per weight forms the
 //    table address, and the looked-up fp16 weights go straight from registers
@@ -33,7 +35,7 @@
 //    two tokens (a second MMA adds tokens 2 and 3).  The MMA does the
 //    multiply-adds that would otherwise cost two fp32 instructions per weight
 //    and token;
-//  * the eight K-warps' partial sums are added in a fixed order (bitwise
+//  * the K-warps' partial sums are added in a fixed order (bitwise
 //    deterministic); gate_up items finish with h = silu(gate) * up (fp16),
 //    down items with fp32 y rows; the last down item of a 64-row output tile
 //    combines it.

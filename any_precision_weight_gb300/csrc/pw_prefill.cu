@@ -328,8 +328,15 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
     // the previous item's dequant steps and epilogue are done by every dequant thread
     named_sync_dq();
     // the tile's table: LUT_q[row][v] fp16 -> lut_s[v][row]
+    // (rows of fewer than 8 entries, q < 3, are not 16-byte aligned: 2-byte loads)
+    if (V < 8) {
+      if (half == 0)
+        for (int v = 0; v < V; ++v)
+          reinterpret_cast<uint16_t*>(lut_s)[v * kBN + row] =
+              grow >= 0 ? __ldg(d.lut + static_cast<size_t>(grow) * V + v) : static_cast<uint16_t>(0);
+    }
     // four 16-byte loads in flight per thread before their values are stored
-    for (int vc0 = half; vc0 * 8 < V; vc0 += 8) {
+    for (int vc0 = half; V >= 8 && vc0 * 8 < V; vc0 += 8) {
       uint4 raw[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {

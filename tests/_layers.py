@@ -23,15 +23,17 @@ class SynthBlocks:
                 synth.parent_lut(self.cfg, self.layer, e, kind))
 
 
-def gpu_layer(cfg, n_layers=1, bits=None, blocks=None, alloc_planes=None, layers=None, per_plane=False):
-    """A PagedMoE with the given layers registered.  bits[l] -> [E][2]."""
+def gpu_layer(cfg, n_layers=1, bits=None, blocks=None, alloc_planes=None, layers=None, per_plane=False,
+              b_min=3):
+    """A PagedMoE with the given layers registered.  bits[l] -> [E][2]; b_min:
+    the lowest bitwidth whose tables are stored."""
     import any_precision_weight_gb300 as pw
     from any_precision_weight_gb300.model import load_expert_layer
     m = pw.PagedMoE(n_layers, cfg.E, cfg.H, cfg.I)
     for l in (range(n_layers) if layers is None else layers):
         b = synth.block_bits(cfg, l) if bits is None else bits[l]
         src = SynthBlocks(cfg, l) if blocks is None else blocks[l]
-        load_expert_layer(m, l, src, b, alloc_planes=alloc_planes, per_plane=per_plane)
+        load_expert_layer(m, l, src, b, alloc_planes=alloc_planes, per_plane=per_plane, b_min=b_min)
     return m
 
 

@@ -104,3 +104,10 @@ def test_tile_planes_rejects_bad_shapes():
         pw.pw_tile_planes(np.zeros((1, 48, 2), dtype=np.uint32))      # R % 32
     with pytest.raises(pw.PWError):
         pw.pw_tile_planes(np.zeros((1, 32, 3), dtype=np.uint32))      # K % 64
+
+
+def test_tile_planes_threaded_path_matches_oracle():
+    """A block large enough for the multi-threaded reordering (2^20 words and more)."""
+    rng = np.random.default_rng(5)
+    planes = rng.integers(0, 1 << 32, size=(8, 1024, 2048 // 32), dtype=np.uint64).astype(np.uint32)
+    assert np.array_equal(pw.pw_tile_planes(planes), apl.tile_planes(planes))

@@ -54,6 +54,27 @@ def test_tiny_every_bitwidth(q):
     assert_close(out, ref["out"])
 
 
+@pytest.mark.parametrize("cfg_name", ["tiny", "prefill_small"])
+def test_one_and_two_bit_blocks(cfg_name):
+    """Blocks committed at 1 and 2 bits (tables of 2 and 4 entries per row, below
+    the 8-entry chunks the kernels otherwise load), mixed with higher bitwidths,
+    on the decode kernel (tiny) and on the tensor-core path (300 tokens)."""
+    if cfg_name == "tiny":
+        cfg = synth.CONFIGS["tiny"]
+    else:
+        cfg = synth.CONFIGS["mixtral_prefill"].with_(T=300, H=256, I=512)
+    rng = np.random.default_rng(7)
+    bits = rng.integers(1, 9, size=(cfg.E, 2)).astype(np.int32)
+    bits[0] = (1, 2)
+    bits[1] = (2, 1)
+    m = gpu_layer(cfg, bits={0: bits}, b_min=1)
+    x, L = synth.tokens(cfg, step=11), synth.logits(cfg, step=11)
+    out, ri, rw, ro, rp = _run(m, cfg, x, L)
+    ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), bits))
+    _check_routing(ref, ri, rw, ro, rp)
+    assert_close(out, ref["out"])
+
+
 def test_integer_tables_bit_exact():
     """Integer tables whose child table at the committed q is integer, 0/1 tokens
     with 19 ones, top-1 routing: gate sums lie in [38, 57], where e^-g is below
