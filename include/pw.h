@@ -414,6 +414,14 @@ size_t pw_workspace_bytes(int T, int E, int top_k, int H, int I);
  * `compute` and never waits.  Arithmetic: fp16 in, fp32 accumulate, h kept in fp16,
  * y in fp32, out rounded to fp16.  A NaN logit is reported through the workspace
  * status word (see pw_workspace_status), not through the return value.
+ * Decode-sized batches (T <= 64, T*top_k <= 256) run as one kernel launched with
+ * programmatic dependent launch: it may start while the previous kernel on
+ * `compute` is still running, and reads the logits and the block descriptors
+ * before it waits for that kernel (it touches x, residual, out and the
+ * workspace only after).  Kernels that finish before their dependents start
+ * (every ordinary launch, and this library's own kernels) are safe producers
+ * of the logits; a kernel that releases its dependents early must have written
+ * the logits before it does.
  * Errors: PW_EINVAL (shapes, unregistered block, misaligned pointer), PW_ENOMEM
  * (workspace too small), PW_ECUDA.
  */
