@@ -418,10 +418,11 @@ size_t pw_workspace_bytes(int T, int E, int top_k, int H, int I);
  * programmatic dependent launch: it may start while the previous kernel on
  * `compute` is still running, and reads the logits and the block descriptors
  * before it waits for that kernel (it touches x, residual, out and the
- * workspace only after).  Kernels that finish before their dependents start
- * (every ordinary launch, and this library's own kernels) are safe producers
- * of the logits; a kernel that releases its dependents early must have written
- * the logits before it does.
+ * workspace only after).  A kernel that lets its dependents start only when
+ * it completes (every ordinary launch, and this library's commit kernels) is a
+ * safe producer of the logits or descriptors; a kernel that releases its
+ * dependents early must have written the logits before it does.  (The forward
+ * itself releases its dependents at once; it writes neither.)
  * Errors: PW_EINVAL (shapes, unregistered block, misaligned pointer), PW_ENOMEM
  * (workspace too small), PW_ECUDA.
  */
