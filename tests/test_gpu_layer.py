@@ -336,6 +336,20 @@ def test_fused_path_boundary(T):
     assert_close(out, ref["out"])
 
 
+@pytest.mark.parametrize("E", [78, 79])
+def test_descriptor_cache_boundary(E):
+    """The decode kernel keeps every block descriptor of the layer in shared
+    memory while 2E descriptors fit (E <= 78) and reads them per item from
+    global memory above that; both sides of the boundary against the oracle."""
+    cfg = synth.CONFIGS["tiny"].with_(E=E, T=24, top_k=3, H=128, I=256)
+    m = gpu_layer(cfg)
+    x, L = synth.tokens(cfg), synth.logits(cfg)
+    out, ri, rw, ro, rp = _run(m, cfg, x, L)
+    ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg)))
+    _check_routing(ref, ri, rw, ro, rp)
+    assert_close(out, ref["out"])
+
+
 def test_largest_expert_count_and_pair_count():
     # E = 256 experts (the routing's limit) and T * k = 256 pairs (the fused kernel's limit)
     cfg = synth.CONFIGS["tiny"].with_(E=256, T=32, top_k=8, H=128, I=128)
