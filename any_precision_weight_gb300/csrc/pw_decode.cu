@@ -262,46 +262,75 @@ struct LutRegs {
 
 __device__ __forceinline__ void lut_load(LutRegs& f, const BlockDesc& d, int rho, int rho2, int wv) {
   const int q = d.q, V = 1 << q;
-  if (V >= 8) {
-    const uint4* ra = reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(rho) * V);
-    const uint4* rb = reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(rho2) * V);
-#pragma unroll
-    for (int j = 0; j < kLutChunks; ++j) {
-      const int vc = wv + kWarps * j;
-      if (vc * 8 < V) {
-        f.a[j] = ld_nc16(ra + vc);
-        f.b[j] = ld_nc16(rb + vc);
+  if (q <= 3) {   // pair tables: every thread holds both rows' whole tables
+    f.a[0] = f.b[0] = make_uint4(0u, 0u, 0u, 0u);
+    if (V == 8) {
+      f.a[0] = ld_nc16(reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(rho) * V));
+      f.b[0] = ld_nc16(reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(rho2) * V));
+    } else {   // 2 or 4 entries per row
+      const uint32_t* ra = reinterpret_cast<const uint32_t*>(d.lut + static_cast<size_t>(rho) * V);
+      const uint32_t* rb = reinterpret_cast<const uint32_t*>(d.lut + static_cast<size_t>(rho2) * V);
+      f.a[0].x = __ldg(ra);
+      f.b[0].x = __ldg(rb);
+      if (V == 4) {
+        f.a[0].y = __ldg(ra + 1);
+        f.b[0].y = __ldg(rb + 1);
       }
     }
-  } else if (wv == 0) {   // 2 or 4 entries per row
-    uint32_t wa[2] = {0u, 0u}, wb[2] = {0u, 0u};
-    const uint32_t* ra = reinterpret_cast<const uint32_t*>(d.lut + static_cast<size_t>(rho) * V);
-    const uint32_t* rb = reinterpret_cast<const uint32_t*>(d.lut + static_cast<size_t>(rho2) * V);
-    for (int w = 0; w < V / 2; ++w) {
-      wa[w] = __ldg(ra + w);
-      wb[w] = __ldg(rb + w);
-    }
-    f.a[0] = make_uint4(wa[0], wa[1], 0u, 0u);
-    f.b[0] = make_uint4(wb[0], wb[1], 0u, 0u);
+    return;
   }
-}
-
-// Slot (v, lane) = (row rho entry v) | (row rho2 entry v) << 16.
-__device__ __forceinline__ void lut_store(unsigned char* table, const LutRegs& f, int q, int lane, int wv) {
-  const int V = 1 << q;
+  const uint4* ra = reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(rho) * V);
+  const uint4* rb = reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(rho2) * V);
 #pragma unroll
   for (int j = 0; j < kLutChunks; ++j) {
     const int vc = wv + kWarps * j;
-    if (vc * 8 < V || (j == 0 && vc == 0)) {
+    if (vc * 8 < V) {
+      f.a[j] = ld_nc16(ra + vc);
+      f.b[j] = ld_nc16(rb + vc);
+    }
+  }
+}
+
+// q >= 4: slot (v, lane) = (row rho entry v) | (row rho2 entry v) << 16 in line
+// v.  q <= 3 (pair tables, indexed by a | b << 4 for two neighbouring weights'
+// indices a, b < 8): line a | b << 4 holds (rho entry a) | (rho entry b) << 16,
+// line (a | b << 4) + 128 the same for rho2; warp wv fills the lines of a = wv.
+__device__ __forceinline__ void lut_store(unsigned char* table, const LutRegs& f, int q, int lane, int wv) {
+  const int V = 1 << q;
+  if (q <= 3) {
+    const uint32_t wa[4] = {f.a[0].x, f.a[0].y, f.a[0].z, f.a[0].w};
+    const uint32_t wb[4] = {f.b[0].x, f.b[0].y, f.b[0].z, f.b[0].w};
+    const int a = wv;
+    if (a < V) {
+      // entry a of each row (a warp-uniform index: a funnel of selects)
+      const uint32_t ta = (a & 4) ? ((a & 2) ? wa[3] : wa[2]) : ((a & 2) ? wa[1] : wa[0]);
+      const uint32_t tb = (a & 4) ? ((a & 2) ? wb[3] : wb[2]) : ((a & 2) ? wb[1] : wb[0]);
+      const uint32_t la = (a & 1) ? ta >> 16 : ta & 0xFFFFu;
+      const uint32_t lb = (a & 1) ? tb >> 16 : tb & 0xFFFFu;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        if (b < V) {
+          const uint32_t ha = (b & 1) ? (wa[b >> 1] & 0xFFFF0000u) : (wa[b >> 1] << 16);
+          const uint32_t hb = (b & 1) ? (wb[b >> 1] & 0xFFFF0000u) : (wb[b >> 1] << 16);
+          unsigned char* line = table + (a | (b << 4)) * kLine + lane * 4;
+          *reinterpret_cast<uint32_t*>(line) = la | ha;
+          *reinterpret_cast<uint32_t*>(line + 128 * kLine) = lb | hb;
+        }
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < kLutChunks; ++j) {
+    const int vc = wv + kWarps * j;
+    if (vc * 8 < V) {
       const uint32_t aw[4] = {f.a[j].x, f.a[j].y, f.a[j].z, f.a[j].w};
       const uint32_t bw[4] = {f.b[j].x, f.b[j].y, f.b[j].z, f.b[j].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int v = vc * 8 + 2 * e;
-        if (v < V) {
-          *reinterpret_cast<uint32_t*>(table + v * kLine + lane * 4) = prmt(aw[e], bw[e], 0x5410u);
-          *reinterpret_cast<uint32_t*>(table + (v + 1) * kLine + lane * 4) = prmt(aw[e], bw[e], 0x7632u);
-        }
+        *reinterpret_cast<uint32_t*>(table + v * kLine + lane * 4) = prmt(aw[e], bw[e], 0x5410u);
+        *reinterpret_cast<uint32_t*>(table + (v + 1) * kLine + lane * 4) = prmt(aw[e], bw[e], 0x7632u);
       }
     }
   }
@@ -342,6 +371,33 @@ __device__ __forceinline__ void word_mma(const uint32_t (&o0)[8], const uint32_t
       a[1] = prmt(t[4 * hh + 0], t[4 * hh + 1], 0x7632u);   // row rho2
       a[2] = prmt(s[4 * hh + 2], s[4 * hh + 3], 0x5410u);
       a[3] = prmt(t[4 * hh + 2], t[4 * hh + 3], 0x7632u);
+      mma16816(acc[0][hh], a, hh ? X0[bb].z : X0[bb].x, hh ? X0[bb].w : X0[bb].y);
+      mma16816(acc[1][hh], a, hh ? X1[bb].z : X1[bb].x, hh ? X1[bb].w : X1[bb].y);
+    }
+    ld_x16(X0[bb], x0n + bb, p0);
+    ld_x16(X1[bb], x1n + bb, p1);
+  }
+}
+
+// The same for a q <= 3 block with pair tables: byte bb of o[r], r even, is
+// the pair index of elements 8bb + r and 8bb + r + 1 (the transposes' upper
+// rows are the plane words shifted by one element), so one lookup returns both
+// fp16 weights of an A-register and no packing is needed; row rho2's indices
+// carry bit 7 (its table sits 128 lines up).
+__device__ __forceinline__ void word_mma_pair(const uint32_t (&o0)[8], const uint32_t (&o1)[8], uint32_t laneoff,
+                                              uint4 (&X0)[4], uint4 (&X1)[4],
+                                              const uint4* x0n, const uint4* x1n, bool p0, bool p1,
+                                              float (&acc)[2][2][4]) {
+#pragma unroll
+  for (int bb = 0; bb < 4; ++bb) {
+    const uint32_t sel = 0x7604u | (static_cast<uint32_t>(bb) << 4);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t a[4];
+      a[0] = lut_slot(prmt(o0[4 * hh + 0], laneoff, sel));    // row rho, elements 8bb+4hh+{0,1}
+      a[2] = lut_slot(prmt(o0[4 * hh + 2], laneoff, sel));    // row rho, elements +{2,3}
+      a[1] = lut_slot(prmt(o1[4 * hh + 0], laneoff, sel));    // row rho2
+      a[3] = lut_slot(prmt(o1[4 * hh + 2], laneoff, sel));
       mma16816(acc[0][hh], a, hh ? X0[bb].z : X0[bb].x, hh ? X0[bb].w : X0[bb].y);
       mma16816(acc[1][hh], a, hh ? X1[bb].z : X1[bb].x, hh ? X1[bb].w : X1[bb].y);
     }
@@ -658,12 +714,41 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
         ld_x16(X0[k4], xr[0] + w0 * 4 + k4, xr[0] != nullptr);
         ld_x16(X1[k4], xr[1] + w0 * 4 + k4, xr[1] != nullptr);
       }
+      const bool pairq = d.q <= 3;
       for (int u = u0; u < u1; ++u) {
         cp_wait_n(issued - consumed - 1);
         __syncwarp();   // every lane's copies of this stage visible; the previous stage is read
         fetch_fill(f, p, sm, n_items, i + 1, consumed, issued, warp, lane, ring);
         const uint32_t st = ring + (consumed % kStages) * kStageBytes + lane * 8;
         ++consumed;
+        if (pairq) {   // q <= 3: the q plane words sit in slots 7..5
+          uint2 pa[4], pb[4];
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(pa[rr].x), "=r"(pa[rr].y) : "r"(st + (7 - rr) * 512));
+            asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(pb[rr].x), "=r"(pb[rr].y) : "r"(st + (7 - rr) * 512 + 256));
+          }
+#pragma unroll
+          for (int wi = 0; wi < kUnitWords; ++wi) {
+            const int gw = u * kUnitWords + wi;
+            uint32_t o0[8], o1[8];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+              o0[rr] = wi ? pa[rr].y : pa[rr].x;
+              o1[rr] = wi ? pb[rr].y : pb[rr].x;
+              o0[rr + 4] = o0[rr] >> 1;
+              o1[rr + 4] = o1[rr] >> 1;
+            }
+            planes_to_indices(o0);
+            planes_to_indices(o1);
+#pragma unroll
+            for (int rr = 0; rr < 8; rr += 2) o1[rr] |= 0x80808080u;   // rho2's table: lines + 128
+            const bool more = gw + 1 < w1;
+            word_mma_pair(o0, o1, laneoff, X0, X1, xr[0] + (gw + 1) * 4, xr[1] + (gw + 1) * 4,
+                          more && xr[0] != nullptr, more && xr[1] != nullptr, acc);
+          }
+          continue;
+        }
         uint2 pv0[8], pv1[8];
 #pragma unroll
         for (int rr = 0; rr < 8; ++rr) {
