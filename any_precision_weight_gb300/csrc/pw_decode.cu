@@ -35,10 +35,13 @@
 //    two tokens (a second MMA adds tokens 2 and 3).  The MMA does the
 //    multiply-adds that would otherwise cost two fp32 instructions per weight
 //    and token;
+//  * blocks of at most 3 bits use pair tables: the transposes' upper rows take
+//    the plane words shifted by one element, so one lookup returns two
+//    neighbouring weights already packed for the MMA;
 //  * the K-warps' partial sums are added in a fixed order (bitwise
 //    deterministic); gate_up items finish with h = silu(gate) * up (fp16),
-//    down items with fp32 y rows; the last down item of a 64-row output tile
-//    combines it.
+//    down items with fp32 y rows; the CTA whose down item completes a 64-row
+//    output tile combines it at its next item boundary.
 
 #include <cuda_fp16.h>
 #include <cstdint>
