@@ -31,6 +31,7 @@ PW_EDEVICE = -7
 PW_STATUS_NAN_LOGIT = 1
 PW_STATUS_TIMEOUT = 2
 PW_STATUS_BAD_DESC = 4
+PW_WS_H, PW_WS_Y = 0, 1
 PW_PLANE_HOST, PW_PLANE_HOST_PAGED, PW_PLANE_MOVING, PW_PLANE_DEVICE = 0, 1, 2, 3
 KIND_GATE_UP = 0
 KIND_DOWN = 1
@@ -65,10 +66,12 @@ _SIGS = {
     "pw_table_destroy": (_i, [_vp]),
     "pw_debug_fail_next_reload": (_i, [_vp]),
     "pw_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "pw_workspace_offset": (_sz, [_i, _i, _i, _i, _i, _i]),
     "pw_moe_forward": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "pw_moe_forward_host": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "pw_workspace_status": (_i, [_vp, _vp, _pi]),
     "pw_moe_forward_noalloc": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp]),
+    "pw_noalloc_status": (_i, [_vp, _pi]),
     "pw_profile_attach": (_i, [ctypes.POINTER(_vp), _i]),
     "pw_stats_attach": (_i, [_vp, _vp, ctypes.c_float]),
     "pw_plan_bits": (_i, [_i, _vp, _vp, _vp, _vp, _vp, _i, ctypes.c_double, _i, _i, _i, ctypes.c_double,
@@ -378,6 +381,20 @@ class PagedMoE:
     def pw_debug_fail_next_reload(self):
         return _check(lib().pw_debug_fail_next_reload(self._t), "pw_debug_fail_next_reload")
 
+    def workspace_h(self, ws, T: int, top_k: int):
+        """h (fp16 [T*top_k][I], permuted pair order) left in `ws` by the last forward."""
+        import torch
+        off = lib().pw_workspace_offset(T, self.E, top_k, self.H, self.I, PW_WS_H)
+        n = T * top_k * self.I * 2
+        return ws[off:off + n].view(torch.float16).view(T * top_k, self.I)
+
+    def workspace_y(self, ws, T: int, top_k: int):
+        """y (fp32 [T*top_k][H], permuted pair order) left in `ws` by the last forward."""
+        import torch
+        off = lib().pw_workspace_offset(T, self.E, top_k, self.H, self.I, PW_WS_Y)
+        n = T * top_k * self.H * 4
+        return ws[off:off + n].view(torch.float32).view(T * top_k, self.H)
+
     def workspace(self, T: int, top_k: int):
         import torch
         nb = lib().pw_workspace_bytes(T, self.E, top_k, self.H, self.I)
@@ -436,6 +453,13 @@ class PagedMoE:
         st = _i()
         _check(lib().pw_workspace_status(_ptr(ws), _stream(stream), ctypes.byref(st)),
                "pw_workspace_status")
+        return st.value
+
+    @staticmethod
+    def noalloc_status(stream=None) -> int:
+        """Status bits of the last pw_moe_forward_noalloc ordered before `stream`'s work."""
+        st = _i()
+        _check(lib().pw_noalloc_status(_stream(stream), ctypes.byref(st)), "pw_noalloc_status")
         return st.value
 
     def close(self):

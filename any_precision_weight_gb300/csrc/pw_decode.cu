@@ -438,15 +438,15 @@ __device__ __forceinline__ void fetch_enter(Fetch& f, const Fwd& p, const Smem& 
 }
 
 // Issues ring stages until kStages units are in flight or the next unit
-// belongs to an item whose descriptor is not in shared memory yet
-// (items up to `known`).  `issued` counts units issued by this warp.  The
-// caller has synchronised the warp after the last read of the stage that the
-// next issue overwrites.
-__device__ __forceinline__ void fetch_fill(Fetch& f, const Fwd& p, const Smem& sm, int n_items, int known,
-                                           int consumed, int& issued, int warp, int lane, uint32_t ring) {
+// belongs to an item that is not known yet (an item is known once its
+// descriptor is in shared memory and it exists: items up to `known`).
+// `issued` counts units issued by this warp.  The caller has synchronised the
+// warp after the last read of the stage that the next issue overwrites.
+__device__ __forceinline__ void fetch_fill(Fetch& f, const Fwd& p, const Smem& sm, int known, int consumed,
+                                           int& issued, int warp, int lane, uint32_t ring) {
   while (issued < consumed + kStages) {
     while (f.u == f.end) {   // the warp has no more units in this item
-      if (f.item + 1 > known || f.item + 1 >= n_items) return;
+      if (f.item + 1 > known) return;
       fetch_enter(f, p, sm, f.item + 1, warp, lane);
     }
     // plane p of a q-plane item goes to stage slot 8 - q + p, so that plane
@@ -494,18 +494,7 @@ __device__ __forceinline__ int atom_acq_rel_add(int* ptr, int v) {
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
   return old;
 }
-__device__ __forceinline__ void st_release(int* ptr, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
-}
-// Bounded waits (one thread): true once *ptr == want (resp. >= want), false
-// when the limit runs out.
-__device__ bool wait_eq(const int* ptr, int want) {
-  for (int i = 0; i < kSpinLimit; ++i) {
-    if (ld_acquire(ptr) == want) return true;
-    __nanosleep(64);
-  }
-  return false;
-}
+// Bounded wait (one thread): true once *ptr >= want, false when the limit runs out.
 __device__ bool wait_ge(const int* ptr, int want) {
   for (int i = 0; i < kSpinLimit; ++i) {
     if (ld_acquire(ptr) >= want) return true;
@@ -514,14 +503,45 @@ __device__ bool wait_ge(const int* ptr, int want) {
   return false;
 }
 
+// The item a ticket-word update returned: its count under this forward's tag,
+// or -1 when the word holds another tag or the set-up sentinel.
+__device__ __forceinline__ int ticket_of(const Fwd& p, unsigned long long old) {
+  if ((old & ~kCountMask) != p.tag) return -1;
+  const unsigned long long c = old & kCountMask;
+  return c == kSetupCount ? -1 : static_cast<int>(c);
+}
+
+// First claim of a CTA (one thread), right after the dependency wait: the
+// first CTA to find the ticket word under another tag sets the forward up
+// (returns 1; the caller resets the counters and then publishes the count);
+// every other CTA waits (bounded) for the published tag and takes two tickets
+// (returns 0 with *first = the first ticket, or -1 when the wait gave up).
+__device__ int claim_first(const Fwd& p, int* first) {
+  unsigned long long v = ld_acquire_u64(p.sync);
+  if ((v & ~kCountMask) != p.tag && cas_acq_rel_u64(p.sync, v, p.tag | kSetupCount) == v) return 1;
+  for (int i = 0; i < kSpinLimit; ++i) {
+    v = ld_acquire_u64(p.sync);
+    if ((v & ~kCountMask) == p.tag && (v & kCountMask) != kSetupCount) {
+      *first = ticket_of(p, add_relaxed_u64(p.sync, 2));
+      return *first >= 0 ? 0 : -1;
+    }
+    __nanosleep(64);
+  }
+  return -1;
+}
+
 // One persistent launch (one CTA per SM, the co-resident grid) for the whole
 // decode layer.  Every CTA routes the batch itself into shared memory (a few
 // hundred logits, so no CTA waits for another's routing) and derives the
-// layer's item order from it; CTA b takes items b, b + G, b + 2G, ...  Down
-// items wait until their expert's gate_up items are done (all gate_up items
-// precede all down items, and no CTA waits while it still holds a gate_up
-// item, so the waits end); the last down item of a 64-row output tile combines
-// it.  Every wait is bounded and reports PW_STATUS_TIMEOUT instead of hanging.
+// layer's item order from it.  The items are handed out in that order by
+// tickets: a CTA claims two at its start and one more at the start of each
+// item, and works through its items in claim order.  Down items wait until
+// their expert's gate_up items are done; all gate_up items precede all down
+// items in the order, so every awaited item has been claimed by a CTA that is
+// running and that reaches it without waiting on anything: the waits end
+// whichever CTAs are resident.  The last down item of a 64-row output tile
+// combines it.  Every wait is bounded and reports PW_STATUS_TIMEOUT instead of
+// hanging.
 __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const Smem sm = smem_layout();
@@ -544,8 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   Plan pl;
   pl.tiles_gu = p.I / kGateUpTileRows;
   pl.tiles_dn = p.H / kDownTileRows;
-  int* expert_done = p.sync + 2;
-  int* tile_done = p.sync + 2 + p.E;
+  int* expert_done = reinterpret_cast<int*>(p.sync + 1);
+  int* tile_done = expert_done + p.E;
 
   // The launch lets the next forward on the stream start on SMs this grid frees
   // (programmatic dependent launch): that forward routes its own batch while
@@ -588,12 +608,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   pl.total_gu = cum_gu[pl.nact];
   pl.total = pl.total_gu + cum_dn[pl.nact];
   pl.down_per_tile = pl.tiles_dn > 0 ? cum_dn[pl.nact] / pl.tiles_dn : 0;
-  const int G = gridDim.x, b = blockIdx.x;
-  const int n_items = b < pl.total ? (pl.total - 1 - b) / G + 1 : 0;
 
-  // Items 0 and 1 of this CTA and their descriptors; item 0's tables and the
-  // first ring stages load before the dependency wait (weights only).
-  if (tid < 2) s_item[tid] = item_of(b + tid * G, pl, r);
+  // the previous kernel on the stream (possibly the previous forward, using the
+  // same workspace) has finished and its writes are visible after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (tid == 0) s_int[3] = claim_first(p, &s_int[2]);
+  __syncthreads();
+  const int role = s_int[3];
+  if (role == 1) {
+    // this CTA sets the forward up: counters to zero, the status word, then the
+    // ticket word's count (tickets 0 and 1 are this CTA's)
+    for (int i = tid; i < p.E + pl.tiles_dn; i += kThreads) expert_done[i] = 0;
+    if (tid == 0) p.status[0] = s_int[0] ? PW_STATUS_NAN_LOGIT : 0u;
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      st_release_u64(p.sync, p.tag | 2ull);
+      s_int[2] = 0;
+    }
+    // the routing outputs the caller asked for, and the routing statistics
+    const int P = p.T * p.k;
+    for (int i = tid; i < P; i += kThreads) {
+      if (p.user_idx) p.user_idx[i] = r.idx[i];
+      if (p.user_w) p.user_w[i] = r.w[i];
+      if (p.user_perm) p.user_perm[i] = r.perm[i];
+    }
+    if (p.user_offsets)
+      for (int e = tid; e <= p.E; e += kThreads) p.user_offsets[e] = r.off[e];
+    update_route_stats(p, r.perm, r.w, r.off);
+  } else if (role < 0) {
+    // the set-up never published (bounded wait): leave every item to the others
+    if (tid == 0) atomicOr(p.status, PW_STATUS_TIMEOUT);
+    return;
+  }
+  __syncthreads();
+  // items of the first two tickets and their descriptors
+  if (tid < 2) s_item[tid] = item_of(s_int[2] + tid, pl, r);
   __syncthreads();
   if (warp == 0 && lane < 16) {
     const int sl = lane >> 3, part = lane & 7;
@@ -607,54 +657,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   Fetch f;
   int issued = 0, consumed = 0;
   LutRegs lr;
-  if (n_items > 0) {
+  if (s_item[0].valid) {
     const BlockDesc& d0 = *reinterpret_cast<const BlockDesc*>(piece(sm.table, kPieceDesc));
     int rho, rho2;
     lane_rows(p, s_item[0], lane, rho, rho2);
     const bool ok0 = desc_ok(p, d0, s_item[0].kind);
     if (ok0) lut_load(lr, d0, rho, rho2, warp);
     fetch_enter(f, p, sm, 0, warp, lane);
-    fetch_fill(f, p, sm, n_items, 1, consumed, issued, warp, lane, ring);
+    fetch_fill(f, p, sm, s_item[1].valid ? 1 : 0, consumed, issued, warp, lane, ring);
     if (ok0) lut_store(sm.table, lr, d0.q, lane, warp);
   }
-
-  // the previous kernel on the stream (possibly the previous forward, using the
-  // same workspace) has finished and its writes are visible after this
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (b == 0) {
-    if (tid == 0) p.status[0] = s_int[0] ? PW_STATUS_NAN_LOGIT : 0u;
-    for (int i = tid; i < 1 + p.E + pl.tiles_dn; i += blockDim.x) p.sync[1 + i] = 0;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) st_release(p.sync, static_cast<int>(p.epoch));
-    // the routing outputs the caller asked for
-    const int P = p.T * p.k;
-    for (int i = tid; i < P; i += blockDim.x) {
-      if (p.user_idx) p.user_idx[i] = r.idx[i];
-      if (p.user_w) p.user_w[i] = r.w[i];
-      if (p.user_perm) p.user_perm[i] = r.perm[i];
-    }
-    if (p.user_offsets)
-      for (int e = tid; e <= p.E; e += blockDim.x) p.user_offsets[e] = r.off[e];
-    update_route_stats(p, r.perm, r.w, r.off);
-  } else {
-    if (tid == 0) {
-      const bool ok = wait_eq(p.sync, static_cast<int>(p.epoch));
-      if (!ok) atomicOr(p.status, PW_STATUS_TIMEOUT);
-      s_int[2] = ok;
-    }
-    __syncthreads();
-    if (!s_int[2]) {
-      cp_wait<0>();   // no copy outlives the CTA
-      return;
-    }
-  }
-  __syncthreads();   // the prologue's tables are complete
+  __syncthreads();   // the first item's tables are complete
 
   // thread 0: the last down item's tile and the count its update returned,
   // looked at only at the next item boundary
   int pending_tile = -1, pending_old = -1;
-  for (int i = 0; i < n_items; ++i) {
+  for (int i = 0; s_item[i % kSlots].valid; ++i) {
     const int sl = i % kSlots;
     const ItemInfo it = s_item[sl];
     const BlockDesc& d = *reinterpret_cast<const BlockDesc*>(piece(sm.table, kPieceDesc + sl));
@@ -662,20 +680,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     const bool ok = desc_ok(p, d, it.kind);
     if (!ok && tid == 0) atomicOr(p.status, PW_STATUS_BAD_DESC);
 
-    // item i+2: where it is and its descriptor (stored at the end of this item)
-    uint4 dnext = make_uint4(0u, 0u, 0u, 0u);
-    const int sl2 = (i + 2) % kSlots;
-    if (warp == 0) {
-      if (lane == 0) s_item[sl2] = item_of(b + (i + 2) * G, pl, r);
-      __syncwarp();
-      if (lane < 8 && s_item[sl2].valid)
-        dnext = desc_part(p, sm, cached, s_item[sl2].expert, s_item[sl2].kind, lane);
-    }
-    // item i+1's tables, into registers until this item's lookups are done
-    const int sl1 = (i + 1) % kSlots;
+    // item i+2's ticket: claimed now, looked at when this item ends
+    const int sl1 = (i + 1) % kSlots, sl2 = (i + 2) % kSlots;
     const ItemInfo it1 = s_item[sl1];
+    unsigned long long claim = 0;
+    if (tid == 0 && it1.valid) claim = add_relaxed_u64(p.sync, 1);
+    const int known = it1.valid ? i + 1 : i;   // the ring may run into item i+1
+    // item i+1's tables, into registers until this item's lookups are done
     const BlockDesc& d1 = *reinterpret_cast<const BlockDesc*>(piece(sm.table, kPieceDesc + sl1));
-    const bool ok1 = i + 1 < n_items && it1.valid && desc_ok(p, d1, it1.kind);
+    const bool ok1 = it1.valid && desc_ok(p, d1, it1.kind);
     if (ok1) {
       int rho, rho2;
       lane_rows(p, it1, lane, rho, rho2);
@@ -721,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
       for (int u = u0; u < u1; ++u) {
         cp_wait_n(issued - consumed - 1);
         __syncwarp();   // every lane's copies of this stage visible; the previous stage is read
-        fetch_fill(f, p, sm, n_items, i + 1, consumed, issued, warp, lane, ring);
+        fetch_fill(f, p, sm, known, consumed, issued, warp, lane, ring);
         const uint32_t st = ring + (consumed % kStages) * kStageBytes + lane * 8;
         ++consumed;
         if (pairq) {   // q <= 3: the q plane words sit in slots 7..5
@@ -777,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     }
     // keep the ring running into the next item while this one finishes
     __syncwarp();
-    fetch_fill(f, p, sm, n_items, i + 1, consumed, issued, warp, lane, ring);
+    fetch_fill(f, p, sm, known, consumed, issued, warp, lane, ring);
 
     // ---- partial sums: piece(warp * 8 + half * 4 + token)[lane]
     {
@@ -793,8 +806,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
 #pragma unroll
       for (int k8 = 0; k8 < 8; ++k8) red[k8 * (kLine / 4) + lane] = v[k8];
     }
-    // a down tile whose last item completed with the previous item: combine it now
-    if (tid == 0) s_int[1] = pending_old == pl.down_per_tile - 1 ? pending_tile : -1;
+    // a down tile whose last item completed with the previous item: combine it now;
+    // item i+2 from the ticket claimed at this item's start
+    if (tid == 0) {
+      s_int[1] = pending_old == pl.down_per_tile - 1 ? pending_tile : -1;
+      s_item[sl2] = it1.valid ? item_of(ticket_of(p, claim), pl, r) : ItemInfo{};
+    }
     __syncthreads();   // every lookup of this item is done; partials visible
     if (s_int[1] >= 0) {
       const int r0 = s_int[1] * kDownTileRows;
@@ -804,7 +821,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     pending_old = -1;
 
     if (ok1) lut_store(sm.table, lr, d1.q, lane, warp);
-    if (warp == 0 && lane < 8) reinterpret_cast<uint4*>(piece(sm.table, kPieceDesc + sl2))[lane] = dnext;
+    if (warp == 0 && lane < 8 && s_item[sl2].valid)
+      reinterpret_cast<uint4*>(piece(sm.table, kPieceDesc + sl2))[lane] =
+          desc_part(p, sm, cached, s_item[sl2].expert, s_item[sl2].kind, lane);
     auto red_at = [&](int w, int k8, int l) {
       return reinterpret_cast<const float*>(piece(sm.table, kPieceRed + w * 8 + k8))[l];
     };
@@ -875,11 +894,11 @@ cudaError_t launch_layer_fused(const Fwd& p, cudaStream_t s) {
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     g_fused[dev] = per_sm * sms;
   }
-  // An ordinary launch of exactly the co-resident grid (every wait in the kernel
-  // is on work that a running CTA has already been dealt, or on CTA 0, which is
-  // scheduled first), allowed to start while the previous kernel on the stream
-  // finishes (programmatic stream serialisation; the kernel waits for it with
-  // griddepcontrol.wait before it touches the workspace or the token rows).
+  // An ordinary launch of the co-resident grid (items are handed out by
+  // tickets, so the waits end even when only some CTAs are resident), allowed
+  // to start while the previous kernel on the stream finishes (programmatic
+  // stream serialisation; the kernel waits for it with griddepcontrol.wait
+  // before it touches the workspace or the token rows).
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g_fused[dev]);
   cfg.blockDim = dim3(kThreads);

@@ -20,7 +20,7 @@ struct Fwd {
   float* user_w;
   int32_t* user_offsets;
   int32_t* user_perm;
-  uint32_t* status;         // status word; counters follow
+  uint32_t* status;         // status word: low 32 bits of a tagged 64-bit word (see below)
   int32_t* idx;             // [T*k]
   float* w;                 // [T*k]
   int32_t* counts;          // [E]
@@ -28,11 +28,10 @@ struct Fwd {
   int32_t* perm;            // [T*k]
   int32_t* inv;             // [T*k]
   int32_t* active;          // [E+1] active experts: count, then ids (expert order)
-  int32_t* act_lpt;         // [E+1] the same, most expensive gate_up block first
-  int32_t* sync;            // fused path: [0] ready epoch, [1] work queue,
-                            // [2, 2+E) gate_up tiles done per expert, then
-                            // down items done per 32-row tile of H
-  uint32_t epoch;           // nonzero, differs between consecutive fused forwards
+  unsigned long long* sync; // fused path: [0] the ticket word; from byte 8, int32 counters:
+                            // gate_up items done per expert [E], then down items done
+                            // per 64-row tile of H
+  unsigned long long tag;   // this forward's tag (bits 24..63): never 0, never repeated
   __half* hh;               // [T*k][I] h (fp16) in permuted order
   __half* xp;               // [T*k][H] token rows in permuted (expert) order, prefill GEMMs
   float* y;                 // [T*k][H]
@@ -40,16 +39,48 @@ struct Fwd {
   float stats_alpha;        // its update weight
 };
 
-// Work-queue counters live right after the status word.
-constexpr int kCtrGateUp = 1;
-constexpr int kCtrDown = 2;
+// The fused forward's ticket word.  A forward finds its workspace as the
+// caller left it (fresh memory, an earlier forward's leftovers, anything), so
+// nothing in it can be trusted until this forward has reset it.  The ticket
+// word (64 bits) carries the forward's tag in bits 24..63 and a count in bits
+// 0..23.  The first CTA to find the word under another tag swaps in the tag
+// with the set-up sentinel as count, resets the forward's counters and status,
+// then publishes the count 0 (plus the tickets it took); every other CTA waits
+// for the published tag before it touches the workspace.  The tag is a fixed
+// byte 0xA5 above a 32-bit forward counter, so no index, count, small integer
+// or float the workspace could hold (and no earlier forward's word) reads as
+// the current tag.
+constexpr unsigned long long kTagShift = 24;
+constexpr unsigned long long kCountMask = (1ull << kTagShift) - 1;
+constexpr unsigned long long kSetupCount = kCountMask;   // "being set up"
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* ptr) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long* ptr, unsigned long long v) {
+  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long cas_acq_rel_u64(unsigned long long* ptr, unsigned long long cmp,
+                                                              unsigned long long val) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
+               : "=l"(old) : "l"(ptr), "l"(cmp), "l"(val) : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned long long add_relaxed_u64(unsigned long long* ptr, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.relaxed.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(ptr), "l"(v) : "memory");
+  return old;
+}
 
 __device__ __forceinline__ const BlockDesc* block_desc(const Fwd& p, int e, int kind) {
   return p.desc + desc_index(p.layer, e, kind, p.E);
 }
 
-// The whole decode layer (routing, gate_up, down, combine) in one cooperative
-// persistent launch; for batches of at most kFusedMaxT tokens.
+// The whole decode layer (routing, gate_up, down, combine) in one persistent
+// launch; for batches of at most kFusedMaxT tokens.
 constexpr int kFusedMaxT = 64;
 cudaError_t launch_layer_fused(const Fwd& p, cudaStream_t s);
 // Tensor-core GEMM of one block kind over all experts (prefill-sized batches);

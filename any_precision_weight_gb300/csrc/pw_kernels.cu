@@ -55,7 +55,7 @@ constexpr int kRouteThreads = 1024;
 __global__ void __launch_bounds__(kRouteThreads) k_route_permute(Fwd p) {
   __shared__ int s_cnt[kMaxE];
   __shared__ int s_off[kMaxE + 1];
-  if (threadIdx.x < 4) p.status[threadIdx.x] = 0u;   // status word and work-queue counters
+  if (threadIdx.x == 0) p.status[0] = 0u;
   __syncthreads();
   route_permute_block(p, s_cnt, s_off);
   if (p.stats) {
@@ -100,8 +100,7 @@ static Fwd make_fwd(const ForwardArgs& a) {
   p.perm = reinterpret_cast<int32_t*>(ws + a.lay.perm);
   p.inv = reinterpret_cast<int32_t*>(ws + a.lay.inv);
   p.active = reinterpret_cast<int32_t*>(ws + a.lay.active);
-  p.act_lpt = p.active + (a.E + 1);
-  p.sync = reinterpret_cast<int32_t*>(ws + a.lay.sync);
+  p.sync = reinterpret_cast<unsigned long long*>(ws + a.lay.sync);
   p.hh = reinterpret_cast<__half*>(ws + a.lay.hh);
   p.xp = reinterpret_cast<__half*>(ws + a.lay.xp);
   p.y = reinterpret_cast<float*>(ws + a.lay.y);
@@ -114,15 +113,15 @@ static inline void mark(const ForwardArgs& a, int i, cudaStream_t s) {
   if (a.prof[i]) cudaEventRecord(a.prof[i], s);
 }
 
-static std::atomic<uint32_t> g_epoch{0};
+// Forward counter of this process: each forward's tag is 0xA5 above it (the
+// fused forward's ticket word, pw_device.cuh).
+static std::atomic<uint32_t> g_forwards{0};
 
 cudaError_t launch_forward(const ForwardArgs& a, cudaStream_t s) {
   Fwd p = make_fwd(a);
+  p.tag = ((0xA5ull << 32) | ++g_forwards) << kTagShift;
   mark(a, 0, s);
   if (p.T <= kFusedMaxT && p.T * p.k <= kRouteSmemMaxPairs) {
-    uint32_t ep = ++g_epoch;
-    if (ep == 0) ep = ++g_epoch;
-    p.epoch = ep;
     const cudaError_t e = launch_layer_fused(p, s);
     for (int i = 1; i < 5; ++i) mark(a, i, s);
     return e;

@@ -964,6 +964,14 @@ size_t pw_workspace_bytes(int T, int E, int top_k, int H, int I) {
   return pw::workspace_layout(T, E, top_k, H, I).total;
 }
 
+size_t pw_workspace_offset(int T, int E, int top_k, int H, int I, int section) {
+  if (T < 0 || E < 1 || top_k < 1 || H < 1 || I < 1) return static_cast<size_t>(-1);
+  const pw::Workspace w = pw::workspace_layout(T, E, top_k, H, I);
+  if (section == PW_WS_H) return w.hh;
+  if (section == PW_WS_Y) return w.y;
+  return static_cast<size_t>(-1);
+}
+
 static int forward_checks(pw_table* t, int layer, int T, int top_k, const void* ws,
                           size_t ws_bytes) {
   if (!t) return fail(PW_EINVAL, "pw_moe_forward: null table");

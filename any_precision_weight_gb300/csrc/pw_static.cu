@@ -11,6 +11,8 @@
 // long as the process lives.  Nothing here calls cudaMalloc, cudaFree or any
 // allocating library routine.
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cstdio>
 #include <mutex>
 
@@ -27,24 +29,57 @@ constexpr size_t kStaticScratchBytes = size_t(8) << 20;   // 8 MiB per device
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchSlot {
+  unsigned long long ctx_id;   // the context the address belongs to (0: none yet)
+  void* ptr;
+};
+ScratchSlot g_scratch[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
+// Unique id of the calling thread's current context (0 when none is current or
+// the driver cannot say).  A device reset ends the context and with it the
+// array's address; the next context has another id.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 // Device address of the scratch array on the current device, looked up once per
-// device (the lookup may load this library's kernels onto the device).
+// device and context (the lookup may load this library's kernels onto the device).
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  const unsigned long long id = current_context_id();
+  ScratchSlot& sl = g_scratch[dev];
+  if (id == 0 || sl.ctx_id != id || !sl.ptr) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
+    sl.ptr = p;
+    sl.ctx_id = current_context_id();   // the lookup made the device's context current
   }
-  *out = g_scratch_ptr[dev];
+  *out = sl.ptr;
   return cudaSuccess;
 }
 
@@ -76,9 +111,20 @@ extern "C" int pw_moe_forward_noalloc(pw_table* t, int layer, const void* x, con
              cudaGetErrorString(e));
     return pw::set_error(PW_ECUDA, msg);
   }
-  // Every word the forward reads from its workspace is written earlier in the
-  // same forward (the status word and work counters are reset by its first
-  // kernel), so the previous call's leftovers need no clearing.
+  // The array keeps the previous call's contents; the forward resets what its
+  // CTAs share before any of them reads it, so nothing needs clearing here.
   return pw_moe_forward(t, layer, x, logits, T, top_k, renorm, residual, out, nullptr, nullptr,
                         nullptr, nullptr, ws, pw::kStaticScratchBytes, compute);
+}
+
+extern "C" int pw_noalloc_status(pw_stream_t s, int* status) {
+  if (!status) return pw::set_error(PW_EINVAL, "pw_noalloc_status: null status");
+  void* ws = nullptr;
+  const cudaError_t e = pw::scratch_address(&ws);
+  if (e != cudaSuccess) {
+    char msg[200];
+    snprintf(msg, sizeof msg, "pw_noalloc_status: scratch lookup failed: %s", cudaGetErrorString(e));
+    return pw::set_error(PW_ECUDA, msg);
+  }
+  return pw_workspace_status(ws, s, status);
 }

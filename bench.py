@@ -2,16 +2,27 @@
 """Throughput of the fused APL MoE layer (decode), one JSON line on rank 0.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload qwen_decode|mixtral_decode_t1|mixtral_decode_t4|tiny]
+                    [--workload mixtral_decode_t4|mixtral_decode_t1|qwen_decode|tiny|
+                                mixtral_prefill|qwen_stack]
+                    [--per-config all|none|name,name]
 
 A step is one pass of the whole hot path (routing, permutation, gate_up
-dequant GEMV + SiLU*up, down dequant GEMV, combine) over one decode batch of
-the Qwen1.5-MoE-A2.7B-shaped layer (hidden 2048, 60 experts, intermediate
-1408, top-4, batch 4, per-block bits in {3..8}, hot experts >= 6).  Inputs are
-seeded synthetic tensors resident in HBM.  Consecutive steps walk through
-``--instances`` distinct layers of that shape (as a model walks its layers),
-so the weights a step reads were last touched several hundred MB earlier and
-are not served from the 129 MB L2.
+dequant GEMV + SiLU*up, down dequant GEMV, combine) over one batch.  The
+default workload is the largest single-GPU decode configuration: the
+Mixtral-8x7B-shaped layer (hidden 4096, 8 experts, intermediate 14336, top-2,
+batch 4, per-block bits in {3, 4, 5, 6, 8}).  Inputs are seeded synthetic
+tensors resident in HBM.  Consecutive steps walk through ``--instances``
+distinct layers of that shape (as a model walks its layers), so the weights a
+step reads were last touched several hundred MB earlier and are not served
+from the 129 MB L2.
+
+Each timed step is one forward bracketed by CUDA events on its stream, so
+steps do not overlap and every launch has its own duration: ``value`` and
+``roofline`` come from the same region.  The back-to-back rate (forwards
+overlapping through programmatic dependent launch) is reported beside it,
+labelled.  ``per_q`` sweeps every block of the layer through uniform
+bitwidths 3..8 (a commit, no reload).  ``per_config`` measures the other
+workloads of the list the same way in the same run, each with its clocks.
 
 Multi-GPU (torchrun): the layer does not shard here, so every rank runs an
 independent replica ("scaling": "weak"); value = all ranks' tokens / the
@@ -38,19 +49,25 @@ FALLBACK_HBM = 6800.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="qwen_decode")
+    ap.add_argument("--workload", default="mixtral_decode_t4")
     ap.add_argument("--instances", type=int, default=0,
                     help="distinct layer instances cycled (default 8 for decode, 1 for prefill)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-q", action="store_true", help="skip the uniform-bitwidth sweep")
+    ap.add_argument("--per-config", default="all",
+                    help="other workloads measured into the same line: all, none, or a comma list")
     ap.add_argument("--uniform-bits", action="store_true",
                     help="every block at the byte-weighted mean bitwidth (mixed vs uniform check)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reload-at", type=int, default=100, help="stack workload: step of the mid-run reload")
     ap.add_argument("--reload-inflight-mb", type=int, default=64,
                     help="stack workload: bound on the mover's copies in flight")
+    ap.add_argument("--stack-reps", type=int, default=3, help="stack workload: reload windows measured")
+    ap.add_argument("--independent-logits", action="store_true",
+                    help="stack workload: precomputed logits (lets consecutive layers overlap)")
     return ap.parse_args()
 
 
@@ -285,6 +302,189 @@ def cpu_cores():
         return os.cpu_count()
 
 
+# ----------------------------------------------------------------------------- measurement
+
+def commit_uniform(m, n_inst, q, stream=None):
+    """Every block of every instance committed at q (all planes are resident)."""
+    items = [(l, e, k, q) for l in range(n_inst) for e in range(m.E) for k in (0, 1)]
+    for i in range(0, len(items), 4096):
+        m.pw_set_commit_many(items[i:i + 4096], stream=stream)
+
+
+def commit_bits(m, bits, stream=None):
+    items = [(l, e, k, int(bits[l][e][k])) for l in bits for e in range(m.E) for k in (0, 1)]
+    for i in range(0, len(items), 4096):
+        m.pw_set_commit_many(items[i:i + 4096], stream=stream)
+
+
+def timed_forwards(m, cfg, X, Lg, ws, out, n, start=0, serial=True):
+    """n forwards cycling the instances.  serial: each forward's kernels are
+    bracketed by CUDA events recorded on the launching stream
+    (pw_profile_attach), so consecutive forwards do not overlap and every
+    launch has its own duration; otherwise the forwards go back to back
+    (programmatic dependent launch lets one forward's routing overlap the
+    previous one's tail).  Returns (region ms, [per-forward event lists])."""
+    import torch
+    import any_precision_weight_gb300 as pw
+    n_inst = len(X)
+    stream = torch.cuda.current_stream()
+    evs = []
+    if serial:
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+        for row in evs:              # torch creates the CUDA event at its first record
+            for e in row:
+                e.record(stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(n):
+        l = (start + i) % n_inst
+        if serial:
+            pw.pw_profile_attach(evs[i])
+        m.pw_moe_forward(l, X[l], Lg[l], cfg.top_k, cfg.renorm, out=out, ws=ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1), evs
+
+
+def kernel_times(cfg, evs):
+    """Average ms per launch of each kernel from the per-forward events."""
+    fused = is_fused(cfg)
+    if fused:
+        return {"layer_fused": sum(r[0].elapsed_time(r[4]) for r in evs) / len(evs)}
+    names = ["route_permute", "gate_up", "down", "combine"]
+    return {nm: sum(r[j].elapsed_time(r[j + 1]) for r in evs) / len(evs) for j, nm in enumerate(names)}
+
+
+def is_fused(cfg):
+    return cfg.T <= 64 and cfg.T * cfg.top_k <= 256     # one persistent kernel per layer
+
+
+def roofline(cfg, kms, byt_avg):
+    """The dominant kernel against its roof: HBM bytes/s for the decode kernel,
+    fp16 tensor FLOP/s for the prefill GEMMs.  Duration = the kernel's own
+    CUDA-event time per launch."""
+    if is_fused(cfg):
+        peak, kind = hbm_peak()
+        ms = kms["layer_fused"]
+        b = byt_avg["layer"]
+        a = b / (ms / 1e3) / 1e9
+        return {"bound": "hbm", "kernel": "k_layer (whole decode layer, one launch)",
+                "duration": "CUDA events around each launch, launches serialised", "ms_per_launch": ms,
+                "achieved": a, "peak": peak, "unit": "GB/s", "frac": a / peak, "peak_kind": peak_kind_note(kind),
+                "traffic": profiled_traffic("layer_fused", cfg.name), "bytes_per_launch": b}
+    dom = max(("gate_up", "down"), key=lambda n: kms[n])
+    P = cfg.T * cfg.top_k
+    fl = {"gate_up": 2.0 * P * 2 * cfg.I * cfg.H, "down": 2.0 * P * cfg.H * cfg.I}[dom]
+    peak, kind = tensor_peak()
+    a = fl / (kms[dom] / 1e3) / 1e12
+    return {"bound": "tensor", "kernel": f"k_prefill<{dom}>", "duration": "CUDA events around each launch",
+            "ms_per_launch": kms[dom], "achieved": a, "peak": peak, "unit": "TFLOP/s", "frac": a / peak,
+            "peak_kind": kind, "traffic": None, "flops_per_launch": fl}
+
+
+def peak_kind_note(kind):
+    return f"{kind} (HBM copy bandwidth, MEASURED_PEAKS.json)" if kind == "measured" else kind
+
+
+def routed_bytes(m, cfg, X, Lg, ws, bits):
+    """Algorithmic bytes of each instance's forward (its routing is fixed by its logits)."""
+    import numpy as np
+    import torch
+    byt = []
+    for l in range(len(X)):
+        _, _, _, off, _ = m.pw_moe_forward(l, X[l], Lg[l], cfg.top_k, cfg.renorm, ws=ws, routing=True)
+        counts = np.diff(off.cpu().numpy())
+        byt.append(algorithmic_bytes(cfg, bits[l], counts))
+    torch.cuda.synchronize()
+    return byt
+
+
+def avg_bytes(byt, n, start=0):
+    keys = byt[0].keys()
+    return {k: sum(byt[(start + i) % len(byt)][k] for i in range(n)) / n for k in keys}
+
+
+def measure_layer(cfg, dev, local, steps, warmup, n_inst, world=1, uniform=None, per_q=False, e2e_steps=0,
+                  overlapped=True):
+    """Builds n_inst seeded layers of cfg and measures them.  Returns a dict:
+    timed region (serialised forwards, per-launch events), roofline of the
+    dominant kernel, the back-to-back step rate, optional host-buffer end to
+    end rate and per-bitwidth sweep."""
+    import torch
+    import synth
+    m, bits = build_model(cfg, n_inst, dev, uniform=uniform)
+    X = [torch.from_numpy(synth.tokens(cfg, step=l)).to(dev) for l in range(n_inst)]
+    Lg = [torch.from_numpy(synth.logits(cfg, l)).to(dev) for l in range(n_inst)]
+    out = torch.empty((cfg.T, cfg.H), dtype=torch.float16, device=dev)
+    ws = m.workspace(cfg.T, cfg.top_k)
+    byt = routed_bytes(m, cfg, X, Lg, ws, bits)
+    timed_forwards(m, cfg, X, Lg, ws, out, warmup, serial=False)
+    res = {"workload": cfg.name, "instances": n_inst}
+
+    clocks = Clocks(local)
+    clocks.start()
+    barrier(world)
+    w0 = time.perf_counter()
+    ms, evs = timed_forwards(m, cfg, X, Lg, ws, out, steps, serial=True)
+    wall = time.perf_counter() - w0
+    barrier(world)
+    res["clocks"] = clocks.stop()
+    res["region_ms"] = ms
+    res["wall_s"] = wall
+    res["ms_per_step"] = ms / steps
+    res["tokens_per_s"] = cfg.T * steps / (ms / 1e3)
+    kms = kernel_times(cfg, evs)
+    res["kernel_ms"] = kms
+    b = avg_bytes(byt, steps)
+    res["layer_bytes_per_step"] = b["layer"]
+    res["roofline"] = roofline(cfg, kms, b)
+    if overlapped and is_fused(cfg):
+        oms, _ = timed_forwards(m, cfg, X, Lg, ws, out, steps, serial=False)
+        res["step_rate_overlapped"] = {
+            "tokens_per_s": cfg.T * steps / (oms / 1e3), "ms_per_step": oms / steps,
+            "note": "the same forwards back to back with no events between them: each forward routes its "
+                    "batch while the previous one finishes (programmatic dependent launch), possible only "
+                    "because the logits are ready in advance; in a model other layers sit between two MoE "
+                    "layers, so this overlap is not counted in value or roofline"}
+    if per_q and is_fused(cfg):
+        sweep = {}
+        for q in (3, 4, 5, 6, 7, 8):
+            commit_uniform(m, n_inst, q)
+            ubits = {l: [[q, q] for _ in range(cfg.E)] for l in range(n_inst)}
+            ub = routed_bytes(m, cfg, X, Lg, ws, ubits)
+            timed_forwards(m, cfg, X, Lg, ws, out, max(3, warmup), serial=False)
+            n = max(50, min(steps, 200))
+            qms, qevs = timed_forwards(m, cfg, X, Lg, ws, out, n, serial=True)
+            kq = kernel_times(cfg, qevs)["layer_fused"]
+            bq = avg_bytes(ub, n)["layer"]
+            gbs = bq / (kq / 1e3) / 1e9
+            sweep[str(q)] = {"ms_per_launch": kq, "bytes_per_launch": bq, "achieved_gbs": gbs,
+                             "frac": gbs / hbm_peak()[0], "tokens_per_s": cfg.T / (kq / 1e3)}
+        commit_bits(m, bits)
+        torch.cuda.synchronize()
+        res["per_q"] = sweep
+    if e2e_steps:
+        xh = [torch.from_numpy(synth.tokens(cfg, step=l)).pin_memory() for l in range(n_inst)]
+        lh = [torch.from_numpy(synth.logits(cfg, l)).pin_memory() for l in range(n_inst)]
+        oh = torch.empty((cfg.T, cfg.H), dtype=torch.float16).pin_memory()
+        for i in range(min(10, e2e_steps)):
+            m.pw_moe_forward_host(i % n_inst, xh[i % n_inst], lh[i % n_inst], cfg.top_k, cfg.renorm, oh, ws=ws)
+        barrier(world)
+        t0 = time.perf_counter()
+        for i in range(e2e_steps):
+            l = i % n_inst
+            m.pw_moe_forward_host(l, xh[l], lh[l], cfg.top_k, cfg.renorm, oh, ws=ws)
+        res["e2e_s"] = max_over_ranks(time.perf_counter() - t0, world)
+    res["bits"] = (f"uniform q={uniform} (byte-weighted mean of the mixed assignment)" if uniform is not None
+                   else "per block from the config's set" + (", hot experts >= 6" if cfg.hot_bits else ""))
+    del m, X, Lg, ws, out
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
 # ----------------------------------------------------------------------------- arms
 
 def run_reference(args, cfg, rank, world):
@@ -308,119 +508,53 @@ def run_reference(args, cfg, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, cfg, rank, world, local):
-    import numpy as np
-    import torch
-    import any_precision_weight_gb300 as pw
+PER_CONFIG = ["tiny", "qwen_decode", "mixtral_decode_t1", "mixtral_decode_t4", "mixtral_prefill", "qwen_stack"]
+
+
+def per_config_entries(args, head, dev, local, world):
+    """Every other config of the workload list, each measured the same way on a
+    short run (its own clocks), for the same JSON line."""
     import synth
+    out = {}
+    names = [n for n in PER_CONFIG if n != head] if args.per_config == "all" else \
+        [n for n in args.per_config.split(",") if n and n != "none" and n != head]
+    for name in names:
+        cfg = synth.CONFIGS[name]
+        t0 = time.perf_counter()
+        try:
+            if cfg.n_layers > 1:
+                r = measure_stack(args, cfg, dev, local, world, steps=max(200, args.reload_at + 100))
+                ent = {"workload": name, "ms_per_step": r["ms_per_step"], "tokens_per_s": r["tokens_per_s"],
+                       "roofline": r["roofline"], "stack": r["stack"], "clocks": r["clocks"]}
+            else:
+                n_inst = 8 if is_fused(cfg) else 1
+                steps = 200 if is_fused(cfg) else 5
+                r = measure_layer(cfg, dev, local, steps, 5, n_inst, world=world)
+                ent = {k: r[k] for k in ("workload", "ms_per_step", "tokens_per_s", "kernel_ms", "roofline",
+                                         "clocks") if k in r}
+                if "step_rate_overlapped" in r:
+                    ent["step_rate_overlapped_tokens_per_s"] = r["step_rate_overlapped"]["tokens_per_s"]
+                if not is_fused(cfg) or cfg.name == "tiny":
+                    ent["l2"] = ("one layer instance; its 1.5 GB of planes exceed L2" if not is_fused(cfg)
+                                 else "8 instances of 2 MB: L2-resident, a latency check")
+        except Exception as ex:      # one config failing does not lose the others
+            ent = {"workload": name, "error": f"{type(ex).__name__}: {ex}"}
+        ent["setup_and_run_s"] = time.perf_counter() - t0
+        out[name] = ent
+    return out
+
+
+def run_ours(args, cfg, rank, world, local):
+    import torch
 
     dev = torch.device("cuda", local)
-    n_inst = args.instances or (8 if cfg.T <= 64 else 1)
+    n_inst = args.instances or (8 if is_fused(cfg) else 1)
     uq = uniform_bits(cfg, n_inst) if args.uniform_bits else None
-    m, bits = build_model(cfg, n_inst, dev, uniform=uq)
-    X = [torch.from_numpy(synth.tokens(cfg, step=l)).to(dev) for l in range(n_inst)]
-    Lg = [torch.from_numpy(synth.logits(cfg, l)).to(dev) for l in range(n_inst)]
-    out = torch.empty((cfg.T, cfg.H), dtype=torch.float16, device=dev)
-    ws = m.workspace(cfg.T, cfg.top_k)
-    stream = torch.cuda.current_stream()
-
-    # routing of each instance (fixed logits): algorithmic bytes per step
-    byt = []
-    for l in range(n_inst):
-        _, _, _, off, _ = m.pw_moe_forward(l, X[l], Lg[l], cfg.top_k, cfg.renorm, ws=ws, routing=True)
-        counts = np.diff(off.cpu().numpy())
-        byt.append(algorithmic_bytes(cfg, bits[l], counts))
-    torch.cuda.synchronize()
-
-    def step(i):
-        l = i % n_inst
-        m.pw_moe_forward(l, X[l], Lg[l], cfg.top_k, cfg.renorm, out=out, ws=ws)
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-
-    clocks = Clocks(local)
-    clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    w0 = time.perf_counter()
-    e0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - w0
-    barrier(world)
-    clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
-    ms_max = max_over_ranks(ms, world)
+    r = measure_layer(cfg, dev, local, args.steps, args.warmup, n_inst, world=world, uniform=uq,
+                      per_q=not args.no_per_q, e2e_steps=min(args.steps, 1000))
+    ms_max = max_over_ranks(r["region_ms"], world)
     value = world * cfg.T * args.steps / (ms_max / 1e3)
-
-    # per-kernel boundary events over a second region of the same steps
-    kn = min(args.steps, 2000)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(kn)]
-    for row in evs:                 # torch creates the CUDA event at its first record
-        for e in row:
-            e.record(stream)
-    torch.cuda.synchronize()
-    for i in range(kn):
-        pw.pw_profile_attach(evs[i])
-        step(i)
-    torch.cuda.synchronize()
-    fused = cfg.T <= 64 and cfg.T * cfg.top_k <= 256     # one persistent kernel per layer
-    if fused:
-        names = ["layer_fused"]
-        tot = {"layer_fused": sum(evs[i][0].elapsed_time(evs[i][4]) for i in range(kn))}
-        dom = "layer_fused"
-    else:
-        names = ["route_permute", "gate_up", "down", "combine"]
-        tot = {n: 0.0 for n in names}
-        for i in range(kn):
-            for j, n in enumerate(names):
-                tot[n] += evs[i][j].elapsed_time(evs[i][j + 1])
-        dom = max(("gate_up", "down"), key=lambda n: tot[n])
-    avg_ms = {n: tot[n] / kn for n in names}
-    key = "layer" if fused else dom
-    dom_bytes = sum(byt[i % n_inst][key] for i in range(kn)) / kn
-    achieved = dom_bytes / (avg_ms[dom] / 1e3) / 1e9
-    duration = "CUDA events around each launch"
-    if fused:
-        # one launch per step and nothing else on the stream: the launch's average
-        # duration in the timed region is the step time (consecutive launches overlap
-        # the next one's routing with this one's tail; events between launches, as in
-        # the per-kernel pass above, would serialise them)
-        dom_bytes = sum(byt[i % n_inst]["layer"] for i in range(args.steps)) / args.steps
-        achieved = dom_bytes / (ms / args.steps / 1e3) / 1e9
-        duration = "timed region / launches (one launch per step)"
-    peak, peak_kind = hbm_peak()
-    bound, unit = "hbm", "GB/s"
-    if not fused:
-        # tensor-core GEMM path: roofline on fp16 FLOP/s of the dominant kernel
-        P = cfg.T * cfg.top_k
-        fl = {"gate_up": 2.0 * P * 2 * cfg.I * cfg.H, "down": 2.0 * P * cfg.H * cfg.I}[dom]
-        achieved = fl / (avg_ms[dom] / 1e3) / 1e12
-        peak, peak_kind = tensor_peak()
-        bound, unit, dom_bytes = "tensor", "TFLOP/s", None
-    layer_bytes = sum(byt[i % n_inst]["layer"] for i in range(args.steps)) / args.steps
-    layer_gbs = layer_bytes / (ms / args.steps / 1e3) / 1e9
-
-    # end to end through the host-buffer entry point (copies inside the region)
-    ne = min(args.steps, 1000)
-    xh = [torch.from_numpy(synth.tokens(cfg, step=l)).pin_memory() for l in range(n_inst)]
-    lh = [torch.from_numpy(synth.logits(cfg, l)).pin_memory() for l in range(n_inst)]
-    oh = torch.empty((cfg.T, cfg.H), dtype=torch.float16).pin_memory()
-    for i in range(min(10, ne)):
-        m.pw_moe_forward_host(i % n_inst, xh[i % n_inst], lh[i % n_inst], cfg.top_k, cfg.renorm, oh, ws=ws)
-    barrier(world)
-    t0 = time.perf_counter()
-    for i in range(ne):
-        l = i % n_inst
-        m.pw_moe_forward_host(l, xh[l], lh[l], cfg.top_k, cfg.renorm, oh, ws=ws)
-    e2e_dt = max_over_ranks(time.perf_counter() - t0, world)
-    e2e = world * cfg.T * ne / e2e_dt
+    e2e = world * cfg.T * min(args.steps, 1000) / r["e2e_s"]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -429,6 +563,7 @@ def run_ours(args, cfg, rank, world, local):
                "value_1_thread": oracle_rate_one_thread(cfg, min(10.0, args.cpu_seconds)),
                "sample": f"{reps} full layer forwards (batch {cfg.T}) of layer instance 0 in {dt:.1f} s, "
                          "fp64 numpy (BLAS matmuls threaded, gathers single-threaded)"}
+    per = per_config_entries(args, cfg.name, dev, local, world) if args.per_config != "none" else None
 
     if rank != 0:
         return
@@ -437,64 +572,78 @@ def run_ours(args, cfg, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I,
-                   "top_k": cfg.top_k, "renorm": cfg.renorm, "bits": (f"uniform q={uq} (byte-weighted mean of the mixed assignment)" if uq is not None
-                            else "per block in {3..8}, hot experts >= 6"),
+                   "top_k": cfg.top_k, "renorm": cfg.renorm, "bits": r["bits"],
                    "accumulate": "f32", "parallelism": f"replicas x{world}",
                    "l2": f"{n_inst} distinct layer instances cycled; inputs larger than L2 between reuses",
-                   "layer_weight_bytes_per_step": layer_bytes, "layer_gbs": layer_gbs,
-                   "kernel_ms": avg_ms},
-        "roofline": {"bound": bound, "kernel": dom, "duration": duration, "achieved": achieved, "peak": peak,
-                     "unit": unit,
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": profiled_traffic(dom, cfg.name),
-                     "bytes_per_launch": dom_bytes},
+                   "timing": "each step one forward bracketed by CUDA events on its stream (no overlap "
+                             "between steps)",
+                   "layer_weight_bytes_per_step": r["layer_bytes_per_step"], "kernel_ms": r["kernel_ms"]},
+        "roofline": r["roofline"],
+        "step_rate_overlapped": r.get("step_rate_overlapped"),
+        "per_q": r.get("per_q"),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4,
                 "d2h_bytes_per_step": cfg.T * cfg.H * 2 + 4},
-        "gpu_launches": (1 if fused else 4) * args.steps,
-        "clocks": clk,
-        "wall_s": wall,
+        "gpu_launches": (1 if is_fused(cfg) else 5) * args.steps,
+        "clocks": r["clocks"],
+        "wall_s": r["wall_s"],
+        "per_config": per,
     }
     print(json.dumps(line), flush=True)
 
 
-def run_stack(args, cfg, rank, world, local):
+def measure_stack(args, cfg, dev, local, world, steps):
     """24-layer Qwen-shaped stack, decode batch 4: bits fitted to 40% of the fp16
-    bytes; at step --reload-at a seeded 25% of the blocks below 8 bits start an
-    asynchronous host->device reload of two more planes on a side stream, and
-    each is committed (stream ordered) at the first step boundary after its copy
-    completed.  Reports tokens/s before, during and after the reload window."""
+    bytes.  Each layer's logits are made by a small kernel that reads the
+    previous layer's output (their values stay the config's seeded logits), so
+    a layer's routing cannot start before the previous layer is done, as in a
+    model.  At step reload_at a seeded 25% of the blocks below 8 bits start an
+    asynchronous host->device reload of two more planes on a side stream
+    (native mover), each committed (stream ordered) at the first step boundary
+    after its copy completed.  The reload is run ``args.stack_reps`` times (the
+    reloaded planes are released again in between); reports tokens/s before,
+    during and after each window and the spread of the loss."""
     import numpy as np
     import torch
     import any_precision_weight_gb300 as pw
     from any_precision_weight_gb300.model import HostStore, load_expert_layer
     import synth
 
-    dev = torch.device("cuda", local)
     L = cfg.n_layers
     bits = synth.stack_bits(cfg)
     plan = synth.reload_plan(cfg, bits)
     target = {(l, e, k): qn for (l, e, k, qo, qn) in plan}
     m = pw.PagedMoE(L, cfg.E, cfg.H, cfg.I, device=dev)
     store = HostStore()
+    t_setup = time.perf_counter()
     for l in range(L):
         src = lambda e, k, l=l: (synth.parent_indices(cfg, l, e, k), synth.parent_lut(cfg, l, e, k))
         load_expert_layer(m, l, src, bits[l], store=store,
                           alloc_planes=lambda e, k, l=l: target.get((l, e, k), int(bits[l, e, k])))
+    t_setup = time.perf_counter() - t_setup
     Lg = [torch.from_numpy(synth.logits(cfg, l)).to(dev) for l in range(L)]
     X0 = [torch.from_numpy(synth.tokens(cfg, step=i)).to(dev) for i in range(8)]
     bufs = [torch.empty((cfg.T, cfg.H), dtype=torch.float16, device=dev) for _ in range(2)]
+    lbuf = torch.empty((cfg.T, cfg.E), dtype=torch.float32, device=dev)
     ws = m.workspace(cfg.T, cfg.top_k)
     stream = torch.cuda.current_stream()
     copy = torch.cuda.Stream(device=dev)
+    dependent = not args.independent_logits
 
     def step(i):
         x = X0[i % len(X0)]
         for l in range(L):
             o = bufs[l & 1]
-            m.pw_moe_forward(l, x, Lg[l], cfg.top_k, cfg.renorm, residual=x, out=o, ws=ws)
+            if dependent:
+                # logits_l = seeded logits + 0 * (the previous layer's output): the values do not
+                # change, but this kernel cannot run before that output exists
+                torch.add(Lg[l], x[:, :cfg.E].float(), alpha=0.0, out=lbuf)
+                lg = lbuf
+            else:
+                lg = Lg[l]
+            m.pw_moe_forward(l, x, lg, cfg.top_k, cfg.renorm, residual=x, out=o, ws=ws)
             x = o
 
-    # routing depends only on each layer's fixed logits: weight bytes per step
     bits_after = bits.copy()
     for (l, e, kind, qo, qn) in plan:
         bits_after[l, e, kind] = qn
@@ -504,88 +653,133 @@ def run_stack(args, cfg, rank, world, local):
         counts = np.diff(off.cpu().numpy())
         step_bytes[0] += algorithmic_bytes(cfg, bits[l], counts)["layer"]
         step_bytes[1] += algorithmic_bytes(cfg, bits_after[l], counts)["layer"]
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    n = args.steps
-    reload_at = min(args.reload_at, n - 1)
-    clocks = Clocks(local)
-    clocks.start()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
-    c0 = torch.cuda.Event(enable_timing=True)
-    c1 = torch.cuda.Event(enable_timing=True)
-    for e_ in ev + [c0, c1]:          # torch creates the CUDA event at its first record
-        e_.record(stream)
-    torch.cuda.synchronize()
     reload_bytes = 0
     for (l, e, kind, qo, qn) in plan:
         R, K = m.rows_cols(kind)
         reload_bytes += (qn - qo) * R * K // 8 + R * 2 * sum(1 << b for b in range(qo + 1, qn + 1))
     items = [(l, e, kind, qn) for (l, e, kind, qo, qn) in plan]
+    n = steps
+    reload_at = min(args.reload_at, n - 1)
     m.pw_mover_start(copy, max_inflight_bytes=args.reload_inflight_mb << 20)
-    committed = 0
-    commit_launches = 0
-    last = reload_at
-    landed = False
-    w0 = time.perf_counter()
-    ev[0].record(stream)
-    for i in range(n):
-        if i >= 2:
-            ev[i - 1].synchronize()      # at most two steps in flight, as a decode loop that
-                                         # needs step i-2's tokens before launching step i
-        if i == reload_at:
-            c0.record(copy)
-            m.pw_mover_submit(items)
-        if i >= reload_at and committed < len(items):
-            c, left = m.pw_commit_arrived()
-            if c:
-                committed += c
-                commit_launches += -(-c // 192)
-                last = i
-            if left == 0:
-                c1.record(stream)        # the boundary at which the last block was committed
-                landed = True
-        step(args.warmup + i)
-        ev[i + 1].record(stream)
+    for i in range(3):
+        step(i)
     torch.cuda.synchronize()
-    wall = time.perf_counter() - w0
+    clocks = Clocks(local)
+    clocks.start()
+    reps = []
+    released = {}
+    for rep in range(args.stack_reps):
+        if rep:
+            # back to the fitted bits, the reloaded planes offloaded again (their pages
+            # re-attached empty), so the next window copies the same bytes
+            m.pw_set_commit_many([(l, e, k, qo) for (l, e, k, qo, qn) in plan])
+            torch.cuda.synchronize()
+            for (l, e, k, qo, qn) in plan:
+                rel = m.pw_block_release(l, e, k, qo)
+                ptrs = (pw._vp * pw.MAX_BITS)(*[rel[p] for p in range(pw.MAX_BITS)])
+                pw._check(pw.lib().pw_block_attach_pages(m._t, l, e, k, ptrs), "pw_block_attach_pages")
+            for i in range(3):
+                step(i)
+            torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        for e_ in ev + [c0, c1]:          # torch creates the CUDA event at its first record
+            e_.record(stream)
+        torch.cuda.synchronize()
+        committed = 0
+        commit_launches = 0
+        last = reload_at
+        landed = False
+        w0 = time.perf_counter()
+        ev[0].record(stream)
+        for i in range(n):
+            if i >= 2:
+                ev[i - 1].synchronize()      # at most two steps in flight, as a decode loop that
+                                             # needs step i-2's tokens before launching step i
+            if i == reload_at:
+                c0.record(copy)
+                m.pw_mover_submit(items)
+            if i >= reload_at and committed < len(items):
+                c, left = m.pw_commit_arrived()
+                if c:
+                    committed += c
+                    commit_launches += -(-c // 192)
+                    last = i
+                if left == 0:
+                    c1.record(stream)        # the boundary at which the last block was committed
+                    landed = True
+            step(3 + i)
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - w0
+        t = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(n)])
+        copy_ms = c0.elapsed_time(c1) if landed else None
+        before, during, after = t[:reload_at], t[reload_at:last + 1], t[last + 1:]
+        tps = lambda a: float(cfg.T / (a.mean() / 1e3)) if len(a) else None
+        reps.append({
+            "tokens_per_s_before": tps(before), "tokens_per_s_during": tps(during),
+            "tokens_per_s_after": tps(after),
+            "loss_pct_during": (1 - tps(during) / tps(before)) * 100 if len(during) and len(before) else None,
+            "last_commit_step": last, "committed": committed, "submit_to_last_commit_ms": copy_ms,
+            "reload_gbs": reload_bytes / (copy_ms / 1e3) / 1e9 if copy_ms else None,
+            "ms_total": float(t.sum()), "before_ms_per_step": float(before.mean()) if len(before) else None,
+            "after_ms_per_step": float(after.mean()) if len(after) else None,
+            "commit_launches": commit_launches, "wall_s": wall})
     clk = clocks.stop()
-    t = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(n)])
-    copy_ms = c0.elapsed_time(c1) if landed else None
-    before = t[:reload_at]
-    during = t[reload_at:last + 1]
-    after = t[last + 1:]
-    tps = lambda a: float(cfg.T / (a.mean() / 1e3)) if len(a) else None
-    ms_total = float(t.sum())
-    ms_max = max_over_ranks(ms_total, world)
+    losses = [r["loss_pct_during"] for r in reps if r["loss_pct_during"] is not None]
+    gbs = [r["reload_gbs"] for r in reps if r["reload_gbs"]]
+    before_ms = float(np.mean([r["before_ms_per_step"] for r in reps]))
+    after_ms = [r["after_ms_per_step"] for r in reps if r["after_ms_per_step"]]
+    res = {
+        "ms_per_step": float(np.mean([r["ms_total"] for r in reps])) / n,
+        "tokens_per_s": cfg.T * n * len(reps) / (sum(r["ms_total"] for r in reps) / 1e3),
+        "clocks": clk, "setup_s": t_setup, "steps": n, "reps": len(reps),
+        "gpu_launches": n * L * (2 if dependent else 1) * len(reps) + sum(r["commit_launches"] for r in reps),
+        "stack": {"logits": "from a kernel reading the previous layer's output" if dependent
+                            else "precomputed (the forwards may overlap)",
+                  "reload_at_step": reload_at, "reloaded_blocks": len(plan), "reload_bytes": reload_bytes,
+                  "mover": f"native mover thread, at most {args.reload_inflight_mb} MiB of copies in flight",
+                  "loss_pct_during_mean": float(np.mean(losses)) if losses else None,
+                  "loss_pct_during_min": float(np.min(losses)) if losses else None,
+                  "loss_pct_during_max": float(np.max(losses)) if losses else None,
+                  "reload_gbs_mean": float(np.mean(gbs)) if gbs else None,
+                  "reload_gbs_min": float(np.min(gbs)) if gbs else None,
+                  "reload_gbs_max": float(np.max(gbs)) if gbs else None,
+                  "runs": reps},
+        "roofline": {"bound": "hbm", "kernel": "k_layer (whole step of 24 layers)",
+                     "duration": "CUDA events around each step",
+                     "achieved": step_bytes[0] / (before_ms / 1e3) / 1e9,
+                     "peak": hbm_peak()[0], "unit": "GB/s", "peak_kind": peak_kind_note(hbm_peak()[1]),
+                     "traffic": None, "bytes_per_step_before": step_bytes[0],
+                     "bytes_per_step_after": step_bytes[1],
+                     "achieved_after": step_bytes[1] / (float(np.mean(after_ms)) / 1e3) / 1e9 if after_ms else None},
+    }
+    res["roofline"]["frac"] = res["roofline"]["achieved"] / res["roofline"]["peak"]
+    m.close()
+    del m, store, ws
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_stack(args, cfg, rank, world, local):
+    import torch
+    dev = torch.device("cuda", local)
+    r = measure_stack(args, cfg, dev, local, world, steps=args.steps)
+    ms_max = max_over_ranks(r["ms_per_step"] * r["steps"], world)
     if rank != 0:
         return
     line = {
-        "metric": METRIC, "value": world * cfg.T * n / (ms_max / 1e3), "unit": "tokens/s", "n_gpus": world,
-        "steps": n, "warmup": args.warmup, "ms_per_step": ms_max / n, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": cfg.name, "layers": L, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I,
+        "metric": METRIC, "value": world * cfg.T * r["steps"] / (ms_max / 1e3), "unit": "tokens/s",
+        "n_gpus": world, "steps": r["steps"], "warmup": args.warmup, "ms_per_step": ms_max / r["steps"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": cfg.name, "layers": cfg.n_layers, "T": cfg.T, "H": cfg.H, "E": cfg.E, "I": cfg.I,
                    "top_k": cfg.top_k, "bits": "greedy fit to 40% of fp16 bytes",
-                   "device_weight_bytes": m.device_bytes(), "host_store_bytes": store.nbytes(),
                    "l2": "24 layers of weights (about 10 GB) between reuses, larger than L2"},
-        "stack": {"tokens_per_s_before": tps(before), "tokens_per_s_during": tps(during),
-                  "tokens_per_s_after": tps(after),
-                  "loss_pct_during": (1 - tps(during) / tps(before)) * 100 if len(during) and len(before) else None,
-                  "reload_at_step": reload_at, "last_commit_step": last, "reloaded_blocks": len(plan),
-                  "reload_bytes": reload_bytes, "committed": committed, "submit_to_last_commit_ms": copy_ms,
-                  "mover": f"native mover thread, at most {args.reload_inflight_mb} MiB of copies in flight",
-                  "reload_gbs": reload_bytes / (copy_ms / 1e3) / 1e9 if copy_ms else None},
-        "roofline": {"bound": "hbm", "kernel": "layer_fused (whole step)",
-                     "achieved": step_bytes[0] / (before.mean() / 1e3) / 1e9 if len(before) else None,
-                     "peak": hbm_peak()[0], "unit": "GB/s", "peak_kind": hbm_peak()[1], "traffic": None,
-                     "bytes_per_step_before": step_bytes[0], "bytes_per_step_after": step_bytes[1],
-                     "achieved_after": step_bytes[1] / (after.mean() / 1e3) / 1e9 if len(after) else None},
-        "gpu_launches": n * L + commit_launches, "clocks": clk, "wall_s": wall,
+        "stack": r["stack"], "roofline": r["roofline"], "gpu_launches": r["gpu_launches"],
+        "clocks": r["clocks"], "setup_s": r["setup_s"],
     }
-    r = line["roofline"]
-    if r["achieved"] is not None:
-        r["frac"] = r["achieved"] / r["peak"]
     print(json.dumps(line), flush=True)
 
 

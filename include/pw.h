@@ -395,6 +395,19 @@ int pw_table_destroy(pw_table* t);
 size_t pw_workspace_bytes(int T, int E, int top_k, int H, int I);
 
 /*
+ * pw_workspace_offset -- where a forward leaves its intermediates inside a
+ * workspace of pw_workspace_bytes(T, E, top_k, H, I) bytes, for inspection
+ * after the forward (the next forward on the workspace overwrites them):
+ *   PW_WS_H  h = silu(gate) * up, fp16 [T*top_k][I], row p = the pair at
+ *            permuted position p (see `perm` of pw_moe_forward);
+ *   PW_WS_Y  y = W_down . h, fp32 [T*top_k][H], same row order.
+ * Returns the byte offset, or (size_t)-1 for a bad section or shape.
+ */
+#define PW_WS_H 0
+#define PW_WS_Y 1
+size_t pw_workspace_offset(int T, int E, int top_k, int H, int I, int section);
+
+/*
  * pw_moe_forward -- one fused MoE expert layer ("Fused Mixed-Precision Kernel"):
  * top-k softmax routing, token->expert permutation (stable counting sort with
  * per-expert offsets), per-block-bitwidth dequantised gate_up GEMV/GEMM with
@@ -423,6 +436,15 @@ size_t pw_workspace_bytes(int T, int E, int top_k, int H, int I);
  * safe producer of the logits or descriptors; a kernel that releases its
  * dependents early must have written the logits before it does.  (The forward
  * itself releases its dependents at once; it writes neither.)
+ * The workspace may hold anything when the call is made (fresh memory, an
+ * earlier forward's leftovers): the forward itself resets what its CTAs share
+ * before any of them uses it.  The decode kernel hands out its work items by
+ * tickets in dependency order, so it finishes correctly even while another
+ * kernel holds some of the SMs.
+ * PW_OK means only that the work was enqueued.  What happens on the device (a
+ * NaN logit, a bounded device-side wait that ran out, an unusable block
+ * descriptor) is reported only through the workspace status word: read it with
+ * pw_workspace_status, or use pw_moe_forward_host, which returns PW_EDEVICE.
  * Errors: PW_EINVAL (shapes, unregistered block, misaligned pointer), PW_ENOMEM
  * (workspace too small), PW_ECUDA.
  */
@@ -453,15 +475,16 @@ int pw_moe_forward_host(pw_table* t, int layer, const void* x_host, const float*
  *   pw_workspace_bytes(T, E, top_k, H, I) exceeds 8 MiB are rejected with
  *   PW_ENOMEM and a message (use pw_moe_forward with your own workspace then).
  *   Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
- *   The first call on a device looks the array's address up on that device
- *   (this may load the library's kernels there); make that first call before
- *   capturing any stream.
- *   All calls share the one array and it keeps the previous call's contents
- *   (every value a call reads is written earlier by the same call): two calls
- *   whose GPU work overlaps in time race on it, so keep them on one stream or
- *   otherwise ordered.
+ *   The first call on a device (and the first after the device's context was
+ *   reset) looks the array's address up on that device (this may load the
+ *   library's kernels there); make that first call before capturing any stream.
+ *   All calls share the one array and it keeps the previous call's contents;
+ *   a call never trusts them (the forward resets what it shares between its
+ *   CTAs itself).  Two calls whose GPU work overlaps in time race on it, so
+ *   keep them on one stream or otherwise ordered.
  *   x, logits, residual, out, T, top_k, renorm, compute: as pw_moe_forward
- *   (no routing outputs).
+ *   (no routing outputs).  Device-side conditions are reported through the
+ *   array's status word: read it with pw_noalloc_status.
  * Errors: as pw_moe_forward, PW_ENOMEM when the batch does not fit, PW_ECUDA
  * when the address lookup fails.
  */
@@ -475,6 +498,16 @@ int pw_moe_forward_noalloc(pw_table* t, int layer, const void* x, const float* l
  * PW_STATUS_* bits set by the last forward that used this workspace.
  */
 int pw_workspace_status(const void* workspace, pw_stream_t s, int* status);
+
+/*
+ * pw_noalloc_status -- pw_workspace_status for the scratch array of
+ * pw_moe_forward_noalloc on the current device: the PW_STATUS_* bits of the
+ * last pw_moe_forward_noalloc whose work is on stream s or ordered before it
+ * (synchronises s).  A noalloc call on another stream that overlaps in time
+ * may already have replaced the word (the same race as the calls themselves).
+ * Allocates nothing.  Errors: PW_EINVAL (null status), PW_ECUDA.
+ */
+int pw_noalloc_status(pw_stream_t s, int* status);
 
 /*
  * pw_profile_attach -- measurement hook: the NEXT pw_moe_forward called on this

@@ -118,18 +118,44 @@ def test_qwen_decode_layer_full():
     assert_close(out, ref["out"])
 
 
+def _check_h(m, cfg, ws, ref):
+    """h left in the workspace (fp16, permuted pair order) against the oracle's
+    fp64 h of every pair, element by element."""
+    h = to_np(m.workspace_h(ws, cfg.T, cfg.top_k)).astype(np.float64)
+    assert h.shape == ref["h"].shape
+    assert_close(h, ref["h"])
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen_decode"])
+def test_intermediate_h_matches_oracle(name):
+    import torch
+    cfg = synth.CONFIGS[name]
+    m = gpu_layer(cfg)
+    x, L = synth.tokens(cfg, step=2), synth.logits(cfg, step=2)
+    ws = m.workspace(cfg.T, cfg.top_k)
+    m.pw_moe_forward(0, torch.from_numpy(x).cuda(), torch.from_numpy(L).cuda(), cfg.top_k, cfg.renorm, ws=ws)
+    torch.cuda.synchronize()
+    ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg)))
+    _check_h(m, cfg, ws, ref)
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["mixtral_decode_t1", "mixtral_decode_t4"])
-def test_mixtral_decode_sampled(name):
+def test_mixtral_decode_full(name):
+    """Full-size Mixtral-shaped decode layer: every output column and every
+    element of h against the fp64 oracle, routing bit-exact."""
+    import torch
     cfg = synth.CONFIGS[name]
     m = gpu_layer(cfg)
     x, L = synth.tokens(cfg), synth.logits(cfg)
-    out, ri, rw, ro, rp = _run(m, cfg, x, L)
-    cols = np.sort(np.random.default_rng(5).choice(cfg.H, size=96, replace=False))
-    ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg)),
-                     out_rows=cols)
-    _check_routing(ref, ri, rw, ro, rp)
-    assert_close(out[:, cols], ref["out"])
+    ws = m.workspace(cfg.T, cfg.top_k)
+    out, ri, rw, ro, rp = m.pw_moe_forward(0, torch.from_numpy(x).cuda(), torch.from_numpy(L).cuda(),
+                                           cfg.top_k, cfg.renorm, ws=ws, routing=True)
+    torch.cuda.synchronize()
+    ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg)))
+    _check_routing(ref, to_np(ri), to_np(rw), to_np(ro), to_np(rp))
+    assert_close(to_np(out), ref["out"])
+    _check_h(m, cfg, ws, ref)
 
 
 def test_prefill_shaped_small():
