@@ -13,31 +13,41 @@
 //  * work items are 64-row tiles of one block (gate_up: 32 gate rows and the
 //    32 matching up rows; down: 64 rows) for one pass of up to four of the
 //    expert's tokens, laid out in a fixed order (largest gate_up cost first,
-//    then all down tiles) and dealt round-robin to the CTAs, so every CTA knows
-//    its next items and loads their descriptors and tables ahead of time;
+//    then all down tiles) and handed out by tickets in that order, so every
+//    CTA knows its next items and loads their descriptors and tables ahead of
+//    time;
 //  * lane l of every warp owns two rows of the tile (gate row l and up row l,
-//    or rows l and 32 + l); the twelve warps split K.  The two rows' q-bit
-//    tables sit in shared memory as one 32-bit slot per (index, lane) holding
-//    both rows' fp16 entries, so a warp's 32 lookups hit 32 different banks
-//    whatever the indices;
-//  * each warp streams its own plane words through a private two-stage
-//    cp.async ring (one coalesced 16-byte copy per lane and plane, the pages
-//    being interleaved across 32-row groups) that runs on into the warp's
-//    share of the next item, so the HBM stream does not stop at item
-//    boundaries;
-//  * per 32-bit plane word, a lane turns q plane words into 32 indices with an
-//    8x8 bit transpose (delta swaps), one byte permute per weight forms the
-//    table address, and the looked-up fp16 weights go straight from registers
-//    into the A operand of a warp-level tensor-core MMA (m16n8k16, fp32
-//    accumulate).  The MMA's 16 k-slots are split between the four lanes of a
-//    row group, and the token operand is zero outside each lane's own column
-//    pair, so every lane accumulates the dot products of its own two rows with
-//    two tokens (a second MMA adds tokens 2 and 3).  The MMA does the
-//    multiply-adds that would otherwise cost two fp32 instructions per weight
-//    and token;
-//  * blocks of at most 3 bits use pair tables: the transposes' upper rows take
-//    the plane words shifted by one element, so one lookup returns two
-//    neighbouring weights already packed for the MMA;
+//    or rows l and 32 + l); the twelve warps split K;
+//  * each warp streams its own plane words through a private cp.async ring of
+//    four 2 KB half-stages (one coalesced 16-byte copy per lane and plane, the
+//    pages being interleaved across 32-row groups; a unit of a q <= 4 block
+//    takes one half-stage, so three can be in flight, a q >= 5 unit two) that
+//    runs on into the warp's share of the next item, so the HBM stream does
+//    not stop at item boundaries;
+//  * the inner loop has two code paths, pair tables (q <= 4) and single
+//    lookups (q >= 5), each for any q of its range (missing planes read as
+//    zero plane slots), so that the hot code stays small;
+//  * q <= 4: pair tables.  The page keeps the even elements of every byte in
+//    its low half and the odd ones in its high half, so a 4x4 bit transpose of
+//    the q plane words nibble by nibble (four delta swaps per four words)
+//    gives one byte per pair of neighbouring elements: the pair index
+//    a | b << 4.  The row's pair table holds LUT[a] | LUT[b] << 16 at that
+//    index, so one shared-memory lookup returns both fp16 weights of an MMA
+//    register (rows rho and rho2 in the two halves of a 256-byte line);
+//  * q >= 5: an 8x8 bit transpose (delta swaps) turns the plane words into one
+//    index byte per element; one lookup per weight in a table whose 32-bit
+//    slot (index, lane) holds both of the lane's rows' fp16 entries, so a
+//    warp's 32 lookups hit 32 different banks whatever the indices, and one
+//    byte permute packs two looked-up weights;
+//  * the table window starts at a 64 KB-aligned shared address, so one byte
+//    permute forms each lookup's full address (index in byte 1, lane offset in
+//    byte 0, the window in bytes 2-3);
+//  * the weights go straight from registers into the A operand of a
+//    warp-level tensor-core MMA (m16n8k16, fp32 accumulate).  The MMA's 16
+//    k-slots are split between the four lanes of a row group, and the token
+//    operand is zero outside each lane's own column pair, so every lane
+//    accumulates the dot products of its own two rows with two tokens (a
+//    second MMA adds tokens 2 and 3);
 //  * the K-warps' partial sums are added in a fixed order (bitwise
 //    deterministic); gate_up items finish with h = silu(gate) * up (fp16),
 //    down items with fp32 y rows; the CTA whose down item completes a 64-row
@@ -54,34 +64,51 @@ namespace {
 constexpr int kThreads = 384;
 constexpr int kWarps = kThreads / 32;
 constexpr int kUnitWords = 2;      // plane words per row per ring stage
-constexpr int kStages = 2;         // ring stages per warp
+constexpr int kHalfStages = 4;     // ring of 2 KB half-stages per warp
 constexpr int kTokPass = 4;        // tokens per pass over a tile (two MMA column sets)
 constexpr int kGateUpTileRows = 32;   // gate rows per gate_up tile (plus as many up rows)
 constexpr int kDownTileRows = 64;
 
-// Shared memory.  Table line v (256 bytes) holds the 32 lanes' slots for index
-// v in its first half; the second halves ("pieces", 128 bytes each) hold the
-// split-K partial sums and the descriptors of the items in flight.  The table
-// starts at a 64 KB-aligned shared address, so that one byte permute forms a
-// lookup's complete address (index in byte 1, lane * 4 in byte 0, the table's
-// 64 KB window in bytes 2-3).  The warps' rings fill the space before it and
-// continue after it, followed by the routing results ("rest").
+// Shared memory: the table window, the warps' rings and one block of the rest
+// ("misc": partial sums, the pair-table source, item descriptors, the layer's
+// descriptors, routing results).  The window is 256 lines of 256 bytes at a
+// 64 KB-aligned shared address; whatever precedes that address holds misc
+// and as many rings as fit, the rest follows the window.
 constexpr int kLine = 256;
 constexpr int kTableBytes = 256 * kLine;
-constexpr int kStageBytes = PW_MAX_BITS * 2 * 32 * 8;   // [plane][row half][lane] x 2 words
-constexpr int kRingWarpBytes = kStages * kStageBytes;
+constexpr int kPlaneSlot = 512;                          // one plane of a unit: [row half][32 rows][2 words]
+constexpr int kHalfStageBytes = 4 * kPlaneSlot;         // four plane slots
+constexpr int kRingWarpBytes = kHalfStages * kHalfStageBytes;
 constexpr int kSlots = 3;          // items in flight: current, next, the one after
-constexpr int kRouteOff = 0;       // offsets within the rest area
+constexpr int kRedOff = 0;                               // [warp][8][32 lanes] fp32 partial sums
+constexpr int kScratchOff = kRedOff + kWarps * 8 * 32 * 4;   // [16 lines][32 lanes] single slots
+constexpr int kDescOff = kScratchOff + 16 * 128;         // [kSlots] BlockDesc of the items in flight
+constexpr int kCacheBlocks = 156;                        // the layer's descriptors when 2E fits
+constexpr int kCacheOff = kDescOff + kSlots * 128;
+constexpr int kRouteOff = kCacheOff + kCacheBlocks * 128;
 constexpr int kCumOff = kRouteOff + route_smem_bytes();
 constexpr int kItemOff = kCumOff + 2 * (kMaxE + 1) * 4;
-constexpr int kRestBytes = kItemOff + 256;
-// whatever the dynamic window's start, everything fits in: at most one ring's
-// worth of bytes before the table is left unused
-constexpr int kSmemBytes = (kWarps + 1) * kRingWarpBytes + kTableBytes + kRestBytes;
-constexpr int kPieceRed = 0;       // warps x 8 (row half, token) x 32 lanes fp32
-constexpr int kPieceDesc = kWarps * 8;   // one BlockDesc per item slot
-constexpr int kPieceCache = kPieceDesc + kSlots;   // descriptors of every block of the layer
-constexpr int kCacheBlocks = 256 - kPieceCache;    // (when 2 E fits)
+constexpr int kMiscBytes = (kItemOff + 256 + 127) / 128 * 128;
+
+// Placement for a window starting toff bytes into the dynamic shared memory.
+struct Place {
+  bool misc_first;   // misc before the window
+  int nb;            // rings before the window
+  int end;           // bytes used
+};
+__host__ __device__ constexpr Place place(int toff) {
+  const bool mf = toff >= kMiscBytes;
+  const int room = toff - (mf ? kMiscBytes : 0);
+  const int nb = room / kRingWarpBytes < kWarps ? room / kRingWarpBytes : kWarps;
+  return Place{mf, nb, toff + kTableBytes + (mf ? 0 : kMiscBytes) + (kWarps - nb) * kRingWarpBytes};
+}
+__host__ __device__ constexpr int smem_need() {
+  int m = 0;
+  for (int t = 0; t < 0x10000; t += 16) m = place(t).end > m ? place(t).end : m;
+  return m;
+}
+constexpr int kSmemBytes = smem_need();
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 
 extern __shared__ __align__(128) unsigned char g_smem[];
 
@@ -94,7 +121,8 @@ __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0
 __device__ __forceinline__ void cp_wait_n(int n) {   // n = groups allowed to stay in flight
   if (n <= 0) cp_wait<0>();
   else if (n == 1) cp_wait<1>();
-  else cp_wait<2>();
+  else if (n == 2) cp_wait<2>();
+  else cp_wait<3>();
 }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -121,8 +149,9 @@ __device__ __forceinline__ void delta_swap(uint32_t& lo, uint32_t& hi, int s, ui
   hi = nhi;
 }
 // 8x8 bit transposes, four byte lanes at once.  Row r of the input holds plane
-// (q-1-r) (zero for r >= q); after the three rounds, byte bb of o[r] is the
-// q-bit index (plane 0 most significant) of element 8*bb + r.
+// (q-1-r) (zero for r >= q); afterwards byte bb of o[r] is the q-bit index
+// (plane 0 most significant) of the element at bit 8*bb + r of the page word:
+// element 8bb + 2r for r < 4, element 8bb + 2(r-4) + 1 for r >= 4.
 __device__ __forceinline__ void planes_to_indices(uint32_t (&o)[8]) {
 #pragma unroll
   for (int r = 0; r < 4; ++r) delta_swap(o[r], o[r + 4], 4, 0x0F0F0F0Fu);
@@ -134,6 +163,16 @@ __device__ __forceinline__ void planes_to_indices(uint32_t (&o)[8]) {
 #pragma unroll
   for (int r = 0; r < 8; r += 2) delta_swap(o[r], o[r + 1], 1, 0x55555555u);
 }
+// 4x4 bit transposes within every nibble.  Row r of the input holds plane
+// (q-1-r) (zero for r >= q, q <= 4); afterwards nibble n of o[j] is the index
+// of the element at bit 4n + j of the page word, so byte bb of o[j] is the
+// pair index idx(8bb + 2j) | idx(8bb + 2j + 1) << 4.
+__device__ __forceinline__ void planes_to_pairs(uint32_t (&o)[4]) {
+  delta_swap(o[0], o[2], 2, 0x33333333u);
+  delta_swap(o[1], o[3], 2, 0x33333333u);
+  delta_swap(o[0], o[1], 1, 0x55555555u);
+  delta_swap(o[2], o[3], 1, 0x55555555u);
+}
 
 // Table slot at shared address a.
 __device__ __forceinline__ uint32_t lut_slot(uint32_t a) {
@@ -141,30 +180,39 @@ __device__ __forceinline__ uint32_t lut_slot(uint32_t a) {
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
 
-// Where the table, the rings and the rest area sit in this CTA's dynamic
-// shared memory (computed once from the window address of g_smem).
+// Where the table, the rings and misc sit in this CTA's dynamic shared memory
+// (computed once from the window address of g_smem).
 struct Smem {
   unsigned char* table;   // 64 KB-aligned shared address
-  unsigned char* rest;
+  unsigned char* misc;
   uint32_t table_hi;      // shared address of the table (bytes 2-3 only)
-  int nb;                 // warps whose rings sit before the table
-  uint32_t toff;
+  uint32_t ring0, ring1;  // shared addresses: rings before / after the window
+  int nb;                 // rings before the window
 };
 __device__ __forceinline__ Smem smem_layout() {
   Smem m;
-  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(g_smem));
-  m.toff = (0x10000u - (base & 0xFFFFu)) & 0xFFFFu;
-  m.nb = min(kWarps, static_cast<int>(m.toff / kRingWarpBytes));
-  m.table = g_smem + m.toff;
-  m.table_hi = base + m.toff;
-  m.rest = m.table + kTableBytes + (kWarps - m.nb) * kRingWarpBytes;
+  const uint32_t base = smem_addr(g_smem);
+  const int toff = static_cast<int>((0x10000u - (base & 0xFFFFu)) & 0xFFFFu);
+  const Place pl = place(toff);
+  m.nb = pl.nb;
+  m.table = g_smem + toff;
+  m.table_hi = base + toff;
+  m.misc = pl.misc_first ? g_smem : g_smem + toff + kTableBytes;
+  m.ring0 = base + (pl.misc_first ? kMiscBytes : 0);
+  m.ring1 = base + toff + kTableBytes + (pl.misc_first ? 0 : kMiscBytes);
   return m;
 }
 __device__ __forceinline__ uint32_t ring_of(const Smem& m, int warp) {
-  const uint32_t off = warp < m.nb ? warp * kRingWarpBytes
-                                   : m.toff + kTableBytes + (warp - m.nb) * kRingWarpBytes;
-  return static_cast<uint32_t>(__cvta_generic_to_shared(g_smem)) + off;
+  return warp < m.nb ? m.ring0 + warp * kRingWarpBytes : m.ring1 + (warp - m.nb) * kRingWarpBytes;
+}
+__device__ __forceinline__ BlockDesc* desc_slot(const Smem& m, int sl) {
+  return reinterpret_cast<BlockDesc*>(m.misc + kDescOff) + sl;
 }
 
 // D += A * B, m16n8k16, fp16 operands, fp32 accumulators.
@@ -182,9 +230,6 @@ __device__ __forceinline__ uint4 ld_nc16(const void* p) {   // read-only for the
   return v;
 }
 
-// 128-byte piece n (second half of table line n).
-__device__ __forceinline__ unsigned char* piece(unsigned char* table, int n) { return table + n * kLine + 128; }
-
 // ------------------------------------------------------------------ work items
 
 struct ItemInfo {
@@ -192,7 +237,7 @@ struct ItemInfo {
   int n;      // tokens of this pass (1..4)
   int off;    // permuted position of the pass's first token
   int need;   // down: gate_up items of the expert that must be done first
-  int pad;
+  int split;  // down: which of the p.ksplit K-ranges
 };
 
 struct Plan {
@@ -202,8 +247,9 @@ struct Plan {
 };
 
 // Item g of the layer's fixed order: gate_up items (experts by cost rank; per
-// expert pass-major, then tile), then down items in the same expert order.
-__device__ ItemInfo item_of(int g, const Plan& pl, const RouteSmem& r) {
+// expert pass-major, then tile), then down items in the same expert order
+// (per expert pass-major, then tile, then K-split).
+__device__ ItemInfo item_of(int g, const Plan& pl, const RouteSmem& r, int ksplit) {
   ItemInfo it{};
   if (g < 0 || g >= pl.total) return it;
   const bool gu = g < pl.total_gu;
@@ -215,7 +261,8 @@ __device__ ItemInfo item_of(int g, const Plan& pl, const RouteSmem& r) {
     if (cum[mid] <= gg) lo = mid;
     else hi = mid - 1;
   }
-  const int tiles = gu ? pl.tiles_gu : pl.tiles_dn;
+  const int S = gu ? 1 : ksplit;
+  const int tiles = (gu ? pl.tiles_gu : pl.tiles_dn) * S;
   const int rem = gg - cum[lo];
   const int e = r.lpt[1 + lo];
   const int pass = rem / tiles;
@@ -223,7 +270,8 @@ __device__ ItemInfo item_of(int g, const Plan& pl, const RouteSmem& r) {
   it.valid = 1;
   it.kind = gu ? PW_KIND_GATE_UP : PW_KIND_DOWN;
   it.expert = e;
-  it.tile = rem % tiles;
+  it.tile = (rem % tiles) / S;
+  it.split = (rem % tiles) % S;
   it.n = min(kTokPass, cnt - pass * kTokPass);
   it.off = r.off[e] + pass * kTokPass;
   it.need = pl.tiles_gu * ((cnt + kTokPass - 1) / kTokPass);
@@ -247,17 +295,21 @@ __device__ __forceinline__ bool desc_ok(const Fwd& p, const BlockDesc& d, int ki
   return d.q >= 1 && d.q <= PW_MAX_BITS && d.K == (gu ? p.H : p.I) && d.R == (gu ? 2 * p.I : p.H);
 }
 
-// This warp's plane-word units (2 words each) of an item: [u0, u1).
-__device__ __forceinline__ void warp_units(const BlockDesc& d, bool ok, int warp, int& u0, int& u1) {
+// This warp's plane-word units (2 words each) of an item: [u0, u1), inside
+// the item's K-range (K-split part `split` of `nsplit`).
+__device__ __forceinline__ void warp_units(const BlockDesc& d, bool ok, int warp, int split, int nsplit, int& u0,
+                                           int& u1) {
   const int U = ok ? (d.K >> 6) : 0;
-  u0 = U * warp / kWarps;
-  u1 = U * (warp + 1) / kWarps;
+  const int s0 = U * split / nsplit, n = U * (split + 1) / nsplit - s0;
+  u0 = s0 + n * warp / kWarps;
+  u1 = s0 + n * (warp + 1) / kWarps;
 }
 
 // ------------------------------------------------------------------ tables
 
 // The next item's two table rows per lane, held in registers while the
 // current item runs: thread (lane, wv) owns 8-entry chunks wv, wv + kWarps, ...
+// (tables of fewer than 8 entries: warp 0 holds them whole in a[0] / b[0]).
 constexpr int kLutChunks = (32 + kWarps - 1) / kWarps;   // 8-entry chunks per thread at q = 8
 struct LutRegs {
   uint4 a[kLutChunks], b[kLutChunks];
@@ -265,12 +317,9 @@ struct LutRegs {
 
 __device__ __forceinline__ void lut_load(LutRegs& f, const BlockDesc& d, int rho, int rho2, int wv) {
   const int q = d.q, V = 1 << q;
-  if (q <= 3) {   // pair tables: every thread holds both rows' whole tables
+  if (V < 8) {
     f.a[0] = f.b[0] = make_uint4(0u, 0u, 0u, 0u);
-    if (V == 8) {
-      f.a[0] = ld_nc16(reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(rho) * V));
-      f.b[0] = ld_nc16(reinterpret_cast<const uint4*>(d.lut + static_cast<size_t>(rho2) * V));
-    } else {   // 2 or 4 entries per row
+    if (wv == 0) {   // 2 or 4 entries per row
       const uint32_t* ra = reinterpret_cast<const uint32_t*>(d.lut + static_cast<size_t>(rho) * V);
       const uint32_t* rb = reinterpret_cast<const uint32_t*>(d.lut + static_cast<size_t>(rho2) * V);
       f.a[0].x = __ldg(ra);
@@ -294,32 +343,22 @@ __device__ __forceinline__ void lut_load(LutRegs& f, const BlockDesc& d, int rho
   }
 }
 
-// q >= 4: slot (v, lane) = (row rho entry v) | (row rho2 entry v) << 16 in line
-// v.  q <= 3 (pair tables, indexed by a | b << 4 for two neighbouring weights'
-// indices a, b < 8): line a | b << 4 holds (rho entry a) | (rho entry b) << 16,
-// line (a | b << 4) + 128 the same for rho2; warp wv fills the lines of a = wv.
-__device__ __forceinline__ void lut_store(unsigned char* table, const LutRegs& f, int q, int lane, int wv) {
+// Single-slot table: slot (v, lane) = (row rho entry v) | (row rho2 entry v) << 16
+// at dst + v * stride + lane * 4.  Used as the table of q >= 5 items (stride: a
+// window line) and as the source of the pair tables of q <= 4 items (stride
+// 128, the scratch lines).
+__device__ __forceinline__ void lut_store_single(unsigned char* dst, int stride, const LutRegs& f, int q,
+                                                 int lane, int wv) {
   const int V = 1 << q;
-  if (q <= 3) {
-    const uint32_t wa[4] = {f.a[0].x, f.a[0].y, f.a[0].z, f.a[0].w};
-    const uint32_t wb[4] = {f.b[0].x, f.b[0].y, f.b[0].z, f.b[0].w};
-    const int a = wv;
-    if (a < V) {
-      // entry a of each row (a warp-uniform index: a funnel of selects)
-      const uint32_t ta = (a & 4) ? ((a & 2) ? wa[3] : wa[2]) : ((a & 2) ? wa[1] : wa[0]);
-      const uint32_t tb = (a & 4) ? ((a & 2) ? wb[3] : wb[2]) : ((a & 2) ? wb[1] : wb[0]);
-      const uint32_t la = (a & 1) ? ta >> 16 : ta & 0xFFFFu;
-      const uint32_t lb = (a & 1) ? tb >> 16 : tb & 0xFFFFu;
+  if (V < 8) {
+    if (wv == 0) {
+      const uint32_t wa[2] = {f.a[0].x, f.a[0].y};
+      const uint32_t wb[2] = {f.b[0].x, f.b[0].y};
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        if (b < V) {
-          const uint32_t ha = (b & 1) ? (wa[b >> 1] & 0xFFFF0000u) : (wa[b >> 1] << 16);
-          const uint32_t hb = (b & 1) ? (wb[b >> 1] & 0xFFFF0000u) : (wb[b >> 1] << 16);
-          unsigned char* line = table + (a | (b << 4)) * kLine + lane * 4;
-          *reinterpret_cast<uint32_t*>(line) = la | ha;
-          *reinterpret_cast<uint32_t*>(line + 128 * kLine) = lb | hb;
-        }
-      }
+      for (int v = 0; v < 4; ++v)
+        if (v < V)
+          *reinterpret_cast<uint32_t*>(dst + v * stride + lane * 4) =
+              prmt(wa[v >> 1], wb[v >> 1], (v & 1) ? 0x7632u : 0x5410u);
     }
     return;
   }
@@ -332,10 +371,53 @@ __device__ __forceinline__ void lut_store(unsigned char* table, const LutRegs& f
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int v = vc * 8 + 2 * e;
-        *reinterpret_cast<uint32_t*>(table + v * kLine + lane * 4) = prmt(aw[e], bw[e], 0x5410u);
-        *reinterpret_cast<uint32_t*>(table + (v + 1) * kLine + lane * 4) = prmt(aw[e], bw[e], 0x7632u);
+        *reinterpret_cast<uint32_t*>(dst + v * stride + lane * 4) = prmt(aw[e], bw[e], 0x5410u);
+        *reinterpret_cast<uint32_t*>(dst + (v + 1) * stride + lane * 4) = prmt(aw[e], bw[e], 0x7632u);
       }
     }
+  }
+}
+
+// Pair tables of a q <= 4 item from its single slots in the scratch lines:
+// line a | b << 4 of the window holds, for lane l, (rho entry a) | (rho entry
+// b) << 16 at byte l * 4 and the same for rho2 at byte 128 + l * 4.  Each
+// thread keeps its lane's 2^q single slots in registers; the work is cut into
+// jobs (b, block of up to 8 a values), job j to warp j mod kWarps.
+template <int Q>
+__device__ __forceinline__ void pair_tables_q(unsigned char* table, const unsigned char* scratch, int lane,
+                                              int wv) {
+  constexpr int V = 1 << Q;
+  constexpr int NB = V > 8 ? 2 : 1;   // blocks of a values
+  constexpr int AB = V / NB;
+  uint32_t sv[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) sv[v] = *reinterpret_cast<const uint32_t*>(scratch + v * 128 + lane * 4);
+  for (int j = wv; j < V * NB; j += kWarps) {
+    const int b = j % V;
+    const uint32_t sb = *reinterpret_cast<const uint32_t*>(scratch + b * 128 + lane * 4);
+    unsigned char* col = table + (b << 4) * kLine + lane * 4;
+    if (j < V) {
+#pragma unroll
+      for (int a = 0; a < AB; ++a) {
+        *reinterpret_cast<uint32_t*>(col + a * kLine) = prmt(sv[a], sb, 0x5410u);
+        *reinterpret_cast<uint32_t*>(col + a * kLine + 128) = prmt(sv[a], sb, 0x7632u);
+      }
+    } else {
+#pragma unroll
+      for (int a = AB; a < V; ++a) {
+        *reinterpret_cast<uint32_t*>(col + a * kLine) = prmt(sv[a], sb, 0x5410u);
+        *reinterpret_cast<uint32_t*>(col + a * kLine + 128) = prmt(sv[a], sb, 0x7632u);
+      }
+    }
+  }
+}
+__device__ __forceinline__ void pair_tables(unsigned char* table, const unsigned char* scratch, int q, int lane,
+                                            int wv) {
+  switch (q) {
+    case 1: pair_tables_q<1>(table, scratch, lane, wv); break;
+    case 2: pair_tables_q<2>(table, scratch, lane, wv); break;
+    case 3: pair_tables_q<3>(table, scratch, lane, wv); break;
+    default: pair_tables_q<4>(table, scratch, lane, wv); break;
   }
 }
 
@@ -350,62 +432,68 @@ __device__ __forceinline__ void ld_x16(uint4& x, const void* ptr, bool pred) {
       : "r"(static_cast<int>(pred)), "l"(ptr));
 }
 
-// One plane word (32 k) of the lane's two rows into the accumulators.
-// o0 / o1: transposed indices of rho / rho2 (byte bb of o[r] = element 8bb + r);
-// X0 / X1: token operand of the word for column sets 0 / 1, refilled with the
-// next word's (x0n / x1n + 16 bytes per bb, when `more`) as each part is used.
-__device__ __forceinline__ void word_mma(const uint32_t (&o0)[8], const uint32_t (&o1)[8], uint32_t laneoff,
-                                         uint4 (&X0)[4], uint4 (&X1)[4], const uint4* x0n, const uint4* x1n,
-                                         bool p0, bool p1, float (&acc)[2][2][4]) {
+// The token operand of one plane word (32 k) for the two column sets, and the
+// address of the next word's (refilled part by part as each part is used).
+struct Tok {
+  uint4 X0[4], X1[4];
+  const uint4* x0;   // token rows of this lane (null: none)
+  const uint4* x1;
+};
+
+// One plane word of a q <= 4 block: o0 / o1 are rho's / rho2's pair indices
+// (planes_to_pairs); lo0 / lo1 the lookup offsets of rho's / rho2's pair tables.
+// MMA hh takes pairs j = 2hh (k-slots 2c, 2c+1) and 2hh + 1 (2c+8, 2c+9), i.e.
+// elements 8bb + 4hh + {0, 1} and {2, 3}: the token operand's natural order.
+__device__ __forceinline__ void word_mma_pairs(const uint32_t (&o0)[4], const uint32_t (&o1)[4], uint32_t lo0,
+                                               uint32_t lo1, Tok& t, int gw, bool more, float (&acc)[2][2][4]) {
+  const bool p0 = more && t.x0 != nullptr, p1 = more && t.x1 != nullptr;
 #pragma unroll
   for (int bb = 0; bb < 4; ++bb) {
     const uint32_t sel = 0x7604u | (static_cast<uint32_t>(bb) << 4);
-    uint32_t s[8], t[8];
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      s[r] = lut_slot(prmt(o0[r], laneoff, sel));
-      t[r] = lut_slot(prmt(o1[r], laneoff, sel));
-    }
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      // k-slots (2c, 2c+1) <- elements 8bb+4hh+{0,1}; (2c+8, 2c+9) <- +{2,3}
       uint32_t a[4];
-      a[0] = prmt(s[4 * hh + 0], s[4 * hh + 1], 0x5410u);   // row rho
-      a[1] = prmt(t[4 * hh + 0], t[4 * hh + 1], 0x7632u);   // row rho2
-      a[2] = prmt(s[4 * hh + 2], s[4 * hh + 3], 0x5410u);
-      a[3] = prmt(t[4 * hh + 2], t[4 * hh + 3], 0x7632u);
-      mma16816(acc[0][hh], a, hh ? X0[bb].z : X0[bb].x, hh ? X0[bb].w : X0[bb].y);
-      mma16816(acc[1][hh], a, hh ? X1[bb].z : X1[bb].x, hh ? X1[bb].w : X1[bb].y);
+      a[0] = lut_slot(prmt(o0[2 * hh], lo0, sel));
+      a[2] = lut_slot(prmt(o0[2 * hh + 1], lo0, sel));
+      a[1] = lut_slot(prmt(o1[2 * hh], lo1, sel));
+      a[3] = lut_slot(prmt(o1[2 * hh + 1], lo1, sel));
+      mma16816(acc[0][hh], a, hh ? t.X0[bb].z : t.X0[bb].x, hh ? t.X0[bb].w : t.X0[bb].y);
+      mma16816(acc[1][hh], a, hh ? t.X1[bb].z : t.X1[bb].x, hh ? t.X1[bb].w : t.X1[bb].y);
     }
-    ld_x16(X0[bb], x0n + bb, p0);
-    ld_x16(X1[bb], x1n + bb, p1);
+    ld_x16(t.X0[bb], t.x0 + (gw + 1) * 4 + bb, p0);
+    ld_x16(t.X1[bb], t.x1 + (gw + 1) * 4 + bb, p1);
   }
 }
 
-// The same for a q <= 3 block with pair tables: byte bb of o[r], r even, is
-// the pair index of elements 8bb + r and 8bb + r + 1 (the transposes' upper
-// rows are the plane words shifted by one element), so one lookup returns both
-// fp16 weights of an A-register and no packing is needed; row rho2's indices
-// carry bit 7 (its table sits 128 lines up).
-__device__ __forceinline__ void word_mma_pair(const uint32_t (&o0)[8], const uint32_t (&o1)[8], uint32_t laneoff,
-                                              uint4 (&X0)[4], uint4 (&X1)[4],
-                                              const uint4* x0n, const uint4* x1n, bool p0, bool p1,
-                                              float (&acc)[2][2][4]) {
+// One plane word of a q >= 5 block: o0 / o1 are rho's / rho2's indices
+// (planes_to_indices: o[r] byte bb is element 8bb + 2r, or 8bb + 2(r-4) + 1
+// for r >= 4).  A lookup returns both rows' entries of one index; rho keeps
+// the low halves, rho2 the high halves, two per MMA register.
+__device__ __forceinline__ void word_mma_single(const uint32_t (&o0)[8], const uint32_t (&o1)[8], uint32_t lo0,
+                                                Tok& t, int gw, bool more, float (&acc)[2][2][4]) {
+  const bool p0 = more && t.x0 != nullptr, p1 = more && t.x1 != nullptr;
 #pragma unroll
   for (int bb = 0; bb < 4; ++bb) {
     const uint32_t sel = 0x7604u | (static_cast<uint32_t>(bb) << 4);
+    uint32_t s[8], u[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      s[r] = lut_slot(prmt(o0[r], lo0, sel));
+      u[r] = lut_slot(prmt(o1[r], lo0, sel));
+    }
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
+      // elements 8bb + 4hh + {0, 1}: rows 2hh and 4 + 2hh; {2, 3}: rows 2hh + 1 and 5 + 2hh
       uint32_t a[4];
-      a[0] = lut_slot(prmt(o0[4 * hh + 0], laneoff, sel));    // row rho, elements 8bb+4hh+{0,1}
-      a[2] = lut_slot(prmt(o0[4 * hh + 2], laneoff, sel));    // row rho, elements +{2,3}
-      a[1] = lut_slot(prmt(o1[4 * hh + 0], laneoff, sel));    // row rho2
-      a[3] = lut_slot(prmt(o1[4 * hh + 2], laneoff, sel));
-      mma16816(acc[0][hh], a, hh ? X0[bb].z : X0[bb].x, hh ? X0[bb].w : X0[bb].y);
-      mma16816(acc[1][hh], a, hh ? X1[bb].z : X1[bb].x, hh ? X1[bb].w : X1[bb].y);
+      a[0] = prmt(s[2 * hh], s[4 + 2 * hh], 0x5410u);
+      a[1] = prmt(u[2 * hh], u[4 + 2 * hh], 0x7632u);
+      a[2] = prmt(s[2 * hh + 1], s[5 + 2 * hh], 0x5410u);
+      a[3] = prmt(u[2 * hh + 1], u[5 + 2 * hh], 0x7632u);
+      mma16816(acc[0][hh], a, hh ? t.X0[bb].z : t.X0[bb].x, hh ? t.X0[bb].w : t.X0[bb].y);
+      mma16816(acc[1][hh], a, hh ? t.X1[bb].z : t.X1[bb].x, hh ? t.X1[bb].w : t.X1[bb].y);
     }
-    ld_x16(X0[bb], x0n + bb, p0);
-    ld_x16(X1[bb], x1n + bb, p1);
+    ld_x16(t.X0[bb], t.x0 + (gw + 1) * 4 + bb, p0);
+    ld_x16(t.X1[bb], t.x1 + (gw + 1) * 4 + bb, p1);
   }
 }
 
@@ -420,15 +508,27 @@ struct Fetch {
   uint32_t desc;     // shared address of the item's descriptor
 };
 
-__device__ __forceinline__ void fetch_enter(Fetch& f, const Fwd& p, const Smem& sm, int item, int warp,
-                                            int lane) {
+// A warp's ring: four 2 KB half-stages.  A unit of a q <= 4 item takes one
+// half-stage (its planes in four plane slots), a unit of a q >= 5 item the two
+// half-stages of one 4 KB half of the ring (eight slots; it starts at an even
+// half-stage, leaving an odd one before it unused).  ih / ch count the half-stages issued /
+// consumed (pads included), iu / cu the units; the unit being consumed starts
+// at ch.
+struct Ring {
+  uint32_t base;
+  int ih, ch, iu, cu;
+};
+__device__ __forceinline__ int unit_halves(int q) { return q <= 4 ? 1 : 2; }
+
+__device__ __forceinline__ void fetch_enter(Fetch& f, const Fwd& p, const Smem& sm, const ItemInfo* s_item,
+                                            int item, int warp, int lane) {
   const int sl = item % kSlots;
-  const ItemInfo& it = reinterpret_cast<const ItemInfo*>(sm.rest + kItemOff)[sl];
-  const BlockDesc& d = *reinterpret_cast<const BlockDesc*>(piece(sm.table, kPieceDesc + sl));
+  const ItemInfo& it = s_item[sl];
+  const BlockDesc& d = *desc_slot(sm, sl);
   f.item = item;
   f.desc = smem_addr(&d);
   const bool ok = it.valid && desc_ok(p, d, it.kind);
-  warp_units(d, ok, warp, f.u, f.end);
+  warp_units(d, ok, warp, it.split, it.kind == PW_KIND_DOWN ? p.ksplit : 1, f.u, f.end);
   const int h = lane >> 4;
   int grp;   // 32-row group of row half h
   if (it.kind == PW_KIND_GATE_UP) grp = h ? p.I / 32 + it.tile : it.tile;
@@ -437,43 +537,98 @@ __device__ __forceinline__ void fetch_enter(Fetch& f, const Fwd& p, const Smem& 
   f.off = static_cast<size_t>(grp) * static_cast<size_t>(d.K >> 6) * 64 + (lane & 15) * 4;
 }
 
-// Issues ring stages until kStages units are in flight or the next unit
-// belongs to an item that is not known yet (an item is known once its
-// descriptor is in shared memory and it exists: items up to `known`).
-// `issued` counts units issued by this warp.  The caller has synchronised the
-// warp after the last read of the stage that the next issue overwrites.
-__device__ __forceinline__ void fetch_fill(Fetch& f, const Fwd& p, const Smem& sm, int known, int consumed,
-                                           int& issued, int warp, int lane, uint32_t ring) {
-  while (issued < consumed + kStages) {
+// Issues units into the ring until it is full or the next unit belongs to an
+// item that is not known yet (an item is known once its descriptor is in
+// shared memory and it exists: items up to `known`).  The planes of a q-bit
+// unit end at its last plane slot: plane p goes to slot s0 + p with s0 = 4 - q
+// (one half-stage) or 8 - q (two), so that bit r of the index (plane q-1-r) is
+// always slot 3 - r or 7 - r; the slots below s0 are zeroed.  The caller has
+// synchronised the warp after the last read of the half-stages the issue may
+// overwrite (everything before the unit being consumed).
+__device__ __forceinline__ void fetch_fill(Fetch& f, const Fwd& p, const Smem& sm, const ItemInfo* s_item,
+                                           int known, Ring& rg, int warp, int lane) {
+  for (;;) {
     while (f.u == f.end) {   // the warp has no more units in this item
       if (f.item + 1 > known) return;
-      fetch_enter(f, p, sm, f.item + 1, warp, lane);
+      fetch_enter(f, p, sm, s_item, f.item + 1, warp, lane);
     }
-    // plane p of a q-plane item goes to stage slot 8 - q + p, so that plane
-    // q-1-r is always slot 7-r; the slots below 8 - q are zeroed
-    const uint32_t dst = ring + (issued % kStages) * kStageBytes + (lane >> 4) * 256 + (lane & 15) * 16;
+    const int sz = unit_halves(f.q);
+    const int pad = (sz == 2 && (rg.ih & 1)) ? 1 : 0;
+    if (rg.ih + pad + sz > rg.ch + kHalfStages) return;   // full
+    rg.ih += pad;
+    const uint32_t dst = rg.base + (rg.ih & (kHalfStages - 1)) * kHalfStageBytes + (lane >> 4) * 256 +
+                         (lane & 15) * 16;
     const size_t w = f.off + static_cast<size_t>(f.u) * 64;
-    const int lo = PW_MAX_BITS - f.q;
+    const int s0 = 4 * sz - f.q;
 #pragma unroll
     for (int sl = 0; sl < PW_MAX_BITS; ++sl) {
-      if (sl >= lo) {
+      if (sl >= s0 && sl < s0 + f.q) {
         uint64_t base;
-        asm volatile("ld.shared.u64 %0, [%1];" : "=l"(base) : "r"(f.desc + (sl - lo) * 8));
+        asm volatile("ld.shared.u64 %0, [%1];" : "=l"(base) : "r"(f.desc + (sl - s0) * 8));
         const uint32_t* src = reinterpret_cast<const uint32_t*>(base) + w;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + sl * 512), "l"(src) : "memory");
-      } else {
-        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst + sl * 512), "r"(0u) : "memory");
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + sl * kPlaneSlot), "l"(src)
+                     : "memory");
+      } else if (sl < s0) {
+        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst + sl * kPlaneSlot), "r"(0u) : "memory");
       }
     }
     cp_commit();
-    ++issued;
+    rg.ih += sz;
+    ++rg.iu;
     ++f.u;
+  }
+}
+
+// The warp's units [u0, u1) of one item: ring stages in, transposes, lookups,
+// MMAs.  Two code paths: pair tables (q <= 4, four plane slots) and single
+// lookups (q >= 5, eight plane slots); missing planes read as zero slots.
+template <bool PAIR>
+__device__ __forceinline__ void run_units(const Fwd& p, const Smem& sm, const ItemInfo* s_item, Fetch& f,
+                                          int known, Ring& rg, int warp, int lane, uint32_t lo0, uint32_t lo1,
+                                          int u0, int u1, Tok& t, float (&acc)[2][2][4]) {
+  constexpr int NR = PAIR ? 4 : 8;   // index bits held (rows of the transposes)
+  constexpr int SZ = PAIR ? 1 : 2;   // half-stages per unit
+  const int w1 = u1 * kUnitWords;
+  for (int u = u0; u < u1; ++u) {
+    cp_wait_n(rg.iu - rg.cu - 1);
+    __syncwarp();   // every lane's copies of this unit visible; the previous unit is read
+    if (SZ == 2 && (rg.ch & 1)) ++rg.ch;   // the issue's pad
+    fetch_fill(f, p, sm, s_item, known, rg, warp, lane);
+    const uint32_t st = rg.base + (rg.ch & (kHalfStages - 1)) * kHalfStageBytes + lane * 8;
+    rg.ch += SZ;
+    ++rg.cu;
+    uint2 pa[NR], pb[NR];   // row r (bit r of the index) = slot NR-1-r, both words of the unit
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      pa[r] = lds64(st + (NR - 1 - r) * kPlaneSlot);
+      pb[r] = lds64(st + (NR - 1 - r) * kPlaneSlot + 256);
+    }
+#pragma unroll
+    for (int wi = 0; wi < kUnitWords; ++wi) {
+      const int gw = u * kUnitWords + wi;
+      const bool more = gw + 1 < w1;
+      uint32_t o0[NR], o1[NR];
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        o0[r] = wi ? pa[r].y : pa[r].x;
+        o1[r] = wi ? pb[r].y : pb[r].x;
+      }
+      if constexpr (PAIR) {
+        planes_to_pairs(o0);
+        planes_to_pairs(o1);
+        word_mma_pairs(o0, o1, lo0, lo1, t, gw, more, acc);
+      } else {
+        planes_to_indices(o0);
+        planes_to_indices(o1);
+        word_mma_single(o0, o1, lo0, t, gw, more, acc);
+      }
+    }
   }
 }
 
 // 16-byte part of a block's descriptor: from the shared cache or global memory.
 __device__ __forceinline__ uint4 desc_part(const Fwd& p, const Smem& sm, bool cached, int e, int kind, int part) {
-  if (cached) return reinterpret_cast<const uint4*>(piece(sm.table, kPieceCache + 2 * e + kind))[part];
+  if (cached) return reinterpret_cast<const uint4*>(sm.misc + kCacheOff + (2 * e + kind) * 128)[part];
   return ld_nc16(reinterpret_cast<const uint4*>(block_desc(p, e, kind)) + part);
 }
 
@@ -503,31 +658,64 @@ __device__ bool wait_ge(const int* ptr, int want) {
   return false;
 }
 
-// The item a ticket-word update returned: its count under this forward's tag,
-// or -1 when the word holds another tag or the set-up sentinel.
+// The first ticket of a claim under this forward's tag: the count the update
+// returned, less the set-up bit (tickets taken while the forward was being set
+// up follow the set-up CTA's tickets 0 and 1); -1 when the word holds another
+// tag.
 __device__ __forceinline__ int ticket_of(const Fwd& p, unsigned long long old) {
   if ((old & ~kCountMask) != p.tag) return -1;
   const unsigned long long c = old & kCountMask;
-  return c == kSetupCount ? -1 : static_cast<int>(c);
+  return (c & kSetupBit) ? static_cast<int>(c & ~kSetupBit) + 2 : static_cast<int>(c);
 }
 
-// First claim of a CTA (one thread), right after the dependency wait: the
-// first CTA to find the ticket word under another tag sets the forward up
-// (returns 1; the caller resets the counters and then publishes the count);
-// every other CTA waits (bounded) for the published tag and takes two tickets
-// (returns 0 with *first = the first ticket, or -1 when the wait gave up).
-__device__ int claim_first(const Fwd& p, int* first) {
-  unsigned long long v = ld_acquire_u64(p.sync);
-  if ((v & ~kCountMask) != p.tag && cas_acq_rel_u64(p.sync, v, p.tag | kSetupCount) == v) return 1;
-  for (int i = 0; i < kSpinLimit; ++i) {
-    v = ld_acquire_u64(p.sync);
-    if ((v & ~kCountMask) == p.tag && (v & kCountMask) != kSetupCount) {
+// First claim of a CTA (one thread), right after the dependency wait; v is the
+// ticket word as read at the kernel's start.  The first CTA to find the word
+// under another tag sets the forward up (returns 1: tickets 0 and 1; the
+// caller resets the counters, then clears the set-up bit); every other CTA
+// takes two tickets at once (returns 0 with *first = its first ticket), or
+// -1 if the word never settles.
+__device__ int claim_first(const Fwd& p, unsigned long long v, int* first) {
+  for (int i = 0; i < 64; ++i) {
+    if ((v & ~kCountMask) == p.tag) {
       *first = ticket_of(p, add_relaxed_u64(p.sync, 2));
       return *first >= 0 ? 0 : -1;
     }
-    __nanosleep(64);
+    const unsigned long long prev = cas_acq_rel_u64(p.sync, v, p.tag | kSetupBit);
+    if (prev == v) return 1;
+    v = prev;
   }
   return -1;
+}
+
+// Bounded wait (one thread) until the set-up CTA has reset the forward's
+// counters and status (the set-up bit is clear): a CTA's first counter update,
+// status bit or down-item wait comes after it.
+__device__ bool wait_published(const Fwd& p) {
+  for (int i = 0; i < kSpinLimit; ++i) {
+    const unsigned long long v = ld_acquire_u64(p.sync);
+    if ((v & ~kCountMask) == p.tag && !(v & kSetupBit)) return true;
+    __nanosleep(64);
+  }
+  return false;
+}
+
+// Combine of one 64-row output tile once all its down items are done (the
+// whole CTA): with K-split down items, y = the parts added in split order
+// (written to y for inspection), then out = residual + sum_j w * y.
+__device__ void combine_tile(const Fwd& p, const RouteSmem& r, int tile, int tid) {
+  const int r0 = tile * kDownTileRows, r1 = min(r0 + kDownTileRows, p.H);
+  if (p.ksplit > 1) {
+    const int P = p.T * p.k, n = r1 - r0;
+    const size_t part = static_cast<size_t>(P) * p.H;
+    for (int q = tid; q < P * n; q += kThreads) {
+      const size_t at = static_cast<size_t>(q / n) * p.H + r0 + q % n;
+      float v = 0.f;
+      for (int sp = 0; sp < p.ksplit; ++sp) v += __ldcg(p.y_part + sp * part + at);
+      p.y[at] = v;
+    }
+    __syncthreads();
+  }
+  combine_rows(p, r.w, r.inv, r0, r1, 0, p.T, tid, kThreads);
 }
 
 // One persistent launch (one CTA per SM, the co-resident grid) for the whole
@@ -545,7 +733,7 @@ __device__ int claim_first(const Fwd& p, int* first) {
 __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const Smem sm = smem_layout();
-  int* rs = reinterpret_cast<int*>(sm.rest + kRouteOff);
+  int* rs = reinterpret_cast<int*>(sm.misc + kRouteOff);
   RouteSmem r;
   r.idx = rs;
   r.w = reinterpret_cast<float*>(rs + kRouteSmemMaxPairs);
@@ -556,9 +744,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   r.act = r.off + (kMaxE + 1);
   r.lpt = r.act + (kMaxE + 1);
   r.qgu = r.lpt + (kMaxE + 1);
-  int* cum_gu = reinterpret_cast<int*>(sm.rest + kCumOff);
+  int* cum_gu = reinterpret_cast<int*>(sm.misc + kCumOff);
   int* cum_dn = cum_gu + (kMaxE + 1);
-  ItemInfo* s_item = reinterpret_cast<ItemInfo*>(sm.rest + kItemOff);
+  ItemInfo* s_item = reinterpret_cast<ItemInfo*>(sm.misc + kItemOff);
+  unsigned char* scratch = sm.misc + kScratchOff;
   int* s_int = reinterpret_cast<int*>(s_item + kSlots);
 
   Plan pl;
@@ -571,13 +760,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   // (programmatic dependent launch): that forward routes its own batch while
   // this one finishes, and waits for it before touching the workspace.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the ticket word as it stands now (a hint for the claim; read again by its CAS)
+  const unsigned long long tw = tid == 0 ? ld_relaxed_u64(p.sync) : 0ull;
   if (tid == 0) s_int[0] = 0;   // NaN logit seen
   // every block descriptor of the layer into shared memory (when they fit),
   // in flight while the batch is routed
   const bool cached = 2 * p.E <= kCacheBlocks;
   if (cached)
     for (int i = tid; i < 2 * p.E * 8; i += kThreads)
-      cp_async16(piece(sm.table, kPieceCache + (i >> 3)) + (i & 7) * 16,
+      cp_async16(sm.misc + kCacheOff + (i >> 3) * 128 + (i & 7) * 16,
                  reinterpret_cast<const uint4*>(p.desc + desc_index(p.layer, i >> 4, (i >> 3) & 1, p.E)) + (i & 7));
   cp_commit();
   __syncthreads();
@@ -596,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
       }
       if (a <= pl.nact) {
         cum_gu[a] = (run + incl - np) * pl.tiles_gu;
-        cum_dn[a] = (run + incl - np) * pl.tiles_dn;
+        cum_dn[a] = (run + incl - np) * pl.tiles_dn * p.ksplit;
       }
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
@@ -612,18 +803,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   // the previous kernel on the stream (possibly the previous forward, using the
   // same workspace) has finished and its writes are visible after this
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (tid == 0) s_int[3] = claim_first(p, &s_int[2]);
+  if (tid == 0) s_int[3] = claim_first(p, tw, &s_int[2]);
   __syncthreads();
   const int role = s_int[3];
+  // published: this thread knows the forward's counters and status are reset
+  // (tid 0 for counter updates and status bits, lane 0 of each warp for the
+  // down-item waits)
+  bool published = role == 1;
   if (role == 1) {
     // this CTA sets the forward up: counters to zero, the status word, then the
-    // ticket word's count (tickets 0 and 1 are this CTA's)
+    // set-up bit cleared (tickets 0 and 1 are this CTA's)
     for (int i = tid; i < p.E + pl.tiles_dn; i += kThreads) expert_done[i] = 0;
     if (tid == 0) p.status[0] = s_int[0] ? PW_STATUS_NAN_LOGIT : 0u;
     __syncthreads();
     if (tid == 0) {
       __threadfence();
-      st_release_u64(p.sync, p.tag | 2ull);
+      add_release_u64(p.sync, 2ull - kSetupBit);
       s_int[2] = 0;
     }
     // the routing outputs the caller asked for, and the routing statistics
@@ -637,35 +832,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
       for (int e = tid; e <= p.E; e += kThreads) p.user_offsets[e] = r.off[e];
     update_route_stats(p, r.perm, r.w, r.off);
   } else if (role < 0) {
-    // the set-up never published (bounded wait): leave every item to the others
-    if (tid == 0) atomicOr(p.status, PW_STATUS_TIMEOUT);
+    // the ticket word never settled (bounded): leave every item to the others
+    if (tid == 0 && wait_published(p)) atomicOr(p.status, PW_STATUS_TIMEOUT);
     return;
   }
   __syncthreads();
   // items of the first two tickets and their descriptors
-  if (tid < 2) s_item[tid] = item_of(s_int[2] + tid, pl, r);
+  if (tid < 2) s_item[tid] = item_of(s_int[2] + tid, pl, r, p.ksplit);
   __syncthreads();
   if (warp == 0 && lane < 16) {
     const int sl = lane >> 3, part = lane & 7;
     if (s_item[sl].valid)
-      reinterpret_cast<uint4*>(piece(sm.table, kPieceDesc + sl))[part] =
+      reinterpret_cast<uint4*>(desc_slot(sm, sl))[part] =
           desc_part(p, sm, cached, s_item[sl].expert, s_item[sl].kind, part);
   }
   __syncthreads();
   const uint32_t ring = ring_of(sm, warp);
-  const uint32_t laneoff = sm.table_hi | (static_cast<uint32_t>(lane) * 4u);
+  const uint32_t lo0 = sm.table_hi | (static_cast<uint32_t>(lane) * 4u);   // rho's lookups
+  const uint32_t lo1 = lo0 + 128u;                                          // rho2's pair table
   Fetch f;
-  int issued = 0, consumed = 0;
+  Ring rg{ring, 0, 0, 0, 0};
   LutRegs lr;
   if (s_item[0].valid) {
-    const BlockDesc& d0 = *reinterpret_cast<const BlockDesc*>(piece(sm.table, kPieceDesc));
+    const BlockDesc& d0 = *desc_slot(sm, 0);
     int rho, rho2;
     lane_rows(p, s_item[0], lane, rho, rho2);
     const bool ok0 = desc_ok(p, d0, s_item[0].kind);
     if (ok0) lut_load(lr, d0, rho, rho2, warp);
-    fetch_enter(f, p, sm, 0, warp, lane);
-    fetch_fill(f, p, sm, s_item[1].valid ? 1 : 0, consumed, issued, warp, lane, ring);
-    if (ok0) lut_store(sm.table, lr, d0.q, lane, warp);
+    fetch_enter(f, p, sm, s_item, 0, warp, lane);
+    fetch_fill(f, p, sm, s_item, s_item[1].valid ? 1 : 0, rg, warp, lane);
+    if (ok0) {
+      if (d0.q >= 5) {
+        lut_store_single(sm.table, kLine, lr, d0.q, lane, warp);
+      } else {
+        lut_store_single(scratch, 128, lr, d0.q, lane, warp);
+        __syncthreads();
+        pair_tables(sm.table, scratch, d0.q, lane, warp);
+      }
+    }
   }
   __syncthreads();   // the first item's tables are complete
 
@@ -675,10 +879,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   for (int i = 0; s_item[i % kSlots].valid; ++i) {
     const int sl = i % kSlots;
     const ItemInfo it = s_item[sl];
-    const BlockDesc& d = *reinterpret_cast<const BlockDesc*>(piece(sm.table, kPieceDesc + sl));
+    const BlockDesc& d = *desc_slot(sm, sl);
     const bool gu = it.kind == PW_KIND_GATE_UP;
     const bool ok = desc_ok(p, d, it.kind);
-    if (!ok && tid == 0) atomicOr(p.status, PW_STATUS_BAD_DESC);
 
     // item i+2's ticket: claimed now, looked at when this item ends
     const int sl1 = (i + 1) % kSlots, sl2 = (i + 2) % kSlots;
@@ -687,7 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     if (tid == 0 && it1.valid) claim = add_relaxed_u64(p.sync, 1);
     const int known = it1.valid ? i + 1 : i;   // the ring may run into item i+1
     // item i+1's tables, into registers until this item's lookups are done
-    const BlockDesc& d1 = *reinterpret_cast<const BlockDesc*>(piece(sm.table, kPieceDesc + sl1));
+    const BlockDesc& d1 = *desc_slot(sm, sl1);
     const bool ok1 = it1.valid && desc_ok(p, d1, it1.kind);
     if (ok1) {
       int rho, rho2;
@@ -696,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     }
 
     int u0, u1;
-    warp_units(d, ok, warp, u0, u1);
+    warp_units(d, ok, warp, it.split, gu ? 1 : p.ksplit, u0, u1);
     float acc[2][2][4];
 #pragma unroll
     for (int j = 0; j < 2; ++j)
@@ -707,94 +910,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     if (u0 < u1) {
       // this lane's token rows (lanes 9c + 4t carry token t of each column set)
       const int tl = (lane >> 2) - 2 * (lane & 3);
-      const uint4* xr[2] = {nullptr, nullptr};
+      Tok t;
+      t.x0 = t.x1 = nullptr;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int tok = 2 * j + tl;
         if (tl >= 0 && tl <= 1 && tok < it.n) {
           const int pos = it.off + tok;
-          xr[j] = reinterpret_cast<const uint4*>(gu ? p.x + static_cast<size_t>(r.perm[pos] / p.k) * p.H
-                                                    : p.hh + static_cast<size_t>(pos) * p.I);
+          const uint4* xr = reinterpret_cast<const uint4*>(gu ? p.x + static_cast<size_t>(r.perm[pos] / p.k) * p.H
+                                                             : p.hh + static_cast<size_t>(pos) * p.I);
+          if (j) t.x1 = xr;
+          else t.x0 = xr;
         }
       }
       if (!gu) {   // h of this expert comes from its gate_up items
-        if (lane == 0 && !wait_ge(&expert_done[it.expert], it.need)) atomicOr(p.status, PW_STATUS_TIMEOUT);
+        if (lane == 0) {
+          if (!published) published = wait_published(p);
+          if (!published || !wait_ge(&expert_done[it.expert], it.need)) atomicOr(p.status, PW_STATUS_TIMEOUT);
+        }
         __syncwarp();
       }
-      uint4 X0[4], X1[4];
-      const int w0 = u0 * kUnitWords, w1 = u1 * kUnitWords;
+      const int w0 = u0 * kUnitWords;
 #pragma unroll
       for (int k4 = 0; k4 < 4; ++k4) {
-        X0[k4] = make_uint4(0u, 0u, 0u, 0u);
-        X1[k4] = make_uint4(0u, 0u, 0u, 0u);
-        ld_x16(X0[k4], xr[0] + w0 * 4 + k4, xr[0] != nullptr);
-        ld_x16(X1[k4], xr[1] + w0 * 4 + k4, xr[1] != nullptr);
+        t.X0[k4] = make_uint4(0u, 0u, 0u, 0u);
+        t.X1[k4] = make_uint4(0u, 0u, 0u, 0u);
+        ld_x16(t.X0[k4], t.x0 + w0 * 4 + k4, t.x0 != nullptr);
+        ld_x16(t.X1[k4], t.x1 + w0 * 4 + k4, t.x1 != nullptr);
       }
-      const bool pairq = d.q <= 3;
-      for (int u = u0; u < u1; ++u) {
-        cp_wait_n(issued - consumed - 1);
-        __syncwarp();   // every lane's copies of this stage visible; the previous stage is read
-        fetch_fill(f, p, sm, known, consumed, issued, warp, lane, ring);
-        const uint32_t st = ring + (consumed % kStages) * kStageBytes + lane * 8;
-        ++consumed;
-        if (pairq) {   // q <= 3: the q plane words sit in slots 7..5
-          uint2 pa[4], pb[4];
-#pragma unroll
-          for (int rr = 0; rr < 4; ++rr) {
-            asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(pa[rr].x), "=r"(pa[rr].y) : "r"(st + (7 - rr) * 512));
-            asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(pb[rr].x), "=r"(pb[rr].y) : "r"(st + (7 - rr) * 512 + 256));
-          }
-#pragma unroll
-          for (int wi = 0; wi < kUnitWords; ++wi) {
-            const int gw = u * kUnitWords + wi;
-            uint32_t o0[8], o1[8];
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-              o0[rr] = wi ? pa[rr].y : pa[rr].x;
-              o1[rr] = wi ? pb[rr].y : pb[rr].x;
-              o0[rr + 4] = o0[rr] >> 1;
-              o1[rr + 4] = o1[rr] >> 1;
-            }
-            planes_to_indices(o0);
-            planes_to_indices(o1);
-#pragma unroll
-            for (int rr = 0; rr < 8; rr += 2) o1[rr] |= 0x80808080u;   // rho2's table: lines + 128
-            const bool more = gw + 1 < w1;
-            word_mma_pair(o0, o1, laneoff, X0, X1, xr[0] + (gw + 1) * 4, xr[1] + (gw + 1) * 4,
-                          more && xr[0] != nullptr, more && xr[1] != nullptr, acc);
-          }
-          continue;
-        }
-        uint2 pv0[8], pv1[8];
-#pragma unroll
-        for (int rr = 0; rr < 8; ++rr) {
-          asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(pv0[rr].x), "=r"(pv0[rr].y) : "r"(st + (7 - rr) * 512));
-          asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(pv1[rr].x), "=r"(pv1[rr].y) : "r"(st + (7 - rr) * 512 + 256));
-        }
-#pragma unroll
-        for (int wi = 0; wi < kUnitWords; ++wi) {
-          const int gw = u * kUnitWords + wi;
-          uint32_t o0[8], o1[8];
-#pragma unroll
-          for (int rr = 0; rr < 8; ++rr) {
-            o0[rr] = wi ? pv0[rr].y : pv0[rr].x;
-            o1[rr] = wi ? pv1[rr].y : pv1[rr].x;
-          }
-          planes_to_indices(o0);
-          planes_to_indices(o1);
-          const bool more = gw + 1 < w1;
-          word_mma(o0, o1, laneoff, X0, X1, xr[0] + (gw + 1) * 4, xr[1] + (gw + 1) * 4,
-                   more && xr[0] != nullptr, more && xr[1] != nullptr, acc);
-        }
-      }
+      if (d.q <= 4) run_units<true>(p, sm, s_item, f, known, rg, warp, lane, lo0, lo1, u0, u1, t, acc);
+      else run_units<false>(p, sm, s_item, f, known, rg, warp, lane, lo0, lo1, u0, u1, t, acc);
     }
     // keep the ring running into the next item while this one finishes
     __syncwarp();
-    fetch_fill(f, p, sm, known, consumed, issued, warp, lane, ring);
+    fetch_fill(f, p, sm, s_item, known, rg, warp, lane);
 
-    // ---- partial sums: piece(warp * 8 + half * 4 + token)[lane]
+    // ---- partial sums: red[warp][half * 4 + token][lane]
+    float* red = reinterpret_cast<float*>(sm.misc + kRedOff);
     {
-      float* red = reinterpret_cast<float*>(piece(sm.table, kPieceRed + warp * 8));
+      float* rw = red + warp * 8 * 32;
       float v[8];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {   // column set j: tokens 2j, 2j+1 of the rows rho / rho2
@@ -804,29 +958,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
         v[4 + 2 * j + 1] = acc[j][0][3] + acc[j][1][3];
       }
 #pragma unroll
-      for (int k8 = 0; k8 < 8; ++k8) red[k8 * (kLine / 4) + lane] = v[k8];
+      for (int k8 = 0; k8 < 8; ++k8) rw[k8 * 32 + lane] = v[k8];
     }
+    // a q <= 4 next item: its single slots into the scratch lines now (the
+    // pair tables are built from them after the barrier)
+    if (ok1 && d1.q <= 4) lut_store_single(scratch, 128, lr, d1.q, lane, warp);
     // a down tile whose last item completed with the previous item: combine it now;
     // item i+2 from the ticket claimed at this item's start
     if (tid == 0) {
       s_int[1] = pending_old == pl.down_per_tile - 1 ? pending_tile : -1;
-      s_item[sl2] = it1.valid ? item_of(ticket_of(p, claim), pl, r) : ItemInfo{};
+      s_item[sl2] = it1.valid ? item_of(ticket_of(p, claim), pl, r, p.ksplit) : ItemInfo{};
     }
     __syncthreads();   // every lookup of this item is done; partials visible
-    if (s_int[1] >= 0) {
-      const int r0 = s_int[1] * kDownTileRows;
-      combine_rows(p, r.w, r.inv, r0, min(r0 + kDownTileRows, p.H), 0, p.T, tid, blockDim.x);
-    }
+    if (s_int[1] >= 0) combine_tile(p, r, s_int[1], tid);
     pending_tile = -1;
     pending_old = -1;
 
-    if (ok1) lut_store(sm.table, lr, d1.q, lane, warp);
+    if (ok1) {
+      if (d1.q >= 5) lut_store_single(sm.table, kLine, lr, d1.q, lane, warp);
+      else pair_tables(sm.table, scratch, d1.q, lane, warp);
+    }
     if (warp == 0 && lane < 8 && s_item[sl2].valid)
-      reinterpret_cast<uint4*>(piece(sm.table, kPieceDesc + sl2))[lane] =
+      reinterpret_cast<uint4*>(desc_slot(sm, sl2))[lane] =
           desc_part(p, sm, cached, s_item[sl2].expert, s_item[sl2].kind, lane);
-    auto red_at = [&](int w, int k8, int l) {
-      return reinterpret_cast<const float*>(piece(sm.table, kPieceRed + w * 8 + k8))[l];
-    };
+    auto red_at = [&](int w, int k8, int l) { return red[(w * 8 + k8) * 32 + l]; };
     if (gu) {
       if (tid < 32 * it.n) {
         const int l = tid & 31, t = tid >> 5;
@@ -845,7 +1000,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
         float yv = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) yv += red_at(w, hf * 4 + t, l);
-        p.y[static_cast<size_t>(it.off + t) * p.H + it.tile * kDownTileRows + hf * 32 + l] = yv;
+        p.y_part[(static_cast<size_t>(it.split) * p.T * p.k + it.off + t) * p.H + it.tile * kDownTileRows + hf * 32 +
+                 l] = yv;
       }
     }
     // Outputs written; next item's tables and descriptor in place.  After the
@@ -856,6 +1012,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     // overlaps the next item), where the CTA that completed the tile combines it.
     __syncthreads();
     if (tid == 0) {
+      if (!published) published = wait_published(p);
+      if (!ok || !published) atomicOr(p.status, published ? PW_STATUS_BAD_DESC : PW_STATUS_TIMEOUT);
       if (gu) {
         red_release_add(&expert_done[it.expert], 1);
       } else {
@@ -866,10 +1024,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   }
   if (tid == 0) s_int[1] = pending_old == pl.down_per_tile - 1 ? pending_tile : -1;
   __syncthreads();
-  if (s_int[1] >= 0) {
-    const int r0 = s_int[1] * kDownTileRows;
-    combine_rows(p, r.w, r.inv, r0, min(r0 + kDownTileRows, p.H), 0, p.T, tid, blockDim.x);
-  }
+  if (s_int[1] >= 0) combine_tile(p, r, s_int[1], tid);
   cp_wait<0>();
 }
 

@@ -35,6 +35,8 @@ struct Fwd {
   __half* hh;               // [T*k][I] h (fp16) in permuted order
   __half* xp;               // [T*k][H] token rows in permuted (expert) order, prefill GEMMs
   float* y;                 // [T*k][H]
+  float* y_part;            // [ksplit][T*k][H] partial y of K-split down items (y when ksplit = 1)
+  int ksplit;               // K-splits of a decode down item
   float* stats;             // [L][E] routing-mass moving average, or null
   float stats_alpha;        // its update weight
 };
@@ -44,15 +46,16 @@ struct Fwd {
 // nothing in it can be trusted until this forward has reset it.  The ticket
 // word (64 bits) carries the forward's tag in bits 24..63 and a count in bits
 // 0..23.  The first CTA to find the word under another tag swaps in the tag
-// with the set-up sentinel as count, resets the forward's counters and status,
-// then publishes the count 0 (plus the tickets it took); every other CTA waits
-// for the published tag before it touches the workspace.  The tag is a fixed
-// byte 0xA5 above a 32-bit forward counter, so no index, count, small integer
-// or float the workspace could hold (and no earlier forward's word) reads as
-// the current tag.
+// with the set-up bit (bit 23) as count and takes tickets 0 and 1; CTAs
+// arriving meanwhile add their claims to the count at once (their tickets
+// follow) but touch no counter or status word until the set-up CTA, having
+// reset the forward's counters and status, clears the set-up bit.  The tag is
+// a fixed byte 0xA5 above a 32-bit forward counter, so no index, count, small
+// integer or float the workspace could hold (and no earlier forward's word)
+// reads as the current tag.
 constexpr unsigned long long kTagShift = 24;
 constexpr unsigned long long kCountMask = (1ull << kTagShift) - 1;
-constexpr unsigned long long kSetupCount = kCountMask;   // "being set up"
+constexpr unsigned long long kSetupBit = 1ull << 23;   // "being set up"
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* ptr) {
   unsigned long long v;
@@ -68,6 +71,14 @@ __device__ __forceinline__ unsigned long long cas_acq_rel_u64(unsigned long long
   asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
                : "=l"(old) : "l"(ptr), "l"(cmp), "l"(val) : "memory");
   return old;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* ptr) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(ptr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void add_release_u64(unsigned long long* ptr, unsigned long long v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(ptr), "l"(v) : "memory");
 }
 __device__ __forceinline__ unsigned long long add_relaxed_u64(unsigned long long* ptr, unsigned long long v) {
   unsigned long long old;

@@ -49,6 +49,7 @@ struct Workspace {
   size_t hh;         // fp16 [T*k][I] in perm order
   size_t xp;         // fp16 [T*k][H] token rows in perm order (prefill GEMMs)
   size_t y;          // f32 [T*k][H] in perm order
+  size_t y_part;     // f32 [down_splits][T*k][H]: partial y of K-split down items (decode path)
   size_t x_in;       // fp16 [T][H]   (host-input staging)
   size_t logits_in;  // f32 [T][E]
   size_t resid_in;   // fp16 [T][H]
@@ -57,6 +58,19 @@ struct Workspace {
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+// The decode path's batches (T <= 64 tokens, T*k <= 256 routed pairs).
+PW_HD inline bool fused_batch(int T, int k) { return T <= 64 && T * k <= 256; }
+
+// K-splits of a decode down item (64 rows x K = I): about I / H parts, so that a
+// down item costs about as much as a gate_up item (64 rows x H), as long as
+// every part keeps at least 24 word pairs (2 per K-warp); 1 when I <= H.
+PW_HD inline int down_splits(int H, int I) {
+  int s = (I + H / 2) / H;
+  const int cap = (I / 64) / 24;
+  if (s > cap) s = cap;
+  return s < 1 ? 1 : s;
+}
 
 inline Workspace workspace_layout(int T, int E, int k, int H, int I) {
   Workspace w{};
@@ -75,6 +89,8 @@ inline Workspace workspace_layout(int T, int E, int k, int H, int I) {
   w.hh = take(P * I * 2);
   w.xp = take(P * H * 2);
   w.y = take(P * H * 4);
+  const int S = fused_batch(T, k) ? down_splits(H, I) : 1;
+  w.y_part = S > 1 ? take(static_cast<size_t>(S) * P * H * 4) : w.y;
   w.x_in = take(static_cast<size_t>(T) * H * 2);
   w.logits_in = take(static_cast<size_t>(T) * E * 4);
   w.resid_in = take(static_cast<size_t>(T) * H * 2);

@@ -104,6 +104,8 @@ static Fwd make_fwd(const ForwardArgs& a) {
   p.hh = reinterpret_cast<__half*>(ws + a.lay.hh);
   p.xp = reinterpret_cast<__half*>(ws + a.lay.xp);
   p.y = reinterpret_cast<float*>(ws + a.lay.y);
+  p.y_part = reinterpret_cast<float*>(ws + a.lay.y_part);
+  p.ksplit = down_splits(a.H, a.I);
   p.stats = a.stats;
   p.stats_alpha = a.stats_alpha;
   return p;
@@ -121,7 +123,7 @@ cudaError_t launch_forward(const ForwardArgs& a, cudaStream_t s) {
   Fwd p = make_fwd(a);
   p.tag = ((0xA5ull << 32) | ++g_forwards) << kTagShift;
   mark(a, 0, s);
-  if (p.T <= kFusedMaxT && p.T * p.k <= kRouteSmemMaxPairs) {
+  if (fused_batch(p.T, p.k)) {
     const cudaError_t e = launch_layer_fused(p, s);
     for (int i = 1; i < 5; ++i) mark(a, i, s);
     return e;

@@ -177,7 +177,8 @@ __device__ __forceinline__ void swap_p(uint32_t& lo, uint32_t& hi, int s, uint32
   lo = nlo;
   hi = nhi;
 }
-// Row r of o holds plane (q-1-r); afterwards byte bb of o[r] is element 8bb + r's index.
+// Row r of o holds plane (q-1-r); afterwards byte bb of o[r] is the index of the
+// element at bit 8bb + r of the page word.
 __device__ __forceinline__ void transpose8(uint32_t (&o)[8]) {
 #pragma unroll
   for (int r = 0; r < 4; ++r) swap_p(o[r], o[r + 4], 4, 0x0F0F0F0Fu);
@@ -256,7 +257,11 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
 
   // dequant role: tile row and which 32-k half of the K step
   const int row = tid & 127, half = (tid >> 7) & 1;
-  const uint32_t rowoff = static_cast<uint32_t>(row) * 2u;     // byte offset of the row in a table line
+  // byte offset of the row's entry in a 256-byte table line: rows r and r + 64
+  // share a 32-bit slot (r % 64), so the 32 rows a warp looks up at once sit in
+  // 32 different banks whatever their indices
+  const uint32_t rowoff = static_cast<uint32_t>(row & 63) * 4u + static_cast<uint32_t>(row >> 6) * 2u;
+  const int lslot = static_cast<int>(rowoff >> 1);             // the same in fp16 entries
   uint32_t g = 0;                                              // K steps so far (stage ring), same in every warp
 
   for (int item = blockIdx.x; item < total; item += gridDim.x) {
@@ -327,12 +332,12 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
     const int grow = wrow<KIND>(p, nt, row);
     // the previous item's dequant steps and epilogue are done by every dequant thread
     named_sync_dq();
-    // the tile's table: LUT_q[row][v] fp16 -> lut_s[v][row]
+    // the tile's table: LUT_q[row][v] fp16 -> lut_s[v][slot of row]
     // (rows of fewer than 8 entries, q < 3, are not 16-byte aligned: 2-byte loads)
     if (V < 8) {
       if (half == 0)
         for (int v = 0; v < V; ++v)
-          reinterpret_cast<uint16_t*>(lut_s)[v * kBN + row] =
+          reinterpret_cast<uint16_t*>(lut_s)[v * kBN + lslot] =
               grow >= 0 ? __ldg(d.lut + static_cast<size_t>(grow) * V + v) : static_cast<uint16_t>(0);
     }
     // four 16-byte loads in flight per thread before their values are stored
@@ -351,7 +356,7 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
         if (vc * 8 >= V) break;
         const uint16_t* hv = reinterpret_cast<const uint16_t*>(&raw[u]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) reinterpret_cast<uint16_t*>(lut_s)[(vc * 8 + j) * kBN + row] = hv[j];
+        for (int j = 0; j < 8; ++j) reinterpret_cast<uint16_t*>(lut_s)[(vc * 8 + j) * kBN + lslot] = hv[j];
       }
     }
     // plane chunks: 16 bytes (4 words = K steps 2j, 2j+1) per row and plane;
@@ -413,11 +418,13 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
             const uint32_t a = prmt_p(o[r], rowoff, 0x5504u | (static_cast<uint32_t>(bb) << 4));
             hv[r] = *reinterpret_cast<const uint16_t*>(lutb + a);
           }
+          // o[r] byte bb holds element 8bb + 2r (r < 4) or 8bb + 2(r-4) + 1 (r >= 4):
+          // the page keeps a byte's even elements in its low half, odd in its high half
           uint4 pk;
-          pk.x = hv[0] | (hv[1] << 16);
-          pk.y = hv[2] | (hv[3] << 16);
-          pk.z = hv[4] | (hv[5] << 16);
-          pk.w = hv[6] | (hv[7] << 16);
+          pk.x = hv[0] | (hv[4] << 16);
+          pk.y = hv[1] | (hv[5] << 16);
+          pk.z = hv[2] | (hv[6] << 16);
+          pk.w = hv[3] | (hv[7] << 16);
           const int chunk = half * 4 + bb;
           *reinterpret_cast<uint4*>(tileB + ((chunk ^ (row & 7)) << 4)) = pk;
         }

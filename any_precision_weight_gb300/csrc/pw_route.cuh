@@ -233,14 +233,26 @@ __device__ __forceinline__ void route_local(const Fwd& p, const RouteSmem& r, in
                                             int tok_cost) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
   const int E = p.E, k = p.k, T = p.T;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {   // issued early: independent loads
-    r.qgu[e] = p.desc[desc_index(p.layer, e, PW_KIND_GATE_UP, E)].q;
-    r.cnt[e] = 0;
+  // each thread's share of the gate_up bitwidths: loads issued first, stored
+  // after the tokens are routed, so their latency overlaps the logits'
+  constexpr int kQPer = (kMaxE + 31) / 32;
+  int qv[kQPer];
+  const int nthr = blockDim.x;
+#pragma unroll
+  for (int j = 0; j < kQPer; ++j) {
+    const int e = threadIdx.x + j * nthr;
+    qv[j] = e < E ? p.desc[desc_index(p.layer, e, PW_KIND_GATE_UP, E)].q : 0;
   }
+  for (int e = threadIdx.x; e < E; e += nthr) r.cnt[e] = 0;
   if (E <= 32) route_tokens<1>(p, r, nan_flag);
   else if (E <= 64) route_tokens<2>(p, r, nan_flag);
   else if (E <= 128) route_tokens<4>(p, r, nan_flag);
   else route_tokens<8>(p, r, nan_flag);
+#pragma unroll
+  for (int j = 0; j < kQPer; ++j) {
+    const int e = threadIdx.x + j * nthr;
+    if (e < E) r.qgu[e] = qv[j];
+  }
   __syncthreads();
   for (int i = threadIdx.x; i < T * k; i += blockDim.x) atomicAdd(&r.cnt[r.idx[i]], 1);
   __syncthreads();

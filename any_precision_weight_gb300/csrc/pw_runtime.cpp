@@ -518,6 +518,18 @@ int pw_pack(const uint8_t* idx, int R, int K, int n_bits, const uint16_t* parent
   return PW_OK;
 }
 
+// Re-places the bits of a plane word for the device page: inside each byte the
+// even elements (bits 0, 2, 4, 6) move to bits 0..3 and the odd ones (1, 3, 5,
+// 7) to bits 4..7, each half in element order.  Two delta swaps: bits 1 <-> 2 of
+// every nibble, then bit pairs 2-3 <-> 4-5 of every byte.
+static inline uint32_t split_even_odd(uint32_t x) {
+  uint32_t t = ((x >> 1) ^ x) & 0x22222222u;
+  x ^= t ^ (t << 1);
+  t = ((x >> 2) ^ x) & 0x0C0C0C0Cu;
+  x ^= t ^ (t << 2);
+  return x;
+}
+
 int pw_tile_planes(const uint32_t* planes, int n_bits, int R, int K, uint32_t* tiled_out) {
   if (!planes || !tiled_out) return fail(PW_EINVAL, "pw_tile_planes: null pointer");
   if (n_bits < 1 || n_bits > PW_MAX_BITS || R < 32 || R % 32 || K < 64 || K % 64)
@@ -527,8 +539,9 @@ int pw_tile_planes(const uint32_t* planes, int n_bits, int R, int K, uint32_t* t
   const uint32_t* hi = planes + plane_words * n_bits;
   if (tiled_out < hi && lo < tiled_out + plane_words * n_bits)
     return fail(PW_EINVAL, "pw_tile_planes: input and output overlap");
-  // word (p, r, w) -> p*R*W + ((r/32)*(W/2) + w/2)*64 + (r%32)*2 + w%2; one
-  // task per (plane, group of 32 rows), spread over CPU threads
+  // word (p, r, w) -> p*R*W + ((r/32)*(W/2) + w/2)*64 + (r%32)*2 + w%2, bits
+  // re-placed by split_even_odd; one task per (plane, group of 32 rows), spread
+  // over CPU threads
   const int groups = R / 32, tasks = n_bits * groups;
   auto work = [&](int t0, int step) {
     for (int t = t0; t < tasks; t += step) {
@@ -539,8 +552,8 @@ int pw_tile_planes(const uint32_t* planes, int n_bits, int R, int K, uint32_t* t
         const uint32_t* row = src + static_cast<size_t>(rr) * W;
         uint32_t* d = dst + rr * 2;
         for (size_t w = 0; w < W; w += 2) {
-          d[w * 32] = row[w];
-          d[w * 32 + 1] = row[w + 1];
+          d[w * 32] = split_even_odd(row[w]);
+          d[w * 32 + 1] = split_even_odd(row[w + 1]);
         }
       }
     }

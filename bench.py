@@ -664,6 +664,35 @@ def measure_stack(args, cfg, dev, local, world, steps):
     for i in range(3):
         step(i)
     torch.cuda.synchronize()
+    # host->device rate of plain copies from the pinned store on the copy stream:
+    # the last chunk (the last layers' planes) twice in a row (its pages first
+    # untouched by the GPU since packing, then just read), then the same copy
+    # while the decode steps run
+    probe = {}
+    chunk = store._chunks[-1]
+    dbuf = torch.empty(chunk.numel(), dtype=torch.uint8, device=dev)
+    for name in ("first", "again"):
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(copy)
+        with torch.cuda.stream(copy):
+            dbuf.copy_(chunk, non_blocking=True)
+        p1.record(copy)
+        p1.synchronize()
+        probe[f"h2d_{name}_gbs"] = chunk.numel() / (p0.elapsed_time(p1) / 1e3) / 1e9
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(copy)
+    with torch.cuda.stream(copy):
+        dbuf.copy_(chunk, non_blocking=True)
+    p1.record(copy)
+    k = 0
+    while not p1.query() and k < 1000:
+        step(k)
+        k += 1
+    p1.synchronize()
+    probe["h2d_beside_decode_gbs"] = chunk.numel() / (p0.elapsed_time(p1) / 1e3) / 1e9
+    probe["probe_bytes"] = chunk.numel()
+    torch.cuda.synchronize()
+    del dbuf
     clocks = Clocks(local)
     clocks.start()
     reps = []
@@ -746,7 +775,7 @@ def measure_stack(args, cfg, dev, local, world, steps):
                   "reload_gbs_mean": float(np.mean(gbs)) if gbs else None,
                   "reload_gbs_min": float(np.min(gbs)) if gbs else None,
                   "reload_gbs_max": float(np.max(gbs)) if gbs else None,
-                  "runs": reps},
+                  "copy_probe": probe, "runs": reps},
         "roofline": {"bound": "hbm", "kernel": "k_layer (whole step of 24 layers)",
                      "duration": "CUDA events around each step",
                      "achieved": step_bytes[0] / (before_ms / 1e3) / 1e9,

@@ -23,7 +23,8 @@
  *   Each plane of a block is one page of R*K/8 bytes, so the planes below the
  *   committed bitwidth form a tail that can live on the CPU and be reloaded.
  *   Inside a device page the words are interleaved across groups of 32 rows
- *   (pw_tile_planes), so that a warp's reads of 32 rows are contiguous.
+ *   and the bits of each word re-placed (pw_tile_planes), so that a warp's
+ *   reads of 32 rows are contiguous.
  *
  * Block shapes: gate_up has R = 2I rows (rows [0, I) gate, [I, 2I) up) and
  * K = H columns; down has R = H rows and K = I columns.  H, I multiples of 128.
@@ -112,7 +113,12 @@ int pw_pack(const uint8_t* idx, int R, int K, int n_bits, const uint16_t* parent
  * rows side by side, [n_bits][R/32][K/64][32][2]; word w of row r of plane p
  * lands at p*R*(K/32) + ((r/32)*(K/64) + w/2)*64 + (r%32)*2 + w%2.  A warp
  * reading two words of 32 consecutive rows then reads 256 contiguous bytes.
- * Each plane is still one contiguous page of R*K/8 bytes.
+ * Inside each word the bits are re-placed: of each byte's 8 elements, the even
+ * ones (k%2 == 0) occupy bits 0..3 and the odd ones bits 4..7, in element
+ * order (element j of the word at bit 8*(j/8) + (j%8)/2 + 4*(j%2)), so that
+ * transposing 4 plane words nibble by nibble yields one byte per pair of
+ * neighbouring elements.  Each plane is still one contiguous page of R*K/8
+ * bytes, and a plane's bits never mix with another plane's.
  *   planes     host [n_bits][R][K/32] uint32 (pw_pack output), read only
  *   tiled_out  host, same size, must not overlap planes
  * Requirements: 1 <= n_bits <= 8, R % 32 == 0, K % 64 == 0.

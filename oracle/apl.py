@@ -62,19 +62,32 @@ def unpack(planes: np.ndarray, b: int, n: int) -> np.ndarray:
     return idx
 
 
+def bit_position(e: int) -> int:
+    """Where element e (0..31) of a plane word sits inside the device page's word:
+    within each byte (8 elements), the even elements take bits 0..3 and the odd
+    ones bits 4..7, in element order: 8*(e//8) + (e%8)//2 + 4*(e%2)."""
+    return 8 * (e // 8) + (e % 8) // 2 + 4 * (e % 2)
+
+
 def tile_planes(planes: np.ndarray) -> np.ndarray:
     """Planes [n][R][W] -> the device page order, flat uint32.
 
     Each plane is cut into groups of 32 rows and pairs of words along K; a
     page lists, for each group (in row order) and each word pair (in K order),
-    the 32 rows' two words side by side: [n][R/32][W/2][32][2].  A pure
-    reordering of the words; R must be a multiple of 32 and W even.
+    the 32 rows' two words side by side: [n][R/32][W/2][32][2].  Inside every
+    word the bits are re-placed by ``bit_position`` (even elements of each
+    byte in its low half, odd elements in its high half).  R must be a
+    multiple of 32 and W even.
     """
     planes = np.asarray(planes, dtype=np.uint32)
     n, R, W = planes.shape
     if R % 32 or W % 2:
         raise ValueError("R must be a multiple of 32 and W even")
-    return planes.reshape(n, R // 32, 32, W // 2, 2).transpose(0, 1, 3, 2, 4).reshape(-1).copy()
+    words = planes.reshape(n, R // 32, 32, W // 2, 2).transpose(0, 1, 3, 2, 4).reshape(-1)
+    out = np.zeros_like(words)
+    for e in range(32):
+        out |= ((words >> np.uint32(e)) & np.uint32(1)) << np.uint32(bit_position(e))
+    return out
 
 
 def child_lut(parent_lut: np.ndarray, b: int, n: int) -> np.ndarray:

@@ -139,6 +139,28 @@ def test_intermediate_h_matches_oracle(name):
     _check_h(m, cfg, ws, ref)
 
 
+def test_split_k_down_items():
+    """An intermediate size much larger than the hidden size (I = 24 H) makes the
+    decode kernel split every down item along K (4 parts, added in a fixed
+    order): out, h and y against the oracle, and bitwise the same on a rerun."""
+    import torch
+    cfg = synth.CONFIGS["tiny"].with_(H=256, I=6144, T=5)
+    m = gpu_layer(cfg)
+    x, L = synth.tokens(cfg, step=8), synth.logits(cfg, step=8)
+    ws = m.workspace(cfg.T, cfg.top_k)
+    xd, Ld = torch.from_numpy(x).cuda(), torch.from_numpy(L).cuda()
+    out = m.pw_moe_forward(0, xd, Ld, cfg.top_k, cfg.renorm, ws=ws).clone()
+    torch.cuda.synchronize()
+    ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg)))
+    assert_close(to_np(out), ref["out"])
+    _check_h(m, cfg, ws, ref)
+    y = to_np(m.workspace_y(ws, cfg.T, cfg.top_k)).astype(np.float64)
+    assert_close(y, ref["y"])
+    again = m.pw_moe_forward(0, xd, Ld, cfg.top_k, cfg.renorm, ws=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(again.view(torch.int16), out.view(torch.int16))
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["mixtral_decode_t1", "mixtral_decode_t4"])
 def test_mixtral_decode_full(name):

@@ -107,10 +107,12 @@ def test_dequant_brute_force():
                 assert W[r, k] == float(lut[r, v])
 
 
-def test_tile_planes_places_every_word_at_its_closed_form_index():
-    """The page order of the planes: word w of row r of plane p sits at
-    p*R*W + ((r/32)*(W/2) + w/2)*64 + (r%32)*2 + w%2, checked word by word
-    against an explicit loop over that formula (tags make each word unique)."""
+def test_tile_planes_places_every_bit_at_its_closed_form_index():
+    """The page order of the planes: element k of row r of plane p (bit k%32 of
+    word w = k//32) sits in page word p*R*W + ((r/32)*(W/2) + w/2)*64 + (r%32)*2
+    + w%2, at bit 8*(j//8) + (j%8)//2 + 4*(j%2) with j = k%32 (even elements of
+    a byte in its low half, odd ones in its high half), checked bit by bit
+    against an explicit loop over that formula."""
     n, R, W = 3, 64, 6
     planes = ((np.arange(n * R * W, dtype=np.uint64) * 2654435761) % (1 << 32)).astype(np.uint32)
     planes = planes.reshape(n, R, W)
@@ -119,12 +121,27 @@ def test_tile_planes_places_every_word_at_its_closed_form_index():
     for p in range(n):
         for r in range(R):
             for w in range(W):
-                want[p * R * W + ((r // 32) * (W // 2) + w // 2) * 64 + (r % 32) * 2 + w % 2] = planes[p, r, w]
+                idx = p * R * W + ((r // 32) * (W // 2) + w // 2) * 64 + (r % 32) * 2 + w % 2
+                for j in range(32):
+                    bit = (int(planes[p, r, w]) >> j) & 1
+                    want[idx] |= np.uint32(bit << (8 * (j // 8) + (j % 8) // 2 + 4 * (j % 2)))
     assert np.array_equal(got, want)
-    assert sorted(got.tolist()) == sorted(planes.reshape(-1).tolist())     # a permutation
+    # the same number of set bits in every word: bits are moved, never made
+    pc = lambda a: np.array([bin(int(v)).count("1") for v in a.reshape(-1)])
+    assert sorted(pc(got).tolist()) == sorted(pc(planes).tolist())
     # a warp reading word pair u of 32 consecutive rows reads 64 contiguous words
     u, g = 1, 1
     block = got[(g * (W // 2) + u) * 64:(g * (W // 2) + u + 1) * 64].reshape(32, 2)
-    assert np.array_equal(block, planes[0, 32 * g:32 * g + 32, 2 * u:2 * u + 2])
-    with pytest.raises(ValueError):
-        apl.tile_planes(np.zeros((1, 48, 4), dtype=np.uint32))
+    src = planes[0, 32 * g:32 * g + 32, 2 * u:2 * u + 2]
+    # element 0 (bit 0) stays at bit 0 and element 1 moves to bit 4
+    assert np.array_equal(block & 1, src & 1)
+    assert np.array_equal((block >> 4) & 1, (src >> 1) & 1)
+
+
+def test_bit_position_is_a_permutation_keeping_even_elements_low():
+    pos = [apl.bit_position(e) for e in range(32)]
+    assert sorted(pos) == list(range(32))
+    for e in range(32):
+        assert pos[e] // 8 == e // 8                   # stays in its byte
+        assert (pos[e] % 8 < 4) == (e % 2 == 0)         # even elements in the low half
+    assert pos[:8] == [0, 4, 1, 5, 2, 6, 3, 7]
