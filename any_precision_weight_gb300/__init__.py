@@ -19,6 +19,7 @@ import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libpw.so")
+CHECK_LIB_PATH = os.path.join(HERE, "libpw_check.so")
 
 PW_OK = 0
 PW_EINVAL = -1
@@ -31,6 +32,7 @@ PW_EDEVICE = -7
 PW_STATUS_NAN_LOGIT = 1
 PW_STATUS_TIMEOUT = 2
 PW_STATUS_BAD_DESC = 4
+PW_STATUS_BOUNDS = 8
 PW_WS_H, PW_WS_Y = 0, 1
 PW_PLANE_HOST, PW_PLANE_HOST_PAGED, PW_PLANE_MOVING, PW_PLANE_DEVICE = 0, 1, 2, 3
 KIND_GATE_UP = 0
@@ -90,13 +92,16 @@ class PWError(RuntimeError):
 
 
 def lib():
-    """Loads libpw.so (once).  Raises if it has not been built."""
+    """Loads libpw.so (once).  Raises if it has not been built.  With the
+    environment variable PW_CHECK=1, loads libpw_check.so instead: the same
+    library with device-side bounds checks that set PW_STATUS_BOUNDS."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+        path = CHECK_LIB_PATH if os.environ.get("PW_CHECK") == "1" else LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first "
                                "(python -m any_precision_weight_gb300.build)")
-        L = ctypes.CDLL(LIB_PATH)
+        L = ctypes.CDLL(path)
         for name, (res, args) in _SIGS.items():
             f = getattr(L, name)
             f.restype = res
@@ -177,10 +182,12 @@ def pw_tile_planes(planes: np.ndarray, out=None):
 
 def pw_profile_attach(events):
     """Next pw_moe_forward on this thread records these 5 torch.cuda.Events at its
-    kernel boundaries (before routing, after routing, gate_up, down, combine)."""
+    kernel boundaries (before routing, after routing, gate_up, down, combine);
+    None entries are not recorded.  The decode path is one kernel: it records
+    events[0] before it and events[1..4] after it."""
     if not events:
         return lib().pw_profile_attach(None, 0)
-    arr = (_vp * len(events))(*[e.cuda_event for e in events])
+    arr = (_vp * len(events))(*[e.cuda_event if e is not None else None for e in events])
     return _check(lib().pw_profile_attach(arr, len(events)), "pw_profile_attach")
 
 
@@ -211,12 +218,19 @@ class PagedMoE:
     (``alloc_planes``) are allocated on the device.
     """
 
-    def __init__(self, n_layers: int, n_experts: int, H: int, I: int, device="cuda", stream=None):
+    def __init__(self, n_layers: int, n_experts: int, H: int, I: int, device="cuda", stream=None,
+                 guard: int = 0):
+        """guard > 0: every device buffer this object allocates (descriptors,
+        plane pages, tables, workspaces) gets canary regions of that many bytes
+        on both sides (``guard.GuardSet``), checked by ``corrupted_guards``."""
         import torch
+        from .guard import GuardSet
         self.L, self.E, self.H, self.I = n_layers, n_experts, H, I
         self.device = torch.device(device)
+        self.guards = GuardSet(guard) if guard > 0 else None
         nb = lib().pw_desc_bytes(n_layers, n_experts)
-        self._desc = torch.zeros(nb + 128, dtype=torch.uint8, device=self.device)
+        self._desc = self._alloc(nb + 128, "descriptors")
+        self._desc.zero_()
         base = self._desc.data_ptr()
         self._desc_ptr = base + ((-base) % 128)
         h = _vp()
@@ -224,6 +238,16 @@ class PagedMoE:
                                      _stream(stream)), "pw_table_create")
         self._t = h
         self._keep = {}
+
+    def _alloc(self, nbytes: int, name: str):
+        import torch
+        if self.guards is None:
+            return torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        return self.guards.alloc(nbytes, self.device, name)
+
+    def corrupted_guards(self) -> list:
+        """Guard regions changed since allocation: [(buffer, side, offset)]."""
+        return [] if self.guards is None else self.guards.corrupted()
 
     def rows_cols(self, kind: int):
         return (2 * self.I, self.H) if kind == KIND_GATE_UP else (self.H, self.I)
@@ -239,13 +263,13 @@ class PagedMoE:
         R, K = self.rows_cols(kind)
         pb = pw_plane_bytes(R, K)
         na = n_bits if alloc_planes is None else max(q_init, min(alloc_planes, n_bits))
-        luts = torch.empty(pw_lut_bytes(R, b_min, n_bits), dtype=torch.uint8, device=self.device)
+        tag = f"{layer}/{expert}/{kind}"
+        luts = self._alloc(pw_lut_bytes(R, b_min, n_bits), f"tables {tag}")
         if per_plane:
-            pages = [torch.empty(pb, dtype=torch.uint8, device=self.device) if p < na else None
-                     for p in range(n_bits)]
+            pages = [self._alloc(pb, f"plane {p} {tag}") if p < na else None for p in range(n_bits)]
             ptrs = (_vp * n_bits)(*[pg.data_ptr() if pg is not None else None for pg in pages])
         else:
-            pages = torch.empty(na * pb, dtype=torch.uint8, device=self.device)
+            pages = self._alloc(na * pb, f"planes {tag}")
             ptrs = (_vp * n_bits)(*[pages.data_ptr() + p * pb if p < na else None for p in range(n_bits)])
         _check(lib().pw_block_register(self._t, layer, expert, kind, n_bits, b_min, _ptr(planes_host),
                                        _ptr(luts_host), ptrs, luts.data_ptr(), q_init, _stream(stream)),
@@ -289,7 +313,7 @@ class PagedMoE:
         new = [None] * MAX_BITS
         for p in range(len(pages)):
             if pages[p] is None:
-                new[p] = torch.empty(pb, dtype=torch.uint8, device=self.device)
+                new[p] = self._alloc(pb, f"plane {p} {layer}/{expert}/{kind} (attached)")
         ptrs = (_vp * MAX_BITS)(*[t.data_ptr() if t is not None else None for t in new])
         _check(lib().pw_block_attach_pages(self._t, layer, expert, kind, ptrs), "pw_block_attach_pages")
         for p in range(len(pages)):
@@ -396,9 +420,8 @@ class PagedMoE:
         return ws[off:off + n].view(torch.float32).view(T * top_k, self.H)
 
     def workspace(self, T: int, top_k: int):
-        import torch
         nb = lib().pw_workspace_bytes(T, self.E, top_k, self.H, self.I)
-        return torch.empty(max(nb, 256), dtype=torch.uint8, device=self.device)
+        return self._alloc(max(nb, 256), f"workspace T={T}")
 
     def pw_moe_forward(self, layer, x, logits, top_k, renorm, residual=None, out=None, ws=None,
                        routing=False, stream=None):

@@ -438,6 +438,7 @@ struct Tok {
   uint4 X0[4], X1[4];
   const uint4* x0;   // token rows of this lane (null: none)
   const uint4* x1;
+  bool two;          // the pass has a third or fourth token (warp-uniform): second MMA column set
 };
 
 // One plane word of a q <= 4 block: o0 / o1 are rho's / rho2's pair indices
@@ -450,18 +451,21 @@ __device__ __forceinline__ void word_mma_pairs(const uint32_t (&o0)[4], const ui
 #pragma unroll
   for (int bb = 0; bb < 4; ++bb) {
     const uint32_t sel = 0x7604u | (static_cast<uint32_t>(bb) << 4);
+    uint32_t a[2][4];   // the byte lane's 8 lookups first, MMA hh = 0's four first
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      uint32_t a[4];
-      a[0] = lut_slot(prmt(o0[2 * hh], lo0, sel));
-      a[2] = lut_slot(prmt(o0[2 * hh + 1], lo0, sel));
-      a[1] = lut_slot(prmt(o1[2 * hh], lo1, sel));
-      a[3] = lut_slot(prmt(o1[2 * hh + 1], lo1, sel));
-      mma16816(acc[0][hh], a, hh ? t.X0[bb].z : t.X0[bb].x, hh ? t.X0[bb].w : t.X0[bb].y);
-      mma16816(acc[1][hh], a, hh ? t.X1[bb].z : t.X1[bb].x, hh ? t.X1[bb].w : t.X1[bb].y);
+      a[hh][0] = lut_slot(prmt(o0[2 * hh], lo0, sel));
+      a[hh][1] = lut_slot(prmt(o1[2 * hh], lo1, sel));
+      a[hh][2] = lut_slot(prmt(o0[2 * hh + 1], lo0, sel));
+      a[hh][3] = lut_slot(prmt(o1[2 * hh + 1], lo1, sel));
+    }
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      mma16816(acc[0][hh], a[hh], hh ? t.X0[bb].z : t.X0[bb].x, hh ? t.X0[bb].w : t.X0[bb].y);
+      if (t.two) mma16816(acc[1][hh], a[hh], hh ? t.X1[bb].z : t.X1[bb].x, hh ? t.X1[bb].w : t.X1[bb].y);
     }
     ld_x16(t.X0[bb], t.x0 + (gw + 1) * 4 + bb, p0);
-    ld_x16(t.X1[bb], t.x1 + (gw + 1) * 4 + bb, p1);
+    if (t.two) ld_x16(t.X1[bb], t.x1 + (gw + 1) * 4 + bb, p1);
   }
 }
 
@@ -475,9 +479,11 @@ __device__ __forceinline__ void word_mma_single(const uint32_t (&o0)[8], const u
 #pragma unroll
   for (int bb = 0; bb < 4; ++bb) {
     const uint32_t sel = 0x7604u | (static_cast<uint32_t>(bb) << 4);
+    // the 16 lookups of the byte lane, those of MMA hh = 0 (rows 0, 4, 1, 5) first
     uint32_t s[8], u[8];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
+    for (int i = 0; i < 8; ++i) {
+      const int r = (i >> 1) + 4 * (i & 1);   // 0, 4, 1, 5, 2, 6, 3, 7
       s[r] = lut_slot(prmt(o0[r], lo0, sel));
       u[r] = lut_slot(prmt(o1[r], lo0, sel));
     }
@@ -490,10 +496,10 @@ __device__ __forceinline__ void word_mma_single(const uint32_t (&o0)[8], const u
       a[2] = prmt(s[2 * hh + 1], s[5 + 2 * hh], 0x5410u);
       a[3] = prmt(u[2 * hh + 1], u[5 + 2 * hh], 0x7632u);
       mma16816(acc[0][hh], a, hh ? t.X0[bb].z : t.X0[bb].x, hh ? t.X0[bb].w : t.X0[bb].y);
-      mma16816(acc[1][hh], a, hh ? t.X1[bb].z : t.X1[bb].x, hh ? t.X1[bb].w : t.X1[bb].y);
+      if (t.two) mma16816(acc[1][hh], a, hh ? t.X1[bb].z : t.X1[bb].x, hh ? t.X1[bb].w : t.X1[bb].y);
     }
     ld_x16(t.X0[bb], t.x0 + (gw + 1) * 4 + bb, p0);
-    ld_x16(t.X1[bb], t.x1 + (gw + 1) * 4 + bb, p1);
+    if (t.two) ld_x16(t.X1[bb], t.x1 + (gw + 1) * 4 + bb, p1);
   }
 }
 
@@ -504,6 +510,10 @@ __device__ __forceinline__ void word_mma_single(const uint32_t (&o0)[8], const u
 // bytes: rows 2(l%16), 2(l%16)+1 of group l/16.
 struct Fetch {
   int item, u, end, q;
+  bool pair;
+#ifdef PW_CHECK
+  size_t words;      // plane words of the block (R * K / 32)
+#endif         // the item's planes use the pair-table layout (four plane slots)
   size_t off;        // page word offset of this lane's 16 bytes at unit 0
   uint32_t desc;     // shared address of the item's descriptor
 };
@@ -518,7 +528,9 @@ struct Ring {
   uint32_t base;
   int ih, ch, iu, cu;
 };
-__device__ __forceinline__ int unit_halves(int q) { return q <= 4 ? 1 : 2; }
+// Pair tables for blocks of at most 4 bits.
+__device__ __forceinline__ bool pair_mode(int q, int /*K*/) { return q <= 4; }
+__device__ __forceinline__ int unit_halves(bool pair) { return pair ? 1 : 2; }
 
 __device__ __forceinline__ void fetch_enter(Fetch& f, const Fwd& p, const Smem& sm, const ItemInfo* s_item,
                                             int item, int warp, int lane) {
@@ -534,6 +546,10 @@ __device__ __forceinline__ void fetch_enter(Fetch& f, const Fwd& p, const Smem& 
   if (it.kind == PW_KIND_GATE_UP) grp = h ? p.I / 32 + it.tile : it.tile;
   else grp = 2 * it.tile + h;
   f.q = d.q;
+  f.pair = pair_mode(d.q, d.K);
+#ifdef PW_CHECK
+  f.words = static_cast<size_t>(d.R) * static_cast<size_t>(d.K) / 32;
+#endif
   f.off = static_cast<size_t>(grp) * static_cast<size_t>(d.K >> 6) * 64 + (lane & 15) * 4;
 }
 
@@ -552,24 +568,30 @@ __device__ __forceinline__ void fetch_fill(Fetch& f, const Fwd& p, const Smem& s
       if (f.item + 1 > known) return;
       fetch_enter(f, p, sm, s_item, f.item + 1, warp, lane);
     }
-    const int sz = unit_halves(f.q);
+    const int sz = unit_halves(f.pair);
     const int pad = (sz == 2 && (rg.ih & 1)) ? 1 : 0;
     if (rg.ih + pad + sz > rg.ch + kHalfStages) return;   // full
     rg.ih += pad;
     const uint32_t dst = rg.base + (rg.ih & (kHalfStages - 1)) * kHalfStageBytes + (lane >> 4) * 256 +
                          (lane & 15) * 16;
     const size_t w = f.off + static_cast<size_t>(f.u) * 64;
-    const int s0 = 4 * sz - f.q;
+    const int s0 = 4 * sz - f.q;   // first plane slot; the slots below it are zeroed
 #pragma unroll
     for (int sl = 0; sl < PW_MAX_BITS; ++sl) {
-      if (sl >= s0 && sl < s0 + f.q) {
+      if (sl < s0) {
+        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst + sl * kPlaneSlot), "r"(0u) : "memory");
+      } else if (sl < s0 + f.q) {
+#ifdef PW_CHECK
+        if (!PW_BOUNDS(p, w + 4 <= f.words, true)) {   // outside the page: zeros instead
+          asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst + sl * kPlaneSlot), "r"(0u) : "memory");
+          continue;
+        }
+#endif
         uint64_t base;
         asm volatile("ld.shared.u64 %0, [%1];" : "=l"(base) : "r"(f.desc + (sl - s0) * 8));
         const uint32_t* src = reinterpret_cast<const uint32_t*>(base) + w;
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + sl * kPlaneSlot), "l"(src)
                      : "memory");
-      } else if (sl < s0) {
-        asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(dst + sl * kPlaneSlot), "r"(0u) : "memory");
       }
     }
     cp_commit();
@@ -862,7 +884,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     fetch_enter(f, p, sm, s_item, 0, warp, lane);
     fetch_fill(f, p, sm, s_item, s_item[1].valid ? 1 : 0, rg, warp, lane);
     if (ok0) {
-      if (d0.q >= 5) {
+      if (!pair_mode(d0.q, d0.K)) {
         lut_store_single(sm.table, kLine, lr, d0.q, lane, warp);
       } else {
         lut_store_single(scratch, 128, lr, d0.q, lane, warp);
@@ -881,7 +903,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     const ItemInfo it = s_item[sl];
     const BlockDesc& d = *desc_slot(sm, sl);
     const bool gu = it.kind == PW_KIND_GATE_UP;
-    const bool ok = desc_ok(p, d, it.kind);
+    const bool ok = desc_ok(p, d, it.kind) &&
+                    PW_BOUNDS(p, it.expert >= 0 && it.expert < p.E && it.off >= 0 && it.off + it.n <= p.T * p.k &&
+                                     it.tile >= 0 && it.tile < (gu ? pl.tiles_gu : pl.tiles_dn) &&
+                                     it.split >= 0 && it.split < (gu ? 1 : p.ksplit),
+                              tid == 0);
 
     // item i+2's ticket: claimed now, looked at when this item ends
     const int sl1 = (i + 1) % kSlots, sl2 = (i + 2) % kSlots;
@@ -912,6 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
       const int tl = (lane >> 2) - 2 * (lane & 3);
       Tok t;
       t.x0 = t.x1 = nullptr;
+      t.two = it.n > 2;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int tok = 2 * j + tl;
@@ -938,7 +965,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
         ld_x16(t.X0[k4], t.x0 + w0 * 4 + k4, t.x0 != nullptr);
         ld_x16(t.X1[k4], t.x1 + w0 * 4 + k4, t.x1 != nullptr);
       }
-      if (d.q <= 4) run_units<true>(p, sm, s_item, f, known, rg, warp, lane, lo0, lo1, u0, u1, t, acc);
+      if (pair_mode(d.q, d.K)) run_units<true>(p, sm, s_item, f, known, rg, warp, lane, lo0, lo1, u0, u1, t, acc);
       else run_units<false>(p, sm, s_item, f, known, rg, warp, lane, lo0, lo1, u0, u1, t, acc);
     }
     // keep the ring running into the next item while this one finishes
@@ -962,7 +989,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     }
     // a q <= 4 next item: its single slots into the scratch lines now (the
     // pair tables are built from them after the barrier)
-    if (ok1 && d1.q <= 4) lut_store_single(scratch, 128, lr, d1.q, lane, warp);
+    if (ok1 && pair_mode(d1.q, d1.K)) lut_store_single(scratch, 128, lr, d1.q, lane, warp);
     // a down tile whose last item completed with the previous item: combine it now;
     // item i+2 from the ticket claimed at this item's start
     if (tid == 0) {
@@ -975,7 +1002,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     pending_old = -1;
 
     if (ok1) {
-      if (d1.q >= 5) lut_store_single(sm.table, kLine, lr, d1.q, lane, warp);
+      if (!pair_mode(d1.q, d1.K)) lut_store_single(sm.table, kLine, lr, d1.q, lane, warp);
       else pair_tables(sm.table, scratch, d1.q, lane, warp);
     }
     if (warp == 0 && lane < 8 && s_item[sl2].valid)

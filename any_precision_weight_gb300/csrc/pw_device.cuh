@@ -86,6 +86,19 @@ __device__ __forceinline__ unsigned long long add_relaxed_u64(unsigned long long
   return old;
 }
 
+// Device-side bounds checks of the PW_CHECK build (libpw_check.so): a failed
+// check sets PW_STATUS_BOUNDS and the caller skips the access; the kernels
+// never trap.  In the normal build the checks compile away.
+#ifdef PW_CHECK
+__device__ __forceinline__ bool pw_in_bounds(const Fwd& p, bool ok, bool report) {
+  if (!ok && report) atomicOr(p.status, PW_STATUS_BOUNDS);
+  return ok;
+}
+#define PW_BOUNDS(p, cond, report) ::pw::pw_in_bounds((p), (cond), (report))
+#else
+#define PW_BOUNDS(p, cond, report) true
+#endif
+
 __device__ __forceinline__ const BlockDesc* block_desc(const Fwd& p, int e, int kind) {
   return p.desc + desc_index(p.layer, e, kind, p.E);
 }

@@ -275,6 +275,7 @@ k_prefill(const Fwd p, const __grid_constant__ CUtensorMap tmA) {
     const int nm = (nvalid + kBM - 1) / kBM;                   // token tiles in this group
     const BlockDesc d = *block_desc(p, e, KIND);
     const int Q = d.q, V = 1 << Q;
+    if (!PW_BOUNDS(p, e < E && row0 >= 0 && row0 + nvalid <= p.T * p.k && nt < ntiles, tid == 0)) continue;
     if (Q < 1 || Q > PW_MAX_BITS || d.K != K) {
       if (tid == 0) atomicOr(p.status, PW_STATUS_BAD_DESC);
       continue;

@@ -363,6 +363,7 @@ __device__ __forceinline__ void combine_rows(const Fwd& p, const float* w, const
     float mix = 0.f;
     for (int j = 0; j < p.k; ++j) {
       const int pos = inv[t * p.k + j];
+      if (!PW_BOUNDS(p, pos >= 0 && pos < p.T * p.k, true)) continue;
       mix = fmaf(w[t * p.k + j], __ldcg(p.y + static_cast<size_t>(pos) * p.H + r), mix);   // L2: written by other SMs
     }
     p.out[static_cast<size_t>(t) * p.H + r] = __float2half_rn(base + mix);

@@ -23,6 +23,8 @@
 #include <thread>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "pw_internal.h"
 
 namespace {
@@ -416,6 +418,15 @@ int table_shape(const pw_table* t, int* E, int* H, int* I) {
 
 }  // namespace pw
 
+// NVTX range around one C-ABI call (visible in Nsight timelines; a no-op when
+// no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 extern "C" {
 
 const char* pw_last_error(void) { return g_err.c_str(); }
@@ -438,6 +449,7 @@ size_t pw_lut_bytes(int R, int b_min, int n_bits) {
 
 int pw_pack(const uint8_t* idx, int R, int K, int n_bits, const uint16_t* parent_lut,
             int b_min, uint32_t* planes_out, uint16_t* luts_out) {
+  NvtxRange nvtx_range("pw_pack");
   if (!idx || !parent_lut || !planes_out || !luts_out) return fail(PW_EINVAL, "pw_pack: null pointer");
   if (R < 1 || K < 32 || K % 32)
     return fail(PW_EINVAL, "pw_pack: need R >= 1, K >= 32, K %% 32 == 0");
@@ -531,6 +543,7 @@ static inline uint32_t split_even_odd(uint32_t x) {
 }
 
 int pw_tile_planes(const uint32_t* planes, int n_bits, int R, int K, uint32_t* tiled_out) {
+  NvtxRange nvtx_range("pw_tile_planes");
   if (!planes || !tiled_out) return fail(PW_EINVAL, "pw_tile_planes: null pointer");
   if (n_bits < 1 || n_bits > PW_MAX_BITS || R < 32 || R % 32 || K < 64 || K % 64)
     return fail(PW_EINVAL, "pw_tile_planes: need 1 <= n_bits <= 8, R %% 32 == 0, K %% 64 == 0");
@@ -610,6 +623,7 @@ int pw_table_create(pw_table** out, int n_layers, int n_experts, int H, int I, v
 int pw_block_register(pw_table* t, int layer, int expert, int kind, int n_bits, int b_min,
                       const uint32_t* host_planes, const uint16_t* host_luts,
                       void* const* d_plane_pages, void* d_luts, int q_init, pw_stream_t s) {
+  NvtxRange nvtx_range("pw_block_register");
   if (!t) return fail(PW_EINVAL, "pw_block_register: null table");
   std::lock_guard<std::mutex> lk(t->mu);
   BlockState* b = block_of(t, layer, expert, kind);
@@ -662,12 +676,14 @@ int pw_block_register(pw_table* t, int layer, int expert, int kind, int n_bits, 
 }
 
 int pw_reload_async(pw_table* t, int layer, int expert, int kind, int q_target, pw_stream_t copy) {
+  NvtxRange nvtx_range("pw_reload_async");
   if (!t) return fail(PW_EINVAL, "pw_reload_async: null table");
   return reload_one(t, layer, expert, kind, q_target, reinterpret_cast<cudaStream_t>(copy));
 }
 
 int pw_reload_many(pw_table* t, int n, const int* layer, const int* expert, const int* kind,
                    const int* q_target, pw_stream_t copy, int* n_done) {
+  NvtxRange nvtx_range("pw_reload_many");
   if (n_done) *n_done = 0;
   if (!t) return fail(PW_EINVAL, "pw_reload_many: null table");
   if (n < 0 || (n > 0 && (!layer || !expert || !kind || !q_target)))
@@ -701,6 +717,7 @@ int pw_reload_query(pw_table* t, int layer, int expert, int kind) {
 }
 
 int pw_set_commit(pw_table* t, int layer, int expert, int kind, int q, pw_stream_t compute) {
+  NvtxRange nvtx_range("pw_set_commit");
   if (!t) return fail(PW_EINVAL, "pw_set_commit: null table");
   std::unique_lock<std::mutex> lk(t->mu);
   BlockState* b = nullptr;
@@ -717,6 +734,7 @@ int pw_set_commit(pw_table* t, int layer, int expert, int kind, int q, pw_stream
 
 int pw_set_commit_many(pw_table* t, int n, const int* layer, const int* expert, const int* kind,
                        const int* q, pw_stream_t compute) {
+  NvtxRange nvtx_range("pw_set_commit_many");
   if (!t) return fail(PW_EINVAL, "pw_set_commit_many: null table");
   if (n < 0 || (n > 0 && (!layer || !expert || !kind || !q)))
     return fail(PW_EINVAL, "pw_set_commit_many: bad count or null array");
@@ -760,6 +778,7 @@ int pw_mover_start(pw_table* t, pw_stream_t copy, size_t max_inflight_bytes) {
 
 int pw_mover_submit(pw_table* t, int n, const int* layer, const int* expert, const int* kind,
                     const int* q_target) {
+  NvtxRange nvtx_range("pw_mover_submit");
   if (!t) return fail(PW_EINVAL, "pw_mover_submit: null table");
   if (n < 0 || (n > 0 && (!layer || !expert || !kind || !q_target)))
     return fail(PW_EINVAL, "pw_mover_submit: bad count or null array");
@@ -787,6 +806,7 @@ int pw_mover_submit(pw_table* t, int n, const int* layer, const int* expert, con
 }
 
 int pw_plan_apply(pw_table* t, const int* desired, pw_stream_t compute, int* n_now, int* n_moved) {
+  NvtxRange nvtx_range("pw_plan_apply");
   if (n_now) *n_now = 0;
   if (n_moved) *n_moved = 0;
   if (!t || !desired) return fail(PW_EINVAL, "pw_plan_apply: null table or plan");
@@ -837,6 +857,7 @@ int pw_plan_apply(pw_table* t, const int* desired, pw_stream_t compute, int* n_n
 }
 
 int pw_commit_arrived(pw_table* t, pw_stream_t compute, int* n_committed, int* n_outstanding) {
+  NvtxRange nvtx_range("pw_commit_arrived");
   if (n_committed) *n_committed = 0;
   if (n_outstanding) *n_outstanding = 0;
   if (!t) return fail(PW_EINVAL, "pw_commit_arrived: null table");
@@ -889,6 +910,7 @@ int pw_commit_arrived(pw_table* t, pw_stream_t compute, int* n_committed, int* n
 }
 
 int pw_block_release(pw_table* t, int layer, int expert, int kind, int keep, void** released) {
+  NvtxRange nvtx_range("pw_block_release");
   if (!t) return fail(PW_EINVAL, "pw_block_release: null table");
   std::lock_guard<std::mutex> lk(t->mu);
   BlockState* b = block_of(t, layer, expert, kind);
@@ -909,6 +931,7 @@ int pw_block_release(pw_table* t, int layer, int expert, int kind, int keep, voi
 }
 
 int pw_block_attach_pages(pw_table* t, int layer, int expert, int kind, void* const* pages) {
+  NvtxRange nvtx_range("pw_block_attach_pages");
   if (!t || !pages) return fail(PW_EINVAL, "pw_block_attach_pages: null table or pages");
   std::lock_guard<std::mutex> lk(t->mu);
   BlockState* b = block_of(t, layer, expert, kind);
@@ -1008,6 +1031,7 @@ int pw_moe_forward(pw_table* t, int layer, const void* x, const float* logits, i
                    int renorm, const void* residual, void* out, int32_t* topk_idx, float* topk_w,
                    int32_t* offsets, int32_t* perm, void* workspace, size_t ws_bytes,
                    pw_stream_t compute) {
+  NvtxRange nvtx_range("pw_moe_forward");
   const int rc = forward_checks(t, layer, T, top_k, workspace, ws_bytes);
   if (rc != PW_OK) return rc;
   if (T == 0) return PW_OK;
@@ -1050,6 +1074,7 @@ int pw_moe_forward(pw_table* t, int layer, const void* x, const float* logits, i
 int pw_moe_forward_host(pw_table* t, int layer, const void* x_host, const float* logits_host,
                         int T, int top_k, int renorm, const void* residual_host, void* out_host,
                         void* workspace, size_t ws_bytes, pw_stream_t compute) {
+  NvtxRange nvtx_range("pw_moe_forward_host");
   int rc = forward_checks(t, layer, T, top_k, workspace, ws_bytes);
   if (rc != PW_OK) return rc;
   if (T == 0) return PW_OK;

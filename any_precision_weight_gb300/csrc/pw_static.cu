@@ -12,6 +12,7 @@
 // allocating library routine.
 
 #include <cuda.h>
+#include <nvtx3/nvToolsExt.h>
 #include <cudaTypedefs.h>
 #include <cstdio>
 #include <mutex>
@@ -22,6 +23,14 @@ namespace pw {
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;   // 8 MiB per device
+
+// NVTX range around the call (a no-op when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Scratch for pw_moe_forward_noalloc.  Host code must not use this name as a
 // pointer: it is a host-side stand-in; the device address comes from
@@ -89,6 +98,7 @@ cudaError_t scratch_address(void** out) {
 extern "C" int pw_moe_forward_noalloc(pw_table* t, int layer, const void* x, const float* logits,
                                       int T, int top_k, int renorm, const void* residual, void* out,
                                       pw_stream_t compute) {
+  pw::NvtxRange nvtx_range("pw_moe_forward_noalloc");
   int E = 0, H = 0, I = 0;   // the table's shapes size the scratch layout
   if (!t || pw::table_shape(t, &E, &H, &I) != PW_OK)
     return pw::set_error(PW_EINVAL, "pw_moe_forward_noalloc: null or invalid table");

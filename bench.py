@@ -330,7 +330,11 @@ def timed_forwards(m, cfg, X, Lg, ws, out, n, start=0, serial=True):
     stream = torch.cuda.current_stream()
     evs = []
     if serial:
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+        # the decode path is one kernel: an event before it and one right after it
+        # (no other events between two forwards); the prefill path has four
+        # kernels and five boundary events
+        ne = 2 if is_fused(cfg) else 5
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(ne)] for _ in range(n)]
         for row in evs:              # torch creates the CUDA event at its first record
             for e in row:
                 e.record(stream)
@@ -341,7 +345,7 @@ def timed_forwards(m, cfg, X, Lg, ws, out, n, start=0, serial=True):
     for i in range(n):
         l = (start + i) % n_inst
         if serial:
-            pw.pw_profile_attach(evs[i])
+            pw.pw_profile_attach(evs[i] if len(evs[i]) == 5 else evs[i] + [None, None, None])
         m.pw_moe_forward(l, X[l], Lg[l], cfg.top_k, cfg.renorm, out=out, ws=ws)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -352,7 +356,7 @@ def kernel_times(cfg, evs):
     """Average ms per launch of each kernel from the per-forward events."""
     fused = is_fused(cfg)
     if fused:
-        return {"layer_fused": sum(r[0].elapsed_time(r[4]) for r in evs) / len(evs)}
+        return {"layer_fused": sum(r[0].elapsed_time(r[1]) for r in evs) / len(evs)}
     names = ["route_permute", "gate_up", "down", "combine"]
     return {nm: sum(r[j].elapsed_time(r[j + 1]) for r in evs) / len(evs) for j, nm in enumerate(names)}
 
@@ -449,6 +453,13 @@ def measure_layer(cfg, dev, local, steps, warmup, n_inst, world=1, uniform=None,
                     "because the logits are ready in advance; in a model other layers sit between two MoE "
                     "layers, so this overlap is not counted in value or roofline"}
     if per_q and is_fused(cfg):
+        # every plane of every block onto the device first (a reload from the
+        # pinned host copies), so that any uniform bitwidth is one commit away
+        items = [(l, e, k, 8) for l in range(n_inst) for e in range(cfg.E) for k in (0, 1)]
+        copy = torch.cuda.Stream(device=dev)
+        for i in range(0, len(items), 4096):
+            m.pw_reload_many(items[i:i + 4096], stream=copy)
+        copy.synchronize()
         sweep = {}
         for q in (3, 4, 5, 6, 7, 8):
             commit_uniform(m, n_inst, q)

@@ -63,6 +63,9 @@ extern "C" {
 #define PW_STATUS_NAN_LOGIT  1  /* a router logit was NaN (treated as -inf)     */
 #define PW_STATUS_TIMEOUT    2  /* a bounded device-side wait gave up           */
 #define PW_STATUS_BAD_DESC   4  /* an active block had no usable descriptor     */
+#define PW_STATUS_BOUNDS     8  /* a device-side bounds check failed; the access
+                                   was skipped (libpw_check.so, built with
+                                   PW_CHECK, only)                             */
 
 #define PW_KIND_GATE_UP 0
 #define PW_KIND_DOWN    1

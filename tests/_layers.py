@@ -10,6 +10,8 @@ from oracle import moe as omoe
 
 REL_L2 = 1e-3     # float tolerance of the fused layer vs the fp64 oracle
 MAX_ABS = 2e-2
+GUARD = 256       # canary bytes on both sides of every device buffer of the test layers
+LIVE = []         # layers built by the running test; their guards are checked after it
 
 
 class SynthBlocks:
@@ -29,7 +31,8 @@ def gpu_layer(cfg, n_layers=1, bits=None, blocks=None, alloc_planes=None, layers
     the lowest bitwidth whose tables are stored."""
     import any_precision_weight_gb300 as pw
     from any_precision_weight_gb300.model import load_expert_layer
-    m = pw.PagedMoE(n_layers, cfg.E, cfg.H, cfg.I)
+    m = pw.PagedMoE(n_layers, cfg.E, cfg.H, cfg.I, guard=GUARD)
+    LIVE.append(m)
     for l in (range(n_layers) if layers is None else layers):
         b = synth.block_bits(cfg, l) if bits is None else bits[l]
         src = SynthBlocks(cfg, l) if blocks is None else blocks[l]

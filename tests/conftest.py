@@ -27,3 +27,18 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _device_buffer_guards(request):
+    """After every GPU test: no canary guard around a device buffer of the
+    test's layers (pages, tables, descriptors, workspaces) has changed."""
+    yield
+    if "gpu" not in request.keywords:
+        return
+    import _layers
+    bad = []
+    for m in _layers.LIVE:
+        bad.extend(m.corrupted_guards())
+    _layers.LIVE.clear()
+    assert not bad, f"device buffer guards overwritten: {bad[:8]}"
