@@ -295,14 +295,19 @@ __device__ __forceinline__ bool desc_ok(const Fwd& p, const BlockDesc& d, int ki
   return d.q >= 1 && d.q <= PW_MAX_BITS && d.K == (gu ? p.H : p.I) && d.R == (gu ? 2 * p.I : p.H);
 }
 
-// This warp's plane-word units (2 words each) of an item: [u0, u1), inside
-// the item's K-range (K-split part `split` of `nsplit`).
-__device__ __forceinline__ void warp_units(const BlockDesc& d, bool ok, int warp, int split, int nsplit, int& u0,
-                                           int& u1) {
-  const int U = ok ? (d.K >> 6) : 0;
-  const int s0 = U * split / nsplit, n = U * (split + 1) / nsplit - s0;
-  u0 = s0 + n * warp / kWarps;
-  u1 = s0 + n * (warp + 1) / kWarps;
+// This warp's share of an item: plane words [w0, w1) of the item's K-range
+// (K-split part `split` of `nsplit`), dealt word by word so that the twelve
+// shares differ by at most one word, and the ring units (word pairs) that
+// hold them, [u0, u1); a share that starts or ends inside a pair uses one of
+// its two words.
+__device__ __forceinline__ void warp_share(const BlockDesc& d, bool ok, int warp, int split, int nsplit, int& w0,
+                                           int& w1, int& u0, int& u1) {
+  const int W = ok ? (d.K >> 5) : 0;
+  const int s0 = W * split / nsplit, n = W * (split + 1) / nsplit - s0;
+  w0 = s0 + n * warp / kWarps;
+  w1 = s0 + n * (warp + 1) / kWarps;
+  u0 = w0 >> 1;
+  u1 = w1 > w0 ? (w1 + 1) >> 1 : u0;
 }
 
 // ------------------------------------------------------------------ tables
@@ -540,7 +545,8 @@ __device__ __forceinline__ void fetch_enter(Fetch& f, const Fwd& p, const Smem& 
   f.item = item;
   f.desc = smem_addr(&d);
   const bool ok = it.valid && desc_ok(p, d, it.kind);
-  warp_units(d, ok, warp, it.split, it.kind == PW_KIND_DOWN ? p.ksplit : 1, f.u, f.end);
+  int w0, w1;
+  warp_share(d, ok, warp, it.split, it.kind == PW_KIND_DOWN ? p.ksplit : 1, w0, w1, f.u, f.end);
   const int h = lane >> 4;
   int grp;   // 32-row group of row half h
   if (it.kind == PW_KIND_GATE_UP) grp = h ? p.I / 32 + it.tile : it.tile;
@@ -601,16 +607,15 @@ __device__ __forceinline__ void fetch_fill(Fetch& f, const Fwd& p, const Smem& s
   }
 }
 
-// The warp's units [u0, u1) of one item: ring stages in, transposes, lookups,
-// MMAs.  Two code paths: pair tables (q <= 4, four plane slots) and single
+// The warp's units [u0, u1) of one item (its words [w0, w1)): ring stages in,
+// transposes, lookups, MMAs.  Two code paths: pair tables (q <= 4, four plane slots) and single
 // lookups (q >= 5, eight plane slots); missing planes read as zero slots.
 template <bool PAIR>
 __device__ __forceinline__ void run_units(const Fwd& p, const Smem& sm, const ItemInfo* s_item, Fetch& f,
                                           int known, Ring& rg, int warp, int lane, uint32_t lo0, uint32_t lo1,
-                                          int u0, int u1, Tok& t, float (&acc)[2][2][4]) {
+                                          int u0, int u1, int w0, int w1, Tok& t, float (&acc)[2][2][4]) {
   constexpr int NR = PAIR ? 4 : 8;   // index bits held (rows of the transposes)
   constexpr int SZ = PAIR ? 1 : 2;   // half-stages per unit
-  const int w1 = u1 * kUnitWords;
   for (int u = u0; u < u1; ++u) {
     cp_wait_n(rg.iu - rg.cu - 1);
     __syncwarp();   // every lane's copies of this unit visible; the previous unit is read
@@ -628,6 +633,7 @@ __device__ __forceinline__ void run_units(const Fwd& p, const Smem& sm, const It
 #pragma unroll
     for (int wi = 0; wi < kUnitWords; ++wi) {
       const int gw = u * kUnitWords + wi;
+      if (gw < w0 || gw >= w1) continue;   // the other word of a pair at the share's edge
       const bool more = gw + 1 < w1;
       uint32_t o0[NR], o1[NR];
 #pragma unroll
@@ -924,8 +930,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
       lut_load(lr, d1, rho, rho2, warp);
     }
 
-    int u0, u1;
-    warp_units(d, ok, warp, it.split, gu ? 1 : p.ksplit, u0, u1);
+    int w0, w1, u0, u1;
+    warp_share(d, ok, warp, it.split, gu ? 1 : p.ksplit, w0, w1, u0, u1);
     float acc[2][2][4];
 #pragma unroll
     for (int j = 0; j < 2; ++j)
@@ -957,7 +963,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
         }
         __syncwarp();
       }
-      const int w0 = u0 * kUnitWords;
 #pragma unroll
       for (int k4 = 0; k4 < 4; ++k4) {
         t.X0[k4] = make_uint4(0u, 0u, 0u, 0u);
@@ -965,8 +970,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
         ld_x16(t.X0[k4], t.x0 + w0 * 4 + k4, t.x0 != nullptr);
         ld_x16(t.X1[k4], t.x1 + w0 * 4 + k4, t.x1 != nullptr);
       }
-      if (pair_mode(d.q, d.K)) run_units<true>(p, sm, s_item, f, known, rg, warp, lane, lo0, lo1, u0, u1, t, acc);
-      else run_units<false>(p, sm, s_item, f, known, rg, warp, lane, lo0, lo1, u0, u1, t, acc);
+      if (pair_mode(d.q, d.K)) run_units<true>(p, sm, s_item, f, known, rg, warp, lane, lo0, lo1, u0, u1, w0, w1, t, acc);
+      else run_units<false>(p, sm, s_item, f, known, rg, warp, lane, lo0, lo1, u0, u1, w0, w1, t, acc);
     }
     // keep the ring running into the next item while this one finishes
     __syncwarp();

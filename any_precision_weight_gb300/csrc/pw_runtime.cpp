@@ -256,6 +256,13 @@ void mover_main(pw_table* t) {
   };
   std::deque<Flight> flight;
   std::vector<cudaEvent_t> spare;
+  // a pool of completion events made before any request arrives, so that the
+  // copies of a reload window are not interleaved with event creation
+  for (int i = 0; i < 128; ++i) {
+    cudaEvent_t ev = nullptr;
+    if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) break;
+    spare.push_back(ev);
+  }
   size_t inflight = 0;
   auto note_error = [t](int rc, const char* msg) {
     std::lock_guard<std::mutex> lk(t->mover_mu);
@@ -657,6 +664,13 @@ int pw_block_register(pw_table* t, int layer, int expert, int kind, int n_bits, 
   for (int p = 0; p < n_bits; ++p) nb.pages[p] = d_plane_pages[p];
   nb.d_luts = d_luts;
   nb.ev = b->ev;
+  if (!nb.ev) {
+    // created here, not at the first reload: a reload window then issues only
+    // copies (creating events inside it cost the first window most of its rate)
+    const cudaError_t ee = cudaEventCreateWithFlags(&nb.ev, cudaEventDisableTiming);
+    if (ee != cudaSuccess) return cuda_fail(ee, "pw_block_register: event create");
+    b->ev = nb.ev;   // owned by the block from now on (destroyed with the table)
+  }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(s);
   const size_t pb = pw_plane_bytes(R, K);
   for (int p = 0; p < q_init; ++p) {
