@@ -26,7 +26,10 @@
 //    not stop at item boundaries;
 //  * the inner loop has two code paths, pair tables (q <= 4) and single
 //    lookups (q >= 5), each for any q of its range (missing planes read as
-//    zero plane slots), so that the hot code stays small;
+//    zero plane slots), so that the hot code stays small.  The kernel is built
+//    twice: with both paths for layers of hidden size >= 4096, and with the
+//    single-lookup path alone (every q) for smaller ones, whose short items
+//    do not repay the pair tables;
 //  * q <= 4: pair tables.  The page keeps the even elements of every byte in
 //    its low half and the odd ones in its high half, so a 4x4 bit transpose of
 //    the q plane words nibble by nibble (four delta swaps per four words)
@@ -176,6 +179,11 @@ __device__ __forceinline__ void planes_to_pairs(uint32_t (&o)[4]) {
 
 // Table slot at shared address a.
 __device__ __forceinline__ uint32_t lut_slot(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
@@ -533,10 +541,12 @@ struct Ring {
   uint32_t base;
   int ih, ch, iu, cu;
 };
-// Pair tables for blocks of at most 4 bits.
-__device__ __forceinline__ bool pair_mode(int q, int /*K*/) { return q <= 4; }
+// Pair tables for blocks of at most 4 bits, in the kernel built with them (kPairs).
+template <bool kPairs>
+__device__ __forceinline__ bool pair_mode(int q) { return kPairs && q <= 4; }
 __device__ __forceinline__ int unit_halves(bool pair) { return pair ? 1 : 2; }
 
+template <bool kPairs>
 __device__ __forceinline__ void fetch_enter(Fetch& f, const Fwd& p, const Smem& sm, const ItemInfo* s_item,
                                             int item, int warp, int lane) {
   const int sl = item % kSlots;
@@ -552,7 +562,7 @@ __device__ __forceinline__ void fetch_enter(Fetch& f, const Fwd& p, const Smem& 
   if (it.kind == PW_KIND_GATE_UP) grp = h ? p.I / 32 + it.tile : it.tile;
   else grp = 2 * it.tile + h;
   f.q = d.q;
-  f.pair = pair_mode(d.q, d.K);
+  f.pair = pair_mode<kPairs>(d.q);
 #ifdef PW_CHECK
   f.words = static_cast<size_t>(d.R) * static_cast<size_t>(d.K) / 32;
 #endif
@@ -567,12 +577,13 @@ __device__ __forceinline__ void fetch_enter(Fetch& f, const Fwd& p, const Smem& 
 // always slot 3 - r or 7 - r; the slots below s0 are zeroed.  The caller has
 // synchronised the warp after the last read of the half-stages the issue may
 // overwrite (everything before the unit being consumed).
+template <bool kPairs>
 __device__ __forceinline__ void fetch_fill(Fetch& f, const Fwd& p, const Smem& sm, const ItemInfo* s_item,
                                            int known, Ring& rg, int warp, int lane) {
   for (;;) {
     while (f.u == f.end) {   // the warp has no more units in this item
       if (f.item + 1 > known) return;
-      fetch_enter(f, p, sm, s_item, f.item + 1, warp, lane);
+      fetch_enter<kPairs>(f, p, sm, s_item, f.item + 1, warp, lane);
     }
     const int sz = unit_halves(f.pair);
     const int pad = (sz == 2 && (rg.ih & 1)) ? 1 : 0;
@@ -610,7 +621,7 @@ __device__ __forceinline__ void fetch_fill(Fetch& f, const Fwd& p, const Smem& s
 // The warp's units [u0, u1) of one item (its words [w0, w1)): ring stages in,
 // transposes, lookups, MMAs.  Two code paths: pair tables (q <= 4, four plane slots) and single
 // lookups (q >= 5, eight plane slots); missing planes read as zero slots.
-template <bool PAIR>
+template <bool kPairs, bool PAIR>
 __device__ __forceinline__ void run_units(const Fwd& p, const Smem& sm, const ItemInfo* s_item, Fetch& f,
                                           int known, Ring& rg, int warp, int lane, uint32_t lo0, uint32_t lo1,
                                           int u0, int u1, int w0, int w1, Tok& t, float (&acc)[2][2][4]) {
@@ -620,26 +631,20 @@ __device__ __forceinline__ void run_units(const Fwd& p, const Smem& sm, const It
     cp_wait_n(rg.iu - rg.cu - 1);
     __syncwarp();   // every lane's copies of this unit visible; the previous unit is read
     if (SZ == 2 && (rg.ch & 1)) ++rg.ch;   // the issue's pad
-    fetch_fill(f, p, sm, s_item, known, rg, warp, lane);
+    fetch_fill<kPairs>(f, p, sm, s_item, known, rg, warp, lane);
     const uint32_t st = rg.base + (rg.ch & (kHalfStages - 1)) * kHalfStageBytes + lane * 8;
     rg.ch += SZ;
     ++rg.cu;
-    uint2 pa[NR], pb[NR];   // row r (bit r of the index) = slot NR-1-r, both words of the unit
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-      pa[r] = lds64(st + (NR - 1 - r) * kPlaneSlot);
-      pb[r] = lds64(st + (NR - 1 - r) * kPlaneSlot + 256);
-    }
-#pragma unroll
+#pragma unroll 1
     for (int wi = 0; wi < kUnitWords; ++wi) {
       const int gw = u * kUnitWords + wi;
       if (gw < w0 || gw >= w1) continue;   // the other word of a pair at the share's edge
       const bool more = gw + 1 < w1;
-      uint32_t o0[NR], o1[NR];
+      uint32_t o0[NR], o1[NR];   // row r (bit r of the index) = slot NR-1-r
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
-        o0[r] = wi ? pa[r].y : pa[r].x;
-        o1[r] = wi ? pb[r].y : pb[r].x;
+        o0[r] = lds32(st + (NR - 1 - r) * kPlaneSlot + wi * 4);
+        o1[r] = lds32(st + (NR - 1 - r) * kPlaneSlot + 256 + wi * 4);
       }
       if constexpr (PAIR) {
         planes_to_pairs(o0);
@@ -758,6 +763,7 @@ __device__ void combine_tile(const Fwd& p, const RouteSmem& r, int tile, int tid
 // whichever CTAs are resident.  The last down item of a 64-row output tile
 // combines it.  Every wait is bounded and reports PW_STATUS_TIMEOUT instead of
 // hanging.
+template <bool kPairs>
 __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const Smem sm = smem_layout();
@@ -887,10 +893,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     lane_rows(p, s_item[0], lane, rho, rho2);
     const bool ok0 = desc_ok(p, d0, s_item[0].kind);
     if (ok0) lut_load(lr, d0, rho, rho2, warp);
-    fetch_enter(f, p, sm, s_item, 0, warp, lane);
-    fetch_fill(f, p, sm, s_item, s_item[1].valid ? 1 : 0, rg, warp, lane);
+    fetch_enter<kPairs>(f, p, sm, s_item, 0, warp, lane);
+    fetch_fill<kPairs>(f, p, sm, s_item, s_item[1].valid ? 1 : 0, rg, warp, lane);
     if (ok0) {
-      if (!pair_mode(d0.q, d0.K)) {
+      if (!pair_mode<kPairs>(d0.q)) {
         lut_store_single(sm.table, kLine, lr, d0.q, lane, warp);
       } else {
         lut_store_single(scratch, 128, lr, d0.q, lane, warp);
@@ -970,12 +976,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
         ld_x16(t.X0[k4], t.x0 + w0 * 4 + k4, t.x0 != nullptr);
         ld_x16(t.X1[k4], t.x1 + w0 * 4 + k4, t.x1 != nullptr);
       }
-      if (pair_mode(d.q, d.K)) run_units<true>(p, sm, s_item, f, known, rg, warp, lane, lo0, lo1, u0, u1, w0, w1, t, acc);
-      else run_units<false>(p, sm, s_item, f, known, rg, warp, lane, lo0, lo1, u0, u1, w0, w1, t, acc);
+      if (pair_mode<kPairs>(d.q))
+        run_units<kPairs, true>(p, sm, s_item, f, known, rg, warp, lane, lo0, lo1, u0, u1, w0, w1, t, acc);
+      else
+        run_units<kPairs, false>(p, sm, s_item, f, known, rg, warp, lane, lo0, lo1, u0, u1, w0, w1, t, acc);
     }
     // keep the ring running into the next item while this one finishes
     __syncwarp();
-    fetch_fill(f, p, sm, s_item, known, rg, warp, lane);
+    fetch_fill<kPairs>(f, p, sm, s_item, known, rg, warp, lane);
 
     // ---- partial sums: red[warp][half * 4 + token][lane]
     float* red = reinterpret_cast<float*>(sm.misc + kRedOff);
@@ -994,7 +1002,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     }
     // a q <= 4 next item: its single slots into the scratch lines now (the
     // pair tables are built from them after the barrier)
-    if (ok1 && pair_mode(d1.q, d1.K)) lut_store_single(scratch, 128, lr, d1.q, lane, warp);
+    if (ok1 && pair_mode<kPairs>(d1.q)) lut_store_single(scratch, 128, lr, d1.q, lane, warp);
     // a down tile whose last item completed with the previous item: combine it now;
     // item i+2 from the ticket claimed at this item's start
     if (tid == 0) {
@@ -1007,7 +1015,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     pending_old = -1;
 
     if (ok1) {
-      if (!pair_mode(d1.q, d1.K)) lut_store_single(sm.table, kLine, lr, d1.q, lane, warp);
+      if (!pair_mode<kPairs>(d1.q)) lut_store_single(sm.table, kLine, lr, d1.q, lane, warp);
       else pair_tables(sm.table, scratch, d1.q, lane, warp);
     }
     if (warp == 0 && lane < 8 && s_item[sl2].valid)
@@ -1063,6 +1071,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
 constexpr int kMaxDevices = 64;
 int g_fused[kMaxDevices] = {};   // co-resident grid of the fused layer per device
 
+// Pair tables pay for their larger tables (64 KB rebuilt per q = 4 item) and
+// the second inner loop only when items are long.  Measured on GB300: with
+// them, Mixtral-8x7B-shaped decode layers (H = 4096) run 5 % faster, and
+// Qwen1.5-MoE-shaped ones (H = 2048; gate_up items of 5 plane words per warp)
+// 6 % slower, since the pair code also slows the q >= 5 loop.  So the kernel
+// is built twice and the layer's hidden size picks one.
+constexpr int kPairsMinH = 4096;
+
 }  // namespace
 
 cudaError_t launch_layer_fused(const Fwd& p, cudaStream_t s) {
@@ -1072,10 +1088,15 @@ cudaError_t launch_layer_fused(const Fwd& p, cudaStream_t s) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (p.H % kDownTileRows != 0 || p.I % kGateUpTileRows != 0) return cudaErrorInvalidValue;
   if (g_fused[dev] == 0) {   // once per device: shared-memory opt-in and co-resident grid size
-    e = cudaFuncSetAttribute(k_layer, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    int per_sm = 0, sms = 0;
+    e = cudaFuncSetAttribute(k_layer<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_layer, kThreads, kSmemBytes);
+      e = cudaFuncSetAttribute(k_layer<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    int per_sm = 0, per_sm1 = 0, sms = 0;
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_layer<true>, kThreads, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm1, k_layer<false>, kThreads, kSmemBytes);
+    per_sm = per_sm < per_sm1 ? per_sm : per_sm1;
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
@@ -1096,7 +1117,7 @@ cudaError_t launch_layer_fused(const Fwd& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_layer, p);
+  return p.H >= kPairsMinH ? cudaLaunchKernelEx(&cfg, k_layer<true>, p) : cudaLaunchKernelEx(&cfg, k_layer<false>, p);
 }
 
 }  // namespace pw

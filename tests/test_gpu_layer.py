@@ -54,19 +54,24 @@ def test_tiny_every_bitwidth(q):
     assert_close(out, ref["out"])
 
 
-@pytest.mark.parametrize("cfg_name", ["tiny", "prefill_small"])
+@pytest.mark.parametrize("cfg_name", ["tiny", "pair_build", "prefill_small"])
 def test_one_and_two_bit_blocks(cfg_name):
     """Blocks committed at 1 and 2 bits (tables of 2 and 4 entries per row, below
     the 8-entry chunks the kernels otherwise load), mixed with higher bitwidths,
-    on the decode kernel (tiny) and on the tensor-core path (300 tokens)."""
+    on both builds of the decode kernel (hidden size 256: without pair tables;
+    4096: with them, for q <= 4) and on the tensor-core path (300 tokens)."""
     if cfg_name == "tiny":
         cfg = synth.CONFIGS["tiny"]
+    elif cfg_name == "pair_build":
+        cfg = synth.CONFIGS["tiny"].with_(H=4096, T=5)
     else:
         cfg = synth.CONFIGS["mixtral_prefill"].with_(T=300, H=256, I=512)
     rng = np.random.default_rng(7)
     bits = rng.integers(1, 9, size=(cfg.E, 2)).astype(np.int32)
     bits[0] = (1, 2)
     bits[1] = (2, 1)
+    bits[2] = (3, 4)
+    bits[3] = (4, 3)
     m = gpu_layer(cfg, bits={0: bits}, b_min=1)
     x, L = synth.tokens(cfg, step=11), synth.logits(cfg, step=11)
     out, ri, rw, ro, rp = _run(m, cfg, x, L)
@@ -75,13 +80,14 @@ def test_one_and_two_bit_blocks(cfg_name):
     assert_close(out, ref["out"])
 
 
-def test_integer_tables_bit_exact():
+@pytest.mark.parametrize("H", [256, 4096])   # the decode kernel's two builds
+def test_integer_tables_bit_exact(H):
     """Integer tables whose child table at the committed q is integer, 0/1 tokens
     with 19 ones, top-1 routing: gate sums lie in [38, 57], where e^-g is below
     half an ulp of 1 in fp64 as in fp32, so silu(g) == g on both sides; every
     sum is an exact integer, |h| <= 57 * 19 fits fp16 exactly, and out must
     equal the oracle's fp16 rounding bit for bit."""
-    cfg = synth.CONFIGS["tiny"].with_(T=16, top_k=1, renorm=1)
+    cfg = synth.CONFIGS["tiny"].with_(T=16, top_k=1, renorm=1, H=H)
     rng = np.random.default_rng(99)
     E, H, I = cfg.E, cfg.H, cfg.I
     bits = rng.integers(3, 9, size=(E, 2)).astype(np.int32)
