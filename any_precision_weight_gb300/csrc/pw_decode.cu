@@ -245,11 +245,13 @@ struct ItemInfo {
   int n;      // tokens of this pass (1..4)
   int off;    // permuted position of the pass's first token
   int need;   // down: gate_up items of the expert that must be done first
-  int split;  // down: which of the p.ksplit K-ranges
+  int split;   // down: which of the nsplit K-ranges
+  int nsplit;  // down: K-ranges of the forward's down items (1 for gate_up)
 };
 
 struct Plan {
   int nact, tiles_gu, tiles_dn, total_gu, total, down_per_tile;
+  int ks;              // K-ranges per down item in this forward (<= p.ksplit)
   const int* cum_gu;   // [nact+1] first gate_up item of each cost rank
   const int* cum_dn;
 };
@@ -280,6 +282,7 @@ __device__ ItemInfo item_of(int g, const Plan& pl, const RouteSmem& r, int kspli
   it.expert = e;
   it.tile = (rem % tiles) / S;
   it.split = (rem % tiles) % S;
+  it.nsplit = S;
   it.n = min(kTokPass, cnt - pass * kTokPass);
   it.off = r.off[e] + pass * kTokPass;
   it.need = pl.tiles_gu * ((cnt + kTokPass - 1) / kTokPass);
@@ -556,7 +559,7 @@ __device__ __forceinline__ void fetch_enter(Fetch& f, const Fwd& p, const Smem& 
   f.desc = smem_addr(&d);
   const bool ok = it.valid && desc_ok(p, d, it.kind);
   int w0, w1;
-  warp_share(d, ok, warp, it.split, it.kind == PW_KIND_DOWN ? p.ksplit : 1, w0, w1, f.u, f.end);
+  warp_share(d, ok, warp, it.split, it.nsplit, w0, w1, f.u, f.end);
   const int h = lane >> 4;
   int grp;   // 32-row group of row half h
   if (it.kind == PW_KIND_GATE_UP) grp = h ? p.I / 32 + it.tile : it.tile;
@@ -668,6 +671,7 @@ __device__ __forceinline__ uint4 desc_part(const Fwd& p, const Smem& sm, bool ca
 // ------------------------------------------------------------------ fused layer
 
 constexpr int kSpinLimit = 1 << 22;   // ~0.3 s of polling before a wait gives up
+constexpr int kSplitWaves = 3;        // down items wanted per CTA before K-splitting stops
 
 __device__ __forceinline__ int ld_acquire(const int* ptr) {
   int v;
@@ -733,9 +737,10 @@ __device__ bool wait_published(const Fwd& p) {
 }
 
 // Combine of one 64-row output tile once all its down items are done (the
-// whole CTA): with K-split down items, y = the parts added in split order
-// (written to y for inspection), then out = residual + sum_j w * y.
-__device__ void combine_tile(const Fwd& p, const RouteSmem& r, int tile, int tid) {
+// whole CTA): when the down items write parts (a workspace with room for a
+// K-split), y = the ks parts added in split order (written to y for
+// inspection), then out = residual + sum_j w * y.
+__device__ void combine_tile(const Fwd& p, const RouteSmem& r, int tile, int ks, int tid) {
   const int r0 = tile * kDownTileRows, r1 = min(r0 + kDownTileRows, p.H);
   if (p.ksplit > 1) {
     const int P = p.T * p.k, n = r1 - r0;
@@ -743,7 +748,7 @@ __device__ void combine_tile(const Fwd& p, const RouteSmem& r, int tile, int tid
     for (int q = tid; q < P * n; q += kThreads) {
       const size_t at = static_cast<size_t>(q / n) * p.H + r0 + q % n;
       float v = 0.f;
-      for (int sp = 0; sp < p.ksplit; ++sp) v += __ldcg(p.y_part + sp * part + at);
+      for (int sp = 0; sp < ks; ++sp) v += __ldcg(p.y_part + sp * part + at);
       p.y[at] = v;
     }
     __syncthreads();
@@ -821,15 +826,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
       }
       if (a <= pl.nact) {
         cum_gu[a] = (run + incl - np) * pl.tiles_gu;
-        cum_dn[a] = (run + incl - np) * pl.tiles_dn * p.ksplit;
+        cum_dn[a] = run + incl - np;   // passes before rank a (scaled below)
       }
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
+    // K-split of the down items: as many K-ranges (up to the workspace's
+    // p.ksplit) as it takes for the down items to fill kSplitWaves waves of
+    // the grid.  A few long down items (one token, two experts) leave most
+    // CTAs idle at the end of the layer; more K-ranges than that only add item
+    // boundaries and partial sums.  Measured on the Mixtral-8x7B-shaped layer:
+    // batch 4 (384 unsplit down items) 352 us at 4 ranges, 344 at 1, 340 at 2;
+    // batch 1 (128) 135 us at 4, 134 at 3.
+    const int items_dn = run * pl.tiles_dn;
+    const int want = kSplitWaves * static_cast<int>(gridDim.x);
+    const int ks = items_dn > 0 ? max(1, min(p.ksplit, (want + items_dn - 1) / items_dn)) : 1;
+    for (int a = lane; a <= pl.nact; a += 32) cum_dn[a] *= pl.tiles_dn * ks;
+    if (lane == 0) s_int[4] = ks;
   }
   cp_wait<0>();   // the descriptor cache
   __syncthreads();
   pl.cum_gu = cum_gu;
   pl.cum_dn = cum_dn;
+  pl.ks = s_int[4];
   pl.total_gu = cum_gu[pl.nact];
   pl.total = pl.total_gu + cum_dn[pl.nact];
   pl.down_per_tile = pl.tiles_dn > 0 ? cum_dn[pl.nact] / pl.tiles_dn : 0;
@@ -872,7 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   }
   __syncthreads();
   // items of the first two tickets and their descriptors
-  if (tid < 2) s_item[tid] = item_of(s_int[2] + tid, pl, r, p.ksplit);
+  if (tid < 2) s_item[tid] = item_of(s_int[2] + tid, pl, r, pl.ks);
   __syncthreads();
   if (warp == 0 && lane < 16) {
     const int sl = lane >> 3, part = lane & 7;
@@ -918,7 +936,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     const bool ok = desc_ok(p, d, it.kind) &&
                     PW_BOUNDS(p, it.expert >= 0 && it.expert < p.E && it.off >= 0 && it.off + it.n <= p.T * p.k &&
                                      it.tile >= 0 && it.tile < (gu ? pl.tiles_gu : pl.tiles_dn) &&
-                                     it.split >= 0 && it.split < (gu ? 1 : p.ksplit),
+                                     it.split >= 0 && it.split < it.nsplit && it.nsplit <= (gu ? 1 : p.ksplit),
                               tid == 0);
 
     // item i+2's ticket: claimed now, looked at when this item ends
@@ -937,7 +955,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     }
 
     int w0, w1, u0, u1;
-    warp_share(d, ok, warp, it.split, gu ? 1 : p.ksplit, w0, w1, u0, u1);
+    warp_share(d, ok, warp, it.split, it.nsplit, w0, w1, u0, u1);
     float acc[2][2][4];
 #pragma unroll
     for (int j = 0; j < 2; ++j)
@@ -1007,10 +1025,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     // item i+2 from the ticket claimed at this item's start
     if (tid == 0) {
       s_int[1] = pending_old == pl.down_per_tile - 1 ? pending_tile : -1;
-      s_item[sl2] = it1.valid ? item_of(ticket_of(p, claim), pl, r, p.ksplit) : ItemInfo{};
+      s_item[sl2] = it1.valid ? item_of(ticket_of(p, claim), pl, r, pl.ks) : ItemInfo{};
     }
     __syncthreads();   // every lookup of this item is done; partials visible
-    if (s_int[1] >= 0) combine_tile(p, r, s_int[1], tid);
+    if (s_int[1] >= 0) combine_tile(p, r, s_int[1], pl.ks, tid);
     pending_tile = -1;
     pending_old = -1;
 
@@ -1064,7 +1082,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   }
   if (tid == 0) s_int[1] = pending_old == pl.down_per_tile - 1 ? pending_tile : -1;
   __syncthreads();
-  if (s_int[1] >= 0) combine_tile(p, r, s_int[1], tid);
+  if (s_int[1] >= 0) combine_tile(p, r, s_int[1], pl.ks, tid);
   cp_wait<0>();
 }
 
