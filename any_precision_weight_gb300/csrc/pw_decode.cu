@@ -15,13 +15,15 @@
 //    expert's tokens, laid out in a fixed order (largest gate_up cost first,
 //    then all down tiles) and handed out by tickets in that order, so every
 //    CTA knows its next items and loads their descriptors and tables ahead of
-//    time;
+//    time; when the routed batch gives few down items (one token, long K),
+//    each is split into K-ranges whose partial sums the combine adds in a
+//    fixed order;
 //  * lane l of every warp owns two rows of the tile (gate row l and up row l,
 //    or rows l and 32 + l); the twelve warps split K;
 //  * each warp streams its own plane words through a private cp.async ring of
 //    four 2 KB half-stages (one coalesced 16-byte copy per lane and plane, the
 //    pages being interleaved across 32-row groups; a unit of a q <= 4 block
-//    takes one half-stage, so three can be in flight, a q >= 5 unit two) that
+//    takes one half-stage, a q >= 5 unit two) that
 //    runs on into the warp's share of the next item, so the HBM stream does
 //    not stop at item boundaries;
 //  * the inner loop has two code paths, pair tables (q <= 4) and single
