@@ -62,9 +62,11 @@ inline size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255);
 // The decode path's batches (T <= 64 tokens, T*k <= 256 routed pairs).
 PW_HD inline bool fused_batch(int T, int k) { return T <= 64 && T * k <= 256; }
 
-// K-splits of a decode down item (64 rows x K = I): about I / H parts, so that a
-// down item costs about as much as a gate_up item (64 rows x H), as long as
-// every part keeps at least 24 word pairs (2 per K-warp); 1 when I <= H.
+// Largest K-split of a decode down item (64 rows x K = I) that the workspace
+// makes room for: about I / H parts, so that a down item costs about as much
+// as a gate_up item (64 rows x H), as long as every part keeps at least 24
+// word pairs (2 per K-warp); 1 when I <= H.  The decode kernel uses fewer
+// parts when the routed batch already gives enough down items.
 PW_HD inline int down_splits(int H, int I) {
   int s = (I + H / 2) / H;
   const int cap = (I / 64) / 24;
