@@ -200,18 +200,26 @@ def test_prefill_shaped_small():
 @pytest.mark.slow
 def test_mixtral_prefill_sampled():
     """Full-size Mixtral-shaped prefill (2048 tokens) on the tensor-core path:
-    routing bit-exact for every token, outputs compared on sampled tokens and rows."""
+    routing bit-exact for every token; for 32 sampled tokens (64 routed pairs,
+    spread over the experts and over the 128-token tiles), every output column
+    and every element of their h rows against the oracle."""
+    import torch
     cfg = synth.CONFIGS["mixtral_prefill"]
     m = gpu_layer(cfg)
     x, L = synth.tokens(cfg), synth.logits(cfg)
-    out, ri, rw, ro, rp = _run(m, cfg, x, L)
+    ws = m.workspace(cfg.T, cfg.top_k)
+    out, ri, rw, ro, rp = m.pw_moe_forward(0, torch.from_numpy(x).cuda(), torch.from_numpy(L).cuda(),
+                                           cfg.top_k, cfg.renorm, ws=ws, routing=True)
+    torch.cuda.synchronize()
     rng = np.random.default_rng(6)
-    toks = np.sort(rng.choice(cfg.T, size=12, replace=False))
-    cols = np.sort(rng.choice(cfg.H, size=64, replace=False))
+    toks = np.sort(rng.choice(cfg.T, size=32, replace=False))
     ref = omoe.layer(x, L, cfg.top_k, cfg.renorm, oracle_blocks(SynthBlocks(cfg, 0), synth.block_bits(cfg)),
-                     out_rows=cols, out_tokens=toks)
-    _check_routing(ref, ri, rw, ro, rp)
-    assert_close(out[toks][:, cols], ref["out"])
+                     out_tokens=toks)
+    _check_routing(ref, to_np(ri), to_np(rw), to_np(ro), to_np(rp))
+    assert_close(to_np(out)[toks], ref["out"])
+    pos = np.sort(ref["inv"].reshape(cfg.T, cfg.top_k)[toks].ravel())   # the sampled tokens' pairs
+    h = to_np(m.workspace_h(ws, cfg.T, cfg.top_k)).astype(np.float64)
+    assert_close(h[pos], ref["h"][pos])
 
 
 def test_prefill_gemm_integer_tables_bit_exact():
