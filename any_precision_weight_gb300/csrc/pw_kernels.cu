@@ -7,8 +7,9 @@
 // of experts per token).
 //
 // Pipeline of one forward pass, all on the caller's stream:
-//   k_route_permute  one CTA: top-k softmax routing per token, stable counting
-//                    sort of the (token, slot) pairs by expert, active list;
+//   k_route          top-k softmax routing, one warp per token over the grid;
+//   k_permute        one CTA: stable counting sort of the (token, slot) pairs
+//                    by expert, offsets, active list;
 //   gate_up          per active expert: dequantised gate/up rows . x, then
 //                    h = silu(gate) * up (fp16);
 //   down             per active expert: dequantised down rows . h (fp32 y);
@@ -51,13 +52,27 @@ cudaError_t launch_commit_batch(BlockDesc* table, const CommitBatch& b, cudaStre
 
 // ------------------------------------------------------------------ routing + permutation
 
-constexpr int kRouteThreads = 1024;
-__global__ void __launch_bounds__(kRouteThreads) k_route_permute(Fwd p) {
-  __shared__ int s_cnt[kMaxE];
+// Routing of a large batch: one warp per token over the whole grid, results
+// into the workspace (idx, w).  The status word was cleared before the launch;
+// a NaN logit ORs PW_STATUS_NAN_LOGIT into it.
+constexpr int kRouteWarps = 8;
+template <int NPER>
+__global__ void __launch_bounds__(kRouteWarps * 32) k_route(Fwd p) {
+  static_assert(PW_STATUS_NAN_LOGIT == 1, "route_tokens ORs 1");
+  RouteSmem r{};
+  r.idx = p.idx;
+  r.w = p.w;
+  const int gw = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
+  route_tokens<NPER>(p, r, reinterpret_cast<int*>(p.status), gw, gridDim.x * kRouteWarps);
+}
+
+// Counts, offsets, perm / inv of the routed pairs (one CTA), then the routing
+// statistics.
+constexpr int kPermuteThreads = 1024;
+__global__ void __launch_bounds__(kPermuteThreads) k_permute(Fwd p) {
+  __shared__ int s_c[kPermuteThreads / 32][kMaxE];
   __shared__ int s_off[kMaxE + 1];
-  if (threadIdx.x == 0) p.status[0] = 0u;
-  __syncthreads();
-  route_permute_block(p, s_cnt, s_off);
+  permute_block(p, s_c, s_off);
   if (p.stats) {
     __syncthreads();
     update_route_stats(p, p.perm, p.w, p.offsets);
@@ -128,7 +143,14 @@ cudaError_t launch_forward(const ForwardArgs& a, cudaStream_t s) {
     for (int i = 1; i < 5; ++i) mark(a, i, s);
     return e;
   }
-  k_route_permute<<<1, kRouteThreads, 0, s>>>(p);
+  cudaError_t e0 = cudaMemsetAsync(p.status, 0, sizeof(uint32_t), s);
+  if (e0 != cudaSuccess) return e0;
+  const dim3 rgrid((p.T + kRouteWarps - 1) / kRouteWarps);
+  if (p.E <= 32) k_route<1><<<rgrid, kRouteWarps * 32, 0, s>>>(p);
+  else if (p.E <= 64) k_route<2><<<rgrid, kRouteWarps * 32, 0, s>>>(p);
+  else if (p.E <= 128) k_route<4><<<rgrid, kRouteWarps * 32, 0, s>>>(p);
+  else k_route<8><<<rgrid, kRouteWarps * 32, 0, s>>>(p);
+  k_permute<<<1, kPermuteThreads, 0, s>>>(p);
   mark(a, 1, s);
   cudaError_t e = launch_prefill(p, PW_KIND_GATE_UP, s);
   if (e != cudaSuccess) return e;

@@ -10,103 +10,59 @@
 namespace pw {
 
 constexpr int kMaxE = 256;
-constexpr int kPerLane = kMaxE / 32;
 
 // Order of the top-k: larger logit first, ties to the lower expert index.
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
-// Routing and permutation of the whole batch by one CTA (any block size that is
-// a multiple of 32).  Phase 1: warp per token, top-k over the fp32 logits and
-// softmax weights.  Phase 2: per-expert counts and offsets.  Phase 3: warp per
-// expert, ballot ranks give the stable (expert, token) order.  s_cnt / s_off:
-// shared scratch of kMaxE and kMaxE + 1 ints.  The caller resets the status word.
-__device__ __forceinline__ void route_permute_block(const Fwd& p, int* s_cnt, int* s_off) {
+// Stable placement of a large batch's routed pairs by one CTA (blockDim.x a
+// multiple of 32, at most 1024): per-expert counts, offsets, the active list,
+// and perm / inv in (expert, token) order.  Warp w owns a contiguous chunk of
+// the pair ids t*k + j (a token has distinct experts, so pair-id order within
+// an expert is token order): it counts its chunk's pairs per expert, the
+// per-expert counts of the chunks are scanned into each chunk's first
+// position, and the warp places its pairs 32 at a time, a pair's rank among
+// the lanes holding the same expert coming from a match.  s_c: shared
+// [32][kMaxE] ints; s_off: shared kMaxE + 1 ints.  idx must be complete.
+__device__ __forceinline__ void permute_block(const Fwd& p, int (*s_c)[kMaxE], int* s_off) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
-  const int E = p.E, k = p.k, T = p.T;
-
-  for (int t = warp; t < T; t += nwarp) {
-    float v[kPerLane];
-    bool taken[kPerLane];
-    bool nan_seen = false;
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i) {
-      const int e = lane + 32 * i;
-      float z = -INFINITY;
-      if (e < E) {
-        z = p.logits[static_cast<size_t>(t) * E + e];
-        if (isnan(z)) { nan_seen = true; z = -INFINITY; }
-      }
-      v[i] = z;
-      taken[i] = (e >= E);
+  const int E = p.E, P = p.T * p.k;
+  const int chunk = (P + nwarp - 1) / nwarp;
+  const int q0 = min(P, warp * chunk), q1 = min(P, q0 + chunk);
+  for (int e = lane; e < E; e += 32) s_c[warp][e] = 0;
+  __syncwarp();
+  for (int q = q0 + lane; q < q1; q += 32) atomicAdd(&s_c[warp][p.idx[q]], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {   // chunk bases within the expert, and its count
+    int run = 0;
+    for (int w = 0; w < nwarp; ++w) {
+      const int c = s_c[w][e];
+      s_c[w][e] = run;
+      run += c;
     }
-    if (__any_sync(0xffffffffu, nan_seen) && lane == 0) atomicOr(p.status, PW_STATUS_NAN_LOGIT);
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i) m = fmaxf(m, v[i]);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i)
-      if (lane + 32 * i < E) s += expf(v[i] - m);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    float wsum = 0.f, wsel = 0.f;
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < kPerLane; ++i)
-        if (!taken[i] && better(v[i], lane + 32 * i, bv, bi)) { bv = v[i]; bi = lane + 32 * i; }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-      }
-#pragma unroll
-      for (int i = 0; i < kPerLane; ++i)
-        if (lane + 32 * i == bi) taken[i] = true;
-      const float wj = expf(bv - m) / s;
-      wsum += wj;
-      if ((j & 31) == lane) wsel = wj;
-      if (lane == 0) p.idx[t * k + j] = bi;
-      if ((j & 31) == 31 || j == k - 1) {   // flush slots [j & ~31, j]
-        const int js = (j & ~31) + lane;
-        if (js <= j) p.w[t * k + js] = wsel;
-      }
-    }
-    if (p.renorm) {
-      __syncwarp();
-      for (int j = lane; j < k; j += 32) p.w[t * k + j] /= wsum;
-    }
+    s_off[e] = run;
+    p.counts[e] = run;
   }
   __syncthreads();
-
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = 0;
-  __syncthreads();
-  for (int i = threadIdx.x; i < T * k; i += blockDim.x) atomicAdd(&s_cnt[p.idx[i]], 1);
-  __syncthreads();
-  if (threadIdx.x < 32) {   // warp-level exclusive scan of counts and of the active flags
+  if (threadIdx.x < 32) {   // warp-level exclusive scan of the counts and of the active flags
     int run = 0, na = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
       const int e = e0 + threadIdx.x;
-      const int c = e < E ? s_cnt[e] : 0;
-      int incl = c, act = c > 0;
+      const int c = e < E ? s_off[e] : 0;
+      int incl = c, actv = c > 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        const int a = __shfl_up_sync(0xffffffffu, act, o);
-        if (threadIdx.x >= o) { incl += v; act += a; }
+        const int a = __shfl_up_sync(0xffffffffu, actv, o);
+        if (threadIdx.x >= o) { incl += v; actv += a; }
       }
       if (e < E) {
         s_off[e] = run + incl - c;
-        if (c) p.active[1 + na + act - 1] = e;
+        if (c) p.active[1 + na + actv - 1] = e;
       }
       run += __shfl_sync(0xffffffffu, incl, 31);
-      na += __shfl_sync(0xffffffffu, act, 31);
+      na += __shfl_sync(0xffffffffu, actv, 31);
     }
     if (threadIdx.x == 0) {
       s_off[E] = run;
@@ -117,28 +73,28 @@ __device__ __forceinline__ void route_permute_block(const Fwd& p, int* s_cnt, in
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     p.offsets[e] = s_off[e];
     if (p.user_offsets) p.user_offsets[e] = s_off[e];
-    if (e < E) p.counts[e] = s_cnt[e];
   }
-  for (int e = warp; e < E; e += nwarp) {
-    int run = 0;
-    for (int base = 0; base < T; base += 32) {
-      const int t = base + lane;
-      int jsel = -1;
-      if (t < T)
-        for (int j = 0; j < k; ++j)
-          if (p.idx[t * k + j] == e) jsel = j;
-      const unsigned mask = __ballot_sync(0xffffffffu, jsel >= 0);
-      if (jsel >= 0) {
-        const int pos = s_off[e] + run + __popc(mask & ((1u << lane) - 1u));
-        p.perm[pos] = t * k + jsel;
-        p.inv[t * k + jsel] = pos;
-        if (p.user_perm) p.user_perm[pos] = t * k + jsel;
-      }
-      run += __popc(mask);
+  for (int i = threadIdx.x; i < nwarp * E; i += blockDim.x) s_c[i / E][i % E] += s_off[i % E];
+  __syncthreads();
+  for (int b = q0; b < q1; b += 32) {
+    const int q = b + lane;
+    const bool v = q < q1;
+    const unsigned act = __ballot_sync(0xffffffffu, v);
+    if (v) {
+      const int e = p.idx[q];
+      const unsigned same = __match_any_sync(act, e);
+      const int rank = __popc(same & ((1u << lane) - 1u));
+      const int pos = s_c[warp][e] + rank;
+      p.perm[pos] = q;
+      p.inv[q] = pos;
+      if (p.user_perm) p.user_perm[pos] = q;
+      __syncwarp(act);   // every lane has read its expert's base
+      if (rank == 0) s_c[warp][e] += __popc(same);
     }
+    __syncwarp();
   }
   if (p.user_idx || p.user_w)
-    for (int i = threadIdx.x; i < T * k; i += blockDim.x) {
+    for (int i = threadIdx.x; i < P; i += blockDim.x) {
       if (p.user_idx) p.user_idx[i] = p.idx[i];
       if (p.user_w) p.user_w[i] = p.w[i];
     }
@@ -163,17 +119,15 @@ __host__ __device__ constexpr int route_smem_bytes() {
   return (4 * kRouteSmemMaxPairs + 5 * (kMaxE + 1)) * 4;
 }
 
-// Every CTA of the fused layer computes the same routing on its own (it is a
-// few hundred logits), so no CTA waits for another's results.  Same order of
-// results as route_permute_block.  A NaN logit sets *nan_flag (shared memory);
-// the caller raises the status bit.  Needs T*k <= kRouteSmemMaxPairs and a block of >= 32 threads.
-// Top-k and softmax weights of the tokens t = warp, warp + nwarp, ... with
-// NPER logits per lane (E <= 32 * NPER); results into r.idx / r.w.
+// Top-k (larger logit first, ties to the lower expert index) and softmax
+// weights over all E of the tokens t0, t0 + tstep, ..., one warp per token,
+// with NPER logits per lane (E <= 32 * NPER); results into r.idx / r.w (shared
+// or global memory).  A NaN logit counts as -inf and ORs 1 into *nan_flag.
 template <int NPER>
-__device__ __forceinline__ void route_tokens(const Fwd& p, const RouteSmem& r, int* nan_flag) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+__device__ __forceinline__ void route_tokens(const Fwd& p, const RouteSmem& r, int* nan_flag, int t0, int tstep) {
+  const int lane = threadIdx.x & 31;
   const int E = p.E, k = p.k, T = p.T;
-  for (int t = warp; t < T; t += nwarp) {
+  for (int t = t0; t < T; t += tstep) {
     float v[NPER];
     bool taken[NPER];
     bool nan_seen = false;
@@ -229,6 +183,10 @@ __device__ __forceinline__ void route_tokens(const Fwd& p, const RouteSmem& r, i
   }
 }
 
+// Routing of a decode batch into one CTA's shared memory: top-k and weights,
+// counts, offsets, the active experts (in expert order and by gate_up cost,
+// largest first), perm / inv.  Needs T*k <= kRouteSmemMaxPairs.  A NaN logit
+// sets *nan_flag (shared memory); the caller raises the status bit.
 __device__ __forceinline__ void route_local(const Fwd& p, const RouteSmem& r, int* nan_flag,
                                             int tok_cost) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
@@ -244,10 +202,12 @@ __device__ __forceinline__ void route_local(const Fwd& p, const RouteSmem& r, in
     qv[j] = e < E ? p.desc[desc_index(p.layer, e, PW_KIND_GATE_UP, E)].q : 0;
   }
   for (int e = threadIdx.x; e < E; e += nthr) r.cnt[e] = 0;
-  if (E <= 32) route_tokens<1>(p, r, nan_flag);
-  else if (E <= 64) route_tokens<2>(p, r, nan_flag);
-  else if (E <= 128) route_tokens<4>(p, r, nan_flag);
-  else route_tokens<8>(p, r, nan_flag);
+  // every CTA of the fused layer routes the whole batch on its own (a few
+  // hundred logits), so no CTA waits for another's results
+  if (E <= 32) route_tokens<1>(p, r, nan_flag, warp, nwarp);
+  else if (E <= 64) route_tokens<2>(p, r, nan_flag, warp, nwarp);
+  else if (E <= 128) route_tokens<4>(p, r, nan_flag, warp, nwarp);
+  else route_tokens<8>(p, r, nan_flag, warp, nwarp);
 #pragma unroll
   for (int j = 0; j < kQPer; ++j) {
     const int e = threadIdx.x + j * nthr;

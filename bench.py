@@ -357,7 +357,7 @@ def kernel_times(cfg, evs):
     fused = is_fused(cfg)
     if fused:
         return {"layer_fused": sum(r[0].elapsed_time(r[1]) for r in evs) / len(evs)}
-    names = ["route_permute", "gate_up", "down", "combine"]
+    names = ["route_permute", "gate_up", "down", "combine"]   # route_permute: routing + permutation launches
     return {nm: sum(r[j].elapsed_time(r[j + 1]) for r in evs) / len(evs) for j, nm in enumerate(names)}
 
 
@@ -595,7 +595,7 @@ def run_ours(args, cfg, rank, world, local):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4,
                 "d2h_bytes_per_step": cfg.T * cfg.H * 2 + 4},
-        "gpu_launches": (1 if is_fused(cfg) else 5) * args.steps,
+        "gpu_launches": (1 if is_fused(cfg) else 6) * args.steps,   # route, permute, gather, two GEMMs, combine
         "clocks": r["clocks"],
         "wall_s": r["wall_s"],
         "per_config": per,
