@@ -753,6 +753,18 @@ def measure_stack(args, cfg, dev, local, world, steps):
             ev[i + 1].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - w0
+        # a window longer than the run: its remaining blocks committed untimed,
+        # so that the next window starts from the same state
+        t_drain = time.perf_counter()
+        while committed < len(items):
+            c, left = m.pw_commit_arrived()
+            committed += c
+            if left == 0 and committed >= len(items):
+                break
+            if time.perf_counter() - t_drain > 120:
+                raise RuntimeError("stack reload did not complete within 120 s")
+            time.sleep(0.001)
+        torch.cuda.synchronize()
         t = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(n)])
         copy_ms = c0.elapsed_time(c1) if landed else None
         before, during, after = t[:reload_at], t[reload_at:last + 1], t[last + 1:]
@@ -761,7 +773,8 @@ def measure_stack(args, cfg, dev, local, world, steps):
             "tokens_per_s_before": tps(before), "tokens_per_s_during": tps(during),
             "tokens_per_s_after": tps(after),
             "loss_pct_during": (1 - tps(during) / tps(before)) * 100 if len(during) and len(before) else None,
-            "last_commit_step": last, "committed": committed, "submit_to_last_commit_ms": copy_ms,
+            "last_commit_step": last, "committed": committed, "window_within_run": landed,
+            "submit_to_last_commit_ms": copy_ms,
             "reload_gbs": reload_bytes / (copy_ms / 1e3) / 1e9 if copy_ms else None,
             "ms_total": float(t.sum()), "before_ms_per_step": float(before.mean()) if len(before) else None,
             "after_ms_per_step": float(after.mean()) if len(after) else None,
