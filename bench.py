@@ -66,6 +66,12 @@ def parse():
     ap.add_argument("--reload-inflight-mb", type=int, default=64,
                     help="stack workload: bound on the mover's copies in flight")
     ap.add_argument("--stack-reps", type=int, default=3, help="stack workload: reload windows measured")
+    ap.add_argument("--read-store-first", action="store_true",
+                    help="stack workload: copy the whole pinned host store to the GPU once before measuring "
+                         "(checks whether the first reload window is slow because its host pages are read for "
+                         "the first time)")
+    ap.add_argument("--eager-steps", action="store_true",
+                    help="stack workload: launch each step's 48 kernels from Python instead of one CUDA graph")
     ap.add_argument("--independent-logits", action="store_true",
                     help="stack workload: precomputed logits (lets consecutive layers overlap)")
     return ap.parse_args()
@@ -641,7 +647,7 @@ def measure_stack(args, cfg, dev, local, world, steps):
     copy = torch.cuda.Stream(device=dev)
     dependent = not args.independent_logits
 
-    def step(i):
+    def step_body(i):
         x = X0[i % len(X0)]
         for l in range(L):
             o = bufs[l & 1]
@@ -673,6 +679,34 @@ def measure_stack(args, cfg, dev, local, world, steps):
     reload_at = min(args.reload_at, n - 1)
     m.pw_mover_start(copy, max_inflight_bytes=args.reload_inflight_mb << 20)
     for i in range(3):
+        step_body(i)
+    torch.cuda.synchronize()
+    # One CUDA graph per token set holds a whole step (the 24 layers' logits
+    # kernels and forwards), so a step costs the host one launch: with 48
+    # launches from Python a step takes about 1 ms of host time against 1.4 ms
+    # of GPU time, and the mover's copy calls during a reload window then make
+    # the host, not the GPU, the bottleneck.  Commits stay outside the graphs
+    # (the forwards read the descriptors when they run).
+    graphs, launch_mode = [], "eager (48 launches per step from Python)"
+    if not args.eager_steps:
+        try:
+            for j in range(len(X0)):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    step_body(j)
+                graphs.append(g)
+            torch.cuda.synchronize()
+            launch_mode = "one CUDA graph per step"
+        except Exception as ex:   # capture refused: measure the eager loop
+            graphs, launch_mode = [], f"eager (graph capture failed: {str(ex)[:120]})"
+            torch.cuda.synchronize()
+
+    def step(i):
+        if graphs:
+            graphs[i % len(graphs)].replay()
+        else:
+            step_body(i)
+    for i in range(3):
         step(i)
     torch.cuda.synchronize()
     # host->device rate of plain copies from the pinned store on the copy stream:
@@ -703,6 +737,17 @@ def measure_stack(args, cfg, dev, local, world, steps):
     probe["h2d_beside_decode_gbs"] = chunk.numel() / (p0.elapsed_time(p1) / 1e3) / 1e9
     probe["probe_bytes"] = chunk.numel()
     torch.cuda.synchronize()
+    try:
+        probe["host_page_bytes"] = os.sysconf("SC_PAGE_SIZE")
+        probe["thp"] = open("/sys/kernel/mm/transparent_hugepage/enabled").read().strip()
+    except Exception:
+        pass
+    if args.read_store_first:
+        t_rd = time.perf_counter()
+        for c in store._chunks:
+            dbuf[:c.numel()].copy_(c, non_blocking=True)
+        torch.cuda.synchronize()
+        probe["store_read_first_gbs"] = store.nbytes() / (time.perf_counter() - t_rd) / 1e9
     del dbuf
     clocks = Clocks(local)
     clocks.start()
@@ -733,10 +778,12 @@ def measure_stack(args, cfg, dev, local, world, steps):
         landed = False
         w0 = time.perf_counter()
         ev[0].record(stream)
+        enq = np.zeros(n)                    # host seconds spent enqueueing each step
         for i in range(n):
             if i >= 2:
                 ev[i - 1].synchronize()      # at most two steps in flight, as a decode loop that
                                              # needs step i-2's tokens before launching step i
+            h0 = time.perf_counter()
             if i == reload_at:
                 c0.record(copy)
                 m.pw_mover_submit(items)
@@ -751,6 +798,7 @@ def measure_stack(args, cfg, dev, local, world, steps):
                     landed = True
             step(3 + i)
             ev[i + 1].record(stream)
+            enq[i] = time.perf_counter() - h0
         torch.cuda.synchronize()
         wall = time.perf_counter() - w0
         # a window longer than the run: its remaining blocks committed untimed,
@@ -778,7 +826,9 @@ def measure_stack(args, cfg, dev, local, world, steps):
             "reload_gbs": reload_bytes / (copy_ms / 1e3) / 1e9 if copy_ms else None,
             "ms_total": float(t.sum()), "before_ms_per_step": float(before.mean()) if len(before) else None,
             "after_ms_per_step": float(after.mean()) if len(after) else None,
-            "commit_launches": commit_launches, "wall_s": wall})
+            "commit_launches": commit_launches, "wall_s": wall,
+            "host_enqueue_ms_before": float(enq[:reload_at].mean() * 1e3),
+            "host_enqueue_ms_during": float(enq[reload_at:last + 1].mean() * 1e3)})
     clk = clocks.stop()
     losses = [r["loss_pct_during"] for r in reps if r["loss_pct_during"] is not None]
     gbs = [r["reload_gbs"] for r in reps if r["reload_gbs"]]
@@ -793,7 +843,10 @@ def measure_stack(args, cfg, dev, local, world, steps):
                             else "precomputed (the forwards may overlap)",
                   "reload_at_step": reload_at, "reloaded_blocks": len(plan), "reload_bytes": reload_bytes,
                   "mover": f"native mover thread, at most {args.reload_inflight_mb} MiB of copies in flight",
+                  "step_launch": launch_mode,
                   "loss_pct_during_mean": float(np.mean(losses)) if losses else None,
+                  "loss_pct_first_window": losses[0] if losses else None,
+                  "loss_pct_later_windows_mean": float(np.mean(losses[1:])) if len(losses) > 1 else None,
                   "loss_pct_during_min": float(np.min(losses)) if losses else None,
                   "loss_pct_during_max": float(np.max(losses)) if losses else None,
                   "reload_gbs_mean": float(np.mean(gbs)) if gbs else None,
