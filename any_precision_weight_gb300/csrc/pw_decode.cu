@@ -738,6 +738,28 @@ __device__ bool wait_published(const Fwd& p) {
   return false;
 }
 
+// A CTA's end of the forward (thread 0), in the build for captured CUDA
+// graphs: it counts itself out, and the last CTA clears the ticket word, after
+// every CTA's last ticket claim (each claim precedes its CTA's count).  The
+// next forward on this workspace then sets up even when it carries the same
+// tag, as the replays of one captured forward do.  (Eager calls take a new tag
+// each and skip this: it costs about 1.5 % of a Mixtral-shaped layer.)
+__device__ __noinline__ void leave_forward(unsigned long long* sync, unsigned long long tag, int n_counters,
+                                           bool published) {
+  for (int i = 0; !published && i < kSpinLimit; ++i) {   // as wait_published
+    const unsigned long long v = ld_acquire_u64(sync);
+    published = (v & ~kCountMask) == tag && !(v & kSetupBit);
+    if (!published) __nanosleep(64);
+  }
+  if (!published) return;   // no set-up was seen: the counters are not this forward's
+  int* exit_count = reinterpret_cast<int*>(sync + 1) + n_counters;
+  __threadfence();
+  if (atomicAdd(exit_count, 1) == static_cast<int>(gridDim.x) - 1) {
+    __threadfence();
+    st_release_u64(sync, 0ull);
+  }
+}
+
 // Combine of one 64-row output tile once all its down items are done (the
 // whole CTA): when the down items write parts (a workspace with room for a
 // K-split), y = the ks parts added in split order (written to y for
@@ -770,7 +792,7 @@ __device__ void combine_tile(const Fwd& p, const RouteSmem& r, int tile, int ks,
 // whichever CTAs are resident.  The last down item of a 64-row output tile
 // combines it.  Every wait is bounded and reports PW_STATUS_TIMEOUT instead of
 // hanging.
-template <bool kPairs>
+template <bool kPairs, bool kGraph>
 __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const Smem sm = smem_layout();
@@ -795,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   pl.tiles_gu = p.I / kGateUpTileRows;
   pl.tiles_dn = p.H / kDownTileRows;
   int* expert_done = reinterpret_cast<int*>(p.sync + 1);
-  int* tile_done = expert_done + p.E;
+  int* tile_done = expert_done + p.E;   // then the count of CTAs that finished this forward
 
   // The launch lets the next forward on the stream start on SMs this grid frees
   // (programmatic dependent launch): that forward routes its own batch while
@@ -867,7 +889,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   if (role == 1) {
     // this CTA sets the forward up: counters to zero, the status word, then the
     // set-up bit cleared (tickets 0 and 1 are this CTA's)
-    for (int i = tid; i < p.E + pl.tiles_dn; i += kThreads) expert_done[i] = 0;
+    for (int i = tid; i < p.E + pl.tiles_dn + 1; i += kThreads) expert_done[i] = 0;   // and the exit count
     if (tid == 0) p.status[0] = s_int[0] ? PW_STATUS_NAN_LOGIT : 0u;
     __syncthreads();
     if (tid == 0) {
@@ -887,7 +909,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
     update_route_stats(p, r.perm, r.w, r.off);
   } else if (role < 0) {
     // the ticket word never settled (bounded): leave every item to the others
-    if (tid == 0 && wait_published(p)) atomicOr(p.status, PW_STATUS_TIMEOUT);
+    if (tid == 0 && wait_published(p)) {
+      atomicOr(p.status, PW_STATUS_TIMEOUT);
+      if (kGraph) leave_forward(p.sync, p.tag, p.E + pl.tiles_dn, true);
+    }
     return;
   }
   __syncthreads();
@@ -1085,6 +1110,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_layer(Fwd p) {
   if (tid == 0) s_int[1] = pending_old == pl.down_per_tile - 1 ? pending_tile : -1;
   __syncthreads();
   if (s_int[1] >= 0) combine_tile(p, r, s_int[1], pl.ks, tid);
+  if (kGraph && tid == 0) leave_forward(p.sync, p.tag, p.E + pl.tiles_dn, published);
   cp_wait<0>();
 }
 
@@ -1108,20 +1134,28 @@ cudaError_t launch_layer_fused(const Fwd& p, cudaStream_t s) {
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (p.H % kDownTileRows != 0 || p.I % kGateUpTileRows != 0) return cudaErrorInvalidValue;
   if (g_fused[dev] == 0) {   // once per device: shared-memory opt-in and co-resident grid size
-    e = cudaFuncSetAttribute(k_layer<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_layer<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    int per_sm = 0, per_sm1 = 0, sms = 0;
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_layer<true>, kThreads, kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm1, k_layer<false>, kThreads, kSmemBytes);
-    per_sm = per_sm < per_sm1 ? per_sm : per_sm1;
+    const void* fns[4] = {reinterpret_cast<const void*>(k_layer<true, false>),
+                          reinterpret_cast<const void*>(k_layer<false, false>),
+                          reinterpret_cast<const void*>(k_layer<true, true>),
+                          reinterpret_cast<const void*>(k_layer<false, true>)};
+    int per_sm = 1 << 30, sms = 0;
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i) {
+      e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      int n = 0;
+      if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fns[i], kThreads, kSmemBytes);
+      per_sm = n < per_sm ? n : per_sm;
+    }
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     g_fused[dev] = per_sm * sms;
   }
+  // A call being captured into a CUDA graph gets the build that clears the
+  // ticket word at its end (its replays repeat the capture's tag).
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(s, &cap);
+  if (e != cudaSuccess) return e;
+  const bool graph = cap != cudaStreamCaptureStatusNone;
   // An ordinary launch of the co-resident grid (items are handed out by
   // tickets, so the waits end even when only some CTAs are resident), allowed
   // to start while the previous kernel on the stream finishes (programmatic
@@ -1137,7 +1171,9 @@ cudaError_t launch_layer_fused(const Fwd& p, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return p.H >= kPairsMinH ? cudaLaunchKernelEx(&cfg, k_layer<true>, p) : cudaLaunchKernelEx(&cfg, k_layer<false>, p);
+  if (p.H >= kPairsMinH)
+    return graph ? cudaLaunchKernelEx(&cfg, k_layer<true, true>, p) : cudaLaunchKernelEx(&cfg, k_layer<true, false>, p);
+  return graph ? cudaLaunchKernelEx(&cfg, k_layer<false, true>, p) : cudaLaunchKernelEx(&cfg, k_layer<false, false>, p);
 }
 
 }  // namespace pw

@@ -45,7 +45,7 @@ struct Workspace {
   size_t inv;        // int32 [T*k]
   size_t active;     // int32 [2][E+1]: active experts (count, ids); same, cost-sorted
   size_t sync;       // fused path: 64-bit ticket word, then int32 gate_up items done per
-                     // expert and down items done per 64-row tile of H
+                     // expert, down items done per 64-row tile of H, CTAs finished
   size_t hh;         // fp16 [T*k][I] in perm order
   size_t xp;         // fp16 [T*k][H] token rows in perm order (prefill GEMMs)
   size_t y;          // f32 [T*k][H] in perm order
@@ -87,7 +87,7 @@ inline Workspace workspace_layout(int T, int E, int k, int H, int I) {
   w.perm = take(P * 4);
   w.inv = take(P * 4);
   w.active = take(static_cast<size_t>(E + 1) * 2 * 4);
-  w.sync = take(8 + static_cast<size_t>(E + (H + 63) / 64) * 4);
+  w.sync = take(8 + static_cast<size_t>(E + (H + 63) / 64 + 1) * 4);
   w.hh = take(P * I * 2);
   w.xp = take(P * H * 2);
   w.y = take(P * H * 4);

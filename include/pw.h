@@ -451,13 +451,11 @@ size_t pw_workspace_offset(int T, int E, int top_k, int H, int I, int section);
  * tickets in dependency order, so it finishes correctly even while another
  * kernel holds some of the SMs.
  * Each decode-sized call takes a new forward tag on the host, and the kernel
- * tells a new forward from the previous one on the same workspace by that tag.
- * A CUDA graph replays captured calls with the tags of their capture, so one
- * captured decode-sized call must not follow its own previous replay on the
- * same workspace directly: a forward with another tag must have used the
- * workspace in between (a captured stack of two or more layers that share one
- * workspace does so by itself).  Otherwise the second replay reuses the first
- * one's counters and its output is wrong.
+ * sets a forward up when the workspace's ticket word holds another tag.  A
+ * call made while `compute` is being captured into a CUDA graph launches a
+ * build of the kernel whose last CTA clears that word, so the graph may replay
+ * the captured call (with the tag of its capture) any number of times in a row
+ * on the same workspace.
  * PW_OK means only that the work was enqueued.  What happens on the device (a
  * NaN logit, a bounded device-side wait that ran out, an unusable block
  * descriptor) is reported only through the workspace status word: read it with

@@ -121,3 +121,28 @@ def test_forward_beside_a_kernel_holding_half_the_sms(name):
         assert int(done.item()) == (rep + 1) * (sms // 2)
         assert m.workspace_status(ws) == 0
         assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen_decode"])
+def test_graph_replays_of_one_forward(name):
+    """One decode forward captured in a CUDA graph and replayed four times in a
+    row on the same workspace (every replay carries the tag of the capture):
+    each replay equals an eager forward bit for bit, with no status bit."""
+    import torch
+    cfg = synth.CONFIGS[name]
+    m = gpu_layer(cfg)
+    x, L = _inputs(cfg, step=31)
+    ws = m.workspace(cfg.T, cfg.top_k)
+    ref = m.pw_moe_forward(0, x, L, cfg.top_k, cfg.renorm, ws=ws).clone()
+    out = torch.empty_like(x)
+    m.pw_moe_forward(0, x, L, cfg.top_k, cfg.renorm, out=out, ws=ws)   # warm the launch path
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        m.pw_moe_forward(0, x, L, cfg.top_k, cfg.renorm, out=out, ws=ws)
+    for _ in range(4):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+        assert m.workspace_status(ws) == 0
