@@ -23,6 +23,9 @@ overlapping through programmatic dependent launch) is reported beside it,
 labelled.  ``per_q`` sweeps every block of the layer through uniform
 bitwidths 3..8 (a commit, no reload).  ``per_config`` measures the other
 workloads of the list the same way in the same run, each with its clocks.
+The 24-layer stack replays each step as one CUDA graph and reloads a quarter
+of its lower-bit blocks mid-run (tokens/s before, during and after each
+reload window).
 
 Multi-GPU (torchrun): the layer does not shard here, so every rank runs an
 independent replica ("scaling": "weak"); value = all ranks' tokens / the
